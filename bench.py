@@ -1,0 +1,416 @@
+"""Benchmark of the HiSA decode step (score + select + attend) on GB300.
+
+Workload: R independent V4-Flash-shaped decode queries per step (each: Np = 32768
+pooled rows of a 131072-token prefix, H_i = 64 x D_i = 128 indexer, index_block = 64,
+keep = 16, index_topk = 512, 64 query heads x Dh = 512, window 128, bf16 keys / KV,
+f32 indexer q). One step = the newest block mean of every sequence, the coarse block
+filter, the fine top-k and the sparse combine: four C-ABI calls, each replayed from its
+own CUDA graph, with CUDA events between them on the launching stream.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from deepseek_sparse_attention_hisa_gb300 import inputs  # noqa: E402
+
+METRIC = "HiSA decode queries/s (score+select+attend) and HBM GB/s vs GB300 peak"
+UNIT = "queries/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes per decode query (V4-Flash shape), by stage
+# ----------------------------------------------------------------------------
+def stage_bytes(wl, nb):
+    H_i, D_i, b, keep, k, H, Dh, W = (wl.H_i, wl.D_i, wl.index_block, wl.index_keep,
+                                      wl.index_topk, wl.H, wl.Dh, wl.window)
+    q_idx = H_i * D_i * 4
+    w = H_i * 4
+    means = b * D_i * 2 + D_i * 4                        # newest block: read b keys, write 1 mean
+    filt = q_idx + w + nb * D_i * 4 + keep * 4           # q, w, all block means, top_blk
+    sel = q_idx + w + keep * b * D_i * 2 + keep * 4 + k * 4   # q, w, kept blocks' keys, top_blk, I
+    att = H * Dh * 2 + W * Dh * 2 + k * Dh * 2 + k * 4 + H * 4 + H * Dh * 4  # q, local, gathered, I, sinks, out
+    # unique bytes of the whole step: q/w and I/top_blk counted once
+    step = means + q_idx + w + nb * D_i * 4 + keep * b * D_i * 2 + H * Dh * 2 + W * Dh * 2 + \
+        k * Dh * 2 + H * 4 + H * Dh * 4 + k * 4 + keep * 4
+    return dict(block_means=means, block_filter=filt, select_topk=sel, sparse_attend=att), step
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+def host_copy_of_sequence(data, b):
+    """Host numpy copy of sequence b of a device-drawn batch (bf16 -> uint16 bits)."""
+    import torch
+
+    def h(t):
+        t = t.detach().cpu()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()
+    k0, k1 = int(data["key_off"][b]), int(data["key_off"][b + 1])
+    return dict(q_idx=h(data["q_idx"][b, 0]), w=h(data["w"][b, 0]), keys=h(data["keys"][k0:k1]),
+                q_attn=h(data["q_attn"][b]), local_kv=h(data["local_kv"][b]),
+                local_pos0=int(data["local_pos0"][b]), pooled_kv=h(data["pooled_kv"][k0:k1]),
+                sinks=h(data["sinks"]), t0=int(data["t0"][b]))
+
+
+def oracle_query(wl, s):
+    from oracle import hisa_oracle as O
+    d = O.hisa_select_decode(s["q_idx"], s["w"], s["keys"], wl.index_block, wl.index_keep,
+                             wl.index_topk)
+    O.sparse_combine(s["q_attn"], s["local_kv"], s["local_pos0"], s["pooled_kv"], d["I"][None],
+                     s["sinks"], s["t0"], wl.r, wl.window)
+
+
+def time_oracle(wl, samples, budget_s):
+    n = 0
+    t_start = time.perf_counter()
+    while True:
+        oracle_query(wl, samples[n % len(samples)])
+        n += 1
+        el = time.perf_counter() - t_start
+        if el >= budget_s:
+            break
+    return n, el
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def host_samples(wl, n):
+    """n sequences drawn on the host (the oracle's input), same recipe as the batch."""
+    one = wl.replace(B=n)
+    data = inputs.generate(one)
+    out = []
+    for b in range(n):
+        k0, k1 = int(data["key_off"][b]), int(data["key_off"][b + 1])
+        out.append(dict(q_idx=data["q_idx"][b, 0], w=data["w"][b, 0], keys=data["keys"][k0:k1],
+                        q_attn=data["q_attn"][b], local_kv=data["local_kv"][b],
+                        local_pos0=int(data["local_pos0"][b]),
+                        pooled_kv=data["pooled_kv"][k0:k1], sinks=data["sinks"],
+                        t0=int(data["t0"][b])))
+    return out
+
+
+def run_reference(args, wl, R):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    samples = host_samples(wl, 2)
+    per_step = max(1, int(args.ref_queries))
+    for _ in range(args.warmup):
+        oracle_query(wl, samples[0])
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        for q in range(per_step):
+            oracle_query(wl, samples[(s * per_step + q) % len(samples)])
+    el = time.perf_counter() - t0
+    value = args.steps * per_step / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"v4flash_decode (Np=32768, H_i=64x128, H=64x512, W=128); "
+                               f"each step {per_step} of the R={R} queries, CPU oracle",
+                   "queries_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                         "sample": f"{args.steps * per_step} queries over 2 host-drawn sequences"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def traffic_from_profile(kernel):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        ent = t.get(kernel)
+        if not ent:
+            return None
+        from deepseek_sparse_attention_hisa_gb300 import build
+        if ent.get("source_stamp") != build._stamp():
+            return None
+        return ent.get("bytes_per_launch")
+    except Exception:
+        return None
+
+
+def run_gpu(args, wl, R):
+    import torch
+    import torch.distributed as dist
+
+    from deepseek_sparse_attention_hisa_gb300 import binding as hb
+    from deepseek_sparse_attention_hisa_gb300 import build
+    from deepseek_sparse_attention_hisa_gb300.problem import Problem
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    build.build_library()
+    hb.lib()
+
+    bwl = wl.replace(B=R)
+    data = inputs.generate_device(bwl, device=dev, seed=1000 + rank)
+    prob = Problem(data, device=dev)
+    nb = int(prob.nb[0])
+    newest = torch.as_tensor(np.full(R, nb - 1, dtype=np.int32), device=dev)
+    prob.block_means()                               # cache of completed blocks
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+    stages = ["block_means", "block_filter", "select_topk", "sparse_attend"]
+    calls = {
+        "block_means": lambda s: hb.block_means(prob.idesc, prob.keys, prob.key_off,
+                                                prob.means_off, newest, prob.means, prob.ws, s),
+        "block_filter": lambda s: prob.block_filter(stream=s),
+        "select_topk": lambda s: prob.select_topk(stream=s),
+        "sparse_attend": lambda s: prob.attend(stream=s),
+    }
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for name in stages:                          # eager warm-up: attributes, lazy init
+            calls[name](stream)
+    stream.synchronize()
+    graphs = {}
+    for name in stages:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            calls[name](stream)
+        graphs[name] = g
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        for i, name in enumerate(stages):
+            graphs[name].replay()
+            if evs is not None:
+                evs[i + 1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+    stream.synchronize()
+    assert prob.status(stream) == 0, "device status flags set during warm-up"
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.zero_()                       # L2 flush outside the step's events
+                step(evs[i])
+        stream.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    torch.cuda.synchronize()
+    step_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(K)]
+    stage_ms = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]
+                for j, name in enumerate(stages)}
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = world * R * K / (total_ms / 1e3)
+
+    # e2e: the same step through the public API from pinned host buffers, with the
+    # per-step query inputs copied in and the results (out, I) copied back.
+    host_in = {n: data[n].detach().cpu().pin_memory() for n in ("q_idx", "w", "q_attn")}
+    host_out = {"out": torch.empty_like(prob.out, device="cpu").pin_memory(),
+                "I": torch.empty_like(prob.I, device="cpu").pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.zero_()
+            e2e_ev[i][0].record(stream)
+            prob.q_idx.copy_(host_in["q_idx"], non_blocking=True)
+            prob.w.copy_(host_in["w"], non_blocking=True)
+            prob.q_attn.copy_(host_in["q_attn"], non_blocking=True)
+            step()
+            host_out["out"].copy_(prob.out, non_blocking=True)
+            host_out["I"].copy_(prob.I, non_blocking=True)
+            e2e_ev[i][1].record(stream)
+    stream.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / K
+    assert prob.status(stream) == 0, "device status flags set during the timed region"
+
+    per_stage_bytes, step_bytes = stage_bytes(wl, nb)
+    peak, peak_src = peaks()
+    stage_avg = {n: statistics.mean(v) for n, v in stage_ms.items()}
+    dom = max(stage_avg, key=stage_avg.get)
+    achieved = per_stage_bytes[dom] * R / (stage_avg[dom] / 1e3) / 1e9
+    kernel_of = {"block_means": "k_block_means", "block_filter": "k_scores_simt",
+                 "select_topk": "k_scores_simt", "sparse_attend": "k_attend_simt"}
+    traffic = traffic_from_profile(kernel_of[dom])
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"v4flash_decode x R={R} independent sequences per GPU "
+                               f"(Np=32768 each, H_i=64x128, b=64, keep=16, k=512, "
+                               f"H=64x512 bf16, W=128)",
+                   "R": R, "Np": 32768, "l2": "256 MiB L2 flush between steps; "
+                                               f"{step_bytes * R / 1e6:.0f} MB touched per step"},
+        "step_hbm_gbs": step_bytes * R / (ms_per_step / 1e3) / 1e9,
+        "step_bytes_per_query": step_bytes,
+        "stages_us": {n: v * 1e3 for n, v in stage_avg.items()},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic},
+        "gpu_launches": K * launches_per_step(prob),
+        "e2e": {"value": world * R / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "wall_s": t_wall,
+    }
+    clocks = clk.summary()
+    line["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        samples = [host_copy_of_sequence(data, 0)]
+        n, el = time_oracle(wl, samples, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": n / el, "unit": UNIT, "cores": cores_used(),
+                                "kind": "oracle",
+                                "sample": f"{n} queries of sequence 0 of the batch, {el:.1f} s"}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def launches_per_step(prob):
+    """Kernels this library launches per step: means 1, filter 2, select 2, attend 1 or 2."""
+    from deepseek_sparse_attention_hisa_gb300 import binding as hb
+    ws_need = hb.workspace_bytes(hb.OP_SPARSE_ATTEND, prob.adesc)
+    attend = 2 if ws_need > 256 else 1
+    return 1 + 2 + 2 + attend
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--R", type=int, default=256, help="independent decode queries per step")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-queries", type=int, default=4, help="oracle queries per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = inputs.WORKLOADS["v4flash_decode"]
+    if args.impl == "reference":
+        run_reference(args, wl, args.R)
+    else:
+        run_gpu(args, wl, args.R)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,335 @@
+// C ABI entry points of libhisa: host-side validation, workspace layout and kernel
+// dispatch. Declarations and the contract live in include/hisa.h.
+#include <cmath>
+#include <cstring>
+
+#include "hisa_internal.cuh"
+
+using namespace hisa;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool dtype_ok(int32_t d) { return d == HISA_F32 || d == HISA_BF16; }
+
+
+// Host-checkable validity of an indexer descriptor.
+hisa_status check_index_desc(const hisa_index_desc *d) {
+    if (!d) return HISA_EINVAL;
+    if (d->B < 1 || d->L < 1 || d->H_i < 1 || d->H_i > 128 || d->r < 1) return HISA_EINVAL;
+    if (d->index_topk < 1 || d->index_topk > kMaxTopk) return HISA_EINVAL;
+    if (d->index_block < 0 || d->index_keep < 0 || d->index_keep > 64) return HISA_EINVAL;
+    if (d->Np_max < 0 || d->Np_max > (int64_t)65535 * 256) return HISA_EINVAL;
+    if ((int64_t)d->B * d->L > 0x7fffffffLL) return HISA_EINVAL;
+    if (!dtype_ok(d->q_dtype) || !dtype_ok(d->k_dtype)) return HISA_EDTYPE;
+    if (d->D_i != 32 && d->D_i != 64 && d->D_i != 128) return HISA_EDTYPE;
+    return HISA_OK;
+}
+
+// Gate conditions the host can see ([HiSA issue] "HiSA decode path": index_block > 0
+// and index_block * index_keep >= k). Np_b >= index_block * index_keep is checked on
+// the device per sequence.
+hisa_status check_hisa_gate(const hisa_index_desc *d) {
+    if (d->index_block < 1 || d->index_keep < 1) return HISA_EINVAL;
+    if ((int64_t)d->index_block * d->index_keep < d->index_topk) return HISA_EINVAL;
+    if ((int64_t)d->index_block * d->index_keep > (int64_t)1 << 20) return HISA_EINVAL;
+    return HISA_OK;
+}
+
+hisa_status check_attn_desc(const hisa_attn_desc *d) {
+    if (!d) return HISA_EINVAL;
+    if (d->B < 1 || d->L < 1 || d->window < 0 || d->W_max < 0 || d->r < 1 || d->k < 0)
+        return HISA_EINVAL;
+    if (d->Np_max < 0 || d->Np_max > 0x7fffffffLL) return HISA_EINVAL;
+    if ((int64_t)d->B * d->L > 0x7fffffffLL) return HISA_EINVAL;
+    if (!dtype_ok(d->q_dtype) || !dtype_ok(d->kv_dtype) || d->q_dtype != d->kv_dtype)
+        return HISA_EDTYPE;
+    if (!attend_simt_supported(d->H, d->Dh)) return HISA_EDTYPE;
+    return HISA_OK;
+}
+
+int64_t n_rows(const hisa_index_desc *d) { return (int64_t)d->B * d->L; }
+
+// Number of split-K ranges for the combine: enough CTAs to cover the GPU twice, never
+// fewer rows per split than one chunk. `list_len` bounds the attended rows per query.
+int pick_nsplit(int64_t queries, int64_t list_len, int64_t *rows_per_split) {
+    const int chunk = attend_chunk_rows();
+    const int64_t chunks = (list_len + chunk - 1) / chunk;
+    int64_t ns = (kTargetCtas + queries - 1) / queries;
+    if (ns > chunks) ns = chunks;
+    if (ns < 1) ns = 1;
+    if (ns > 64) ns = 64;
+    const int64_t per = ((chunks + ns - 1) / ns) * chunk;
+    *rows_per_split = per > 0 ? per : chunk;
+    if (list_len > 0) ns = (list_len + *rows_per_split - 1) / *rows_per_split;
+    return (int)(ns < 1 ? 1 : ns);
+}
+
+int64_t attn_list_len(const hisa_attn_desc *d, bool dense) {
+    return (int64_t)d->W_max + (dense ? d->Np_max : (int64_t)d->k);
+}
+
+size_t attn_part_bytes(const hisa_attn_desc *d, bool dense) {
+    int64_t per = 0;
+    const int ns = pick_nsplit((int64_t)d->B * d->L, attn_list_len(d, dense), &per);
+    if (ns <= 1) return 0;
+    return (size_t)d->B * d->L * ns * d->H * (d->Dh + 2) * sizeof(float);
+}
+
+uint32_t *status_of(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
+
+float *scratch_of(void *ws) {
+    return reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + kStatusBytes);
+}
+
+hisa_status check_ws(void *ws, size_t have, size_t need) {
+    if (!ws || !aligned(ws, kAlign)) return HISA_EWORKSPACE;
+    if (have < need) return HISA_EWORKSPACE;
+    return HISA_OK;
+}
+
+hisa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HISA_OK : HISA_ECUDA; }
+
+ScoreParams score_params(const hisa_index_desc *d, int mode, const void *q, const float *w,
+                         const void *rows, int rows_bf16, const int64_t *key_off,
+                         const int32_t *t0, float *out, int64_t ld, void *ws) {
+    ScoreParams p{};
+    p.mode = mode;
+    p.B = d->B; p.L = d->L; p.H_i = d->H_i; p.D_i = d->D_i; p.r = d->r;
+    p.b = d->index_block; p.keep = d->index_keep;
+    p.causal = d->L > 1;
+    p.q = q; p.q_bf16 = d->q_dtype == HISA_BF16;
+    p.w = w;
+    p.head_scale = (float)(1.0 / std::sqrt((double)d->H_i * (double)d->D_i));
+    p.rows = rows; p.rows_bf16 = rows_bf16;
+    p.key_off = key_off; p.t0 = t0;
+    p.out = out; p.ld_out = ld;
+    p.Np_max = d->Np_max;
+    p.status = status_of(ws);
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *hisa_status_string(int32_t status) {
+    switch (status) {
+        case HISA_OK: return "HISA_OK";
+        case HISA_EINVAL: return "HISA_EINVAL: invalid argument";
+        case HISA_EDTYPE: return "HISA_EDTYPE: unsupported dtype or shape";
+        case HISA_EWORKSPACE: return "HISA_EWORKSPACE: workspace missing, misaligned or too small";
+        case HISA_ECUDA: return "HISA_ECUDA: CUDA call or launch failed";
+        case HISA_EDEVICE: return "HISA_EDEVICE: a kernel flagged bad data";
+        default: return "unknown hisa_status";
+    }
+}
+
+size_t hisa_workspace_bytes(int32_t op, const void *desc) {
+    if (!desc) return 0;
+    if (op == HISA_OP_SPARSE_ATTEND) {
+        const hisa_attn_desc *d = static_cast<const hisa_attn_desc *>(desc);
+        if (check_attn_desc(d) != HISA_OK) return 0;
+        const size_t a = attn_part_bytes(d, false), b = attn_part_bytes(d, true);
+        return kStatusBytes + round_up(a > b ? a : b);
+    }
+    const hisa_index_desc *d = static_cast<const hisa_index_desc *>(desc);
+    if (check_index_desc(d) != HISA_OK) return 0;
+    switch (op) {
+        case HISA_OP_INDEX_SCORES:
+        case HISA_OP_BLOCK_MEANS:
+            return kStatusBytes;
+        case HISA_OP_BLOCK_FILTER: {
+            if (check_hisa_gate(d) != HISA_OK) return 0;
+            const int64_t nb_max = d->Np_max / d->index_block;
+            return kStatusBytes + round_up((size_t)n_rows(d) * nb_max * sizeof(float));
+        }
+        case HISA_OP_SELECT_TOPK: {
+            if (check_hisa_gate(d) != HISA_OK) return 0;
+            const int64_t C = (int64_t)d->index_block * d->index_keep;
+            return kStatusBytes + round_up((size_t)n_rows(d) * C * sizeof(float));
+        }
+        case HISA_OP_FLAT_TOPK:
+            return kStatusBytes + round_up((size_t)n_rows(d) * d->Np_max * sizeof(float));
+        default:
+            return 0;
+    }
+}
+
+hisa_status hisa_workspace_init(void *ws, size_t ws_bytes, hisa_stream_t stream) {
+    hisa_status st = check_ws(ws, ws_bytes, kStatusBytes);
+    if (st != HISA_OK) return st;
+    return from_cuda(cudaMemsetAsync(ws, 0, kStatusBytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hisa_status hisa_device_status(const void *ws, hisa_stream_t stream, uint32_t *flags) {
+    if (!ws || !flags || !aligned(ws, kAlign)) return HISA_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return HISA_ECUDA;
+    *flags = v;
+    return v ? HISA_EDEVICE : HISA_OK;
+}
+
+hisa_status hisa_index_scores(const hisa_index_desc *d, const void *q, const float *w,
+                              const void *keys, const int64_t *key_off, const int32_t *t0,
+                              float *scores, int64_t ld_scores, void *ws, size_t ws_bytes,
+                              hisa_stream_t stream) {
+    hisa_status st = check_index_desc(d);
+    if (st != HISA_OK) return st;
+    if (!q || !w || !keys || !key_off || !t0 || !scores) return HISA_EINVAL;
+    if (!aligned(q, 16) || !aligned(keys, 16) || !aligned(w, 4) || !aligned(scores, 4))
+        return HISA_EINVAL;
+    if (ld_scores < d->Np_max || ld_scores < 1) return HISA_EINVAL;
+    if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_INDEX_SCORES, d))) != HISA_OK)
+        return st;
+    ScoreParams p = score_params(d, kFlat, q, w, keys, d->k_dtype == HISA_BF16, key_off, t0,
+                                 scores, ld_scores, ws);
+    p.n_max = d->Np_max;
+    return from_cuda(launch_scores_simt(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hisa_status hisa_block_means(const hisa_index_desc *d, const void *keys, const int64_t *key_off,
+                             const int64_t *means_off, const int32_t *first_block, float *means,
+                             void *ws, size_t ws_bytes, hisa_stream_t stream) {
+    hisa_status st = check_index_desc(d);
+    if (st != HISA_OK) return st;
+    if (d->index_block < 1) return HISA_EINVAL;
+    if (!keys || !key_off || !means_off || !means) return HISA_EINVAL;
+    if (!aligned(keys, 16) || !aligned(means, 4)) return HISA_EINVAL;
+    if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_BLOCK_MEANS, d))) != HISA_OK)
+        return st;
+    MeansParams p{};
+    p.B = d->B; p.D_i = d->D_i; p.b = d->index_block;
+    p.keys = keys; p.keys_bf16 = d->k_dtype == HISA_BF16;
+    p.key_off = key_off; p.means_off = means_off; p.first_block = first_block;
+    p.means = means; p.Np_max = d->Np_max; p.status = status_of(ws);
+    return from_cuda(launch_block_means(p, d->Np_max / d->index_block,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hisa_status hisa_block_filter(const hisa_index_desc *d, const void *q, const float *w,
+                              const float *means, const int64_t *means_off,
+                              const int64_t *key_off, const int32_t *t0, int32_t *top_blk,
+                              float *cscores, int64_t ld_cscores, void *ws, size_t ws_bytes,
+                              hisa_stream_t stream) {
+    hisa_status st = check_index_desc(d);
+    if (st != HISA_OK) return st;
+    if ((st = check_hisa_gate(d)) != HISA_OK) return st;
+    if (!q || !w || !means || !means_off || !key_off || !t0 || !top_blk) return HISA_EINVAL;
+    if (!aligned(q, 16) || !aligned(means, 16) || !aligned(w, 4)) return HISA_EINVAL;
+    const int64_t nb_max = d->Np_max / d->index_block;
+    if (cscores && ld_cscores < nb_max) return HISA_EINVAL;
+    if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_BLOCK_FILTER, d))) != HISA_OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float *buf = cscores ? cscores : scratch_of(ws);
+    const int64_t ld = cscores ? ld_cscores : (nb_max > 0 ? nb_max : 1);
+    ScoreParams p = score_params(d, kCoarse, q, w, means, 0, key_off, t0, buf, ld, ws);
+    p.means_off = means_off;
+    p.n_max = nb_max;
+    cudaError_t e = launch_scores_simt(p, s);
+    if (e != cudaSuccess) return HISA_ECUDA;
+    SelectParams sp{};
+    sp.mode = kCoarse; sp.B = d->B; sp.L = d->L; sp.b = d->index_block; sp.keep = d->index_keep;
+    sp.k = d->index_keep;
+    sp.scores = buf; sp.ld = ld; sp.key_off = key_off; sp.out = top_blk;
+    sp.Np_max = d->Np_max; sp.status = status_of(ws);
+    return from_cuda(launch_select(sp, nb_max, s));
+}
+
+hisa_status hisa_select_topk(const hisa_index_desc *d, const void *q, const float *w,
+                             const void *keys, const int64_t *key_off, const int32_t *t0,
+                             const int32_t *top_blk, int32_t *I, float *fscores, void *ws,
+                             size_t ws_bytes, hisa_stream_t stream) {
+    hisa_status st = check_index_desc(d);
+    if (st != HISA_OK) return st;
+    if ((st = check_hisa_gate(d)) != HISA_OK) return st;
+    if (!q || !w || !keys || !key_off || !t0 || !top_blk || !I) return HISA_EINVAL;
+    if (!aligned(q, 16) || !aligned(keys, 16) || !aligned(w, 4)) return HISA_EINVAL;
+    if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_SELECT_TOPK, d))) != HISA_OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t C = (int64_t)d->index_block * d->index_keep;
+    float *buf = fscores ? fscores : scratch_of(ws);
+    ScoreParams p = score_params(d, kFine, q, w, keys, d->k_dtype == HISA_BF16, key_off, t0, buf,
+                                 C, ws);
+    p.top_blk = top_blk;
+    p.n_max = C;
+    cudaError_t e = launch_scores_simt(p, s);
+    if (e != cudaSuccess) return HISA_ECUDA;
+    SelectParams sp{};
+    sp.mode = kFine; sp.B = d->B; sp.L = d->L; sp.b = d->index_block; sp.keep = d->index_keep;
+    sp.k = d->index_topk;
+    sp.scores = buf; sp.ld = C; sp.key_off = key_off; sp.top_blk = top_blk; sp.out = I;
+    sp.Np_max = d->Np_max; sp.status = status_of(ws);
+    return from_cuda(launch_select(sp, C, s));
+}
+
+hisa_status hisa_flat_topk(const hisa_index_desc *d, const void *q, const float *w,
+                           const void *keys, const int64_t *key_off, const int32_t *t0,
+                           int32_t *I, void *ws, size_t ws_bytes, hisa_stream_t stream) {
+    hisa_status st = check_index_desc(d);
+    if (st != HISA_OK) return st;
+    if (!q || !w || !keys || !key_off || !t0 || !I) return HISA_EINVAL;
+    if (!aligned(q, 16) || !aligned(keys, 16) || !aligned(w, 4)) return HISA_EINVAL;
+    if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_FLAT_TOPK, d))) != HISA_OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t ld = d->Np_max > 0 ? d->Np_max : 1;
+    float *buf = scratch_of(ws);
+    ScoreParams p = score_params(d, kFlat, q, w, keys, d->k_dtype == HISA_BF16, key_off, t0, buf,
+                                 ld, ws);
+    p.n_max = d->Np_max;
+    cudaError_t e = launch_scores_simt(p, s);
+    if (e != cudaSuccess) return HISA_ECUDA;
+    SelectParams sp{};
+    sp.mode = kFlat; sp.B = d->B; sp.L = d->L; sp.b = d->index_block; sp.keep = d->index_keep;
+    sp.k = d->index_topk;
+    sp.scores = buf; sp.ld = ld; sp.key_off = key_off; sp.out = I;
+    sp.Np_max = d->Np_max; sp.status = status_of(ws);
+    return from_cuda(launch_select(sp, d->Np_max, s));
+}
+
+hisa_status hisa_sparse_attend(const hisa_attn_desc *d, const void *q, const void *local_kv,
+                               const int32_t *local_len, const int32_t *local_pos0,
+                               const void *pooled_kv, const int64_t *kv_off, const int32_t *I,
+                               const float *sinks, const int32_t *t0, float *out, void *ws,
+                               size_t ws_bytes, hisa_stream_t stream) {
+    hisa_status st = check_attn_desc(d);
+    if (st != HISA_OK) return st;
+    if (!q || !local_len || !local_pos0 || !kv_off || !sinks || !t0 || !out) return HISA_EINVAL;
+    if (d->W_max > 0 && !local_kv) return HISA_EINVAL;
+    if (d->Np_max > 0 && !pooled_kv) return HISA_EINVAL;
+    if (I && d->k < 1) return HISA_EINVAL;
+    if (!aligned(q, 16) || !aligned(local_kv, 16) || !aligned(pooled_kv, 16) || !aligned(out, 16))
+        return HISA_EINVAL;
+    if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_SPARSE_ATTEND, d))) != HISA_OK)
+        return st;
+    const bool dense = I == nullptr;
+    AttnParams p{};
+    p.B = d->B; p.L = d->L; p.H = d->H; p.Dh = d->Dh; p.window = d->window; p.W_max = d->W_max;
+    p.r = d->r; p.k = dense ? 0 : d->k;
+    p.causal = d->L > 1;
+    p.Np_max = d->Np_max;
+    p.scale = d->scale > 0.f ? d->scale : (float)(1.0 / std::sqrt((double)d->Dh));
+    p.q = q; p.local_kv = local_kv; p.local_len = local_len; p.local_pos0 = local_pos0;
+    p.pooled_kv = pooled_kv; p.kv_off = kv_off; p.I = I; p.sinks = sinks; p.t0 = t0;
+    p.out = out;
+    p.part = scratch_of(ws);
+    int64_t per = 0;
+    p.nsplit = pick_nsplit((int64_t)d->B * d->L, attn_list_len(d, dense), &per);
+    p.rows_per_split = (int)per;
+    p.kv_bf16 = d->kv_dtype == HISA_BF16;
+    p.status = status_of(ws);
+    return from_cuda(launch_attend_simt(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

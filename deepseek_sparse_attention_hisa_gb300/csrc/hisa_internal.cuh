@@ -1,0 +1,124 @@
+// Internal declarations shared by the kernel translation units of libhisa.
+// Nothing here is part of the C ABI (see include/hisa.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/hisa.h"
+
+namespace hisa {
+
+constexpr float kNeg = -1e30f;            // selection mask value ([HiSA issue] "Flat selection")
+constexpr size_t kStatusBytes = 256;      // status word region at the head of the workspace
+constexpr int kTargetCtas = 304;          // 2 CTAs per SM on a 152-SM GB300
+constexpr int kMaxTopk = 2048;
+
+enum ScoreMode : int { kFlat = 0, kCoarse = 1, kFine = 2 };
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ void flag(uint32_t *status, uint32_t bit) {
+    if (status) atomicOr(status, bit);
+}
+
+// Visible pooled prefix V(t) = min(Np, floor((t+1)/r)).
+__device__ __forceinline__ int64_t visible_len(int64_t t, int r, int64_t Np) {
+    int64_t v = (t + 1) / r;
+    if (t + 1 < 0) v = 0;
+    return v < Np ? v : Np;
+}
+
+// Orderable key of an f32 score: larger float -> larger key; -0.0 == +0.0.
+__device__ __forceinline__ uint32_t order_key(float s) {
+    uint32_t u = __float_as_uint(s);
+    if ((u << 1) == 0u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// launch parameter blocks
+// ---------------------------------------------------------------------------
+struct ScoreParams {
+    int mode;                 // ScoreMode
+    int B, L, H_i, D_i, r, b, keep;
+    int causal;               // apply the pooled causal mask (L > 1)
+    const void *q;            // [B*L, H_i, D_i]
+    int q_bf16;
+    const float *w;           // [B*L, H_i] raw
+    float head_scale;         // H_i^-1/2 * D_i^-1/2
+    const void *rows;         // keys [sum Np, D_i] (flat / fine) or means [*, D_i] f32 (coarse)
+    int rows_bf16;
+    const int64_t *key_off;   // [B+1]
+    const int64_t *means_off; // [B+1] (coarse)
+    const int32_t *t0;        // [B]
+    const int32_t *top_blk;   // [B*L, keep] (fine)
+    float *out;               // [B*L, ld_out]
+    int64_t ld_out;
+    int64_t n_max;            // max scored rows per query row (grid.x extent)
+    int64_t Np_max;
+    uint32_t *status;
+};
+
+struct SelectParams {
+    int mode;                 // ScoreMode: what a score column maps to
+    int B, L, b, keep, k;
+    const float *scores;      // [B*L, ld]
+    int64_t ld;
+    const int64_t *key_off;
+    const int32_t *top_blk;   // fine: [B*L, keep]
+    int32_t *out;             // [B*L, k]
+    int64_t Np_max;
+    uint32_t *status;
+};
+
+struct MeansParams {
+    int B, D_i, b;
+    const void *keys;
+    int keys_bf16;
+    const int64_t *key_off;
+    const int64_t *means_off;
+    const int32_t *first_block;
+    float *means;
+    int64_t Np_max;
+    uint32_t *status;
+};
+
+struct AttnParams {
+    int B, L, H, Dh, window, W_max, r, k;
+    int causal;
+    int64_t Np_max;
+    float scale;
+    const void *q;            // [B*L, H, Dh]
+    const void *local_kv;     // [B, W_max, Dh]
+    const int32_t *local_len;
+    const int32_t *local_pos0;
+    const void *pooled_kv;    // [sum Np, Dh]
+    const int64_t *kv_off;
+    const int32_t *I;         // [B*L, k] or nullptr
+    const float *sinks;       // [H]
+    const int32_t *t0;
+    float *out;               // [B*L, H, Dh]
+    float *part;              // split partials [B*L, nsplit, H, Dh + 2]
+    int nsplit;
+    int rows_per_split;       // multiple of the chunk size
+    int kv_bf16;
+    uint32_t *status;
+};
+
+// ---------------------------------------------------------------------------
+// host launchers (one per kernel file); return the cudaGetLastError() of the launch
+// ---------------------------------------------------------------------------
+cudaError_t launch_scores_simt(const ScoreParams &p, cudaStream_t s);
+cudaError_t launch_select(const SelectParams &p, int64_t n_max, cudaStream_t s);
+cudaError_t launch_block_means(const MeansParams &p, int64_t nb_max, cudaStream_t s);
+cudaError_t launch_attend_simt(const AttnParams &p, cudaStream_t s);
+int attend_simt_supported(int H, int Dh);
+int attend_chunk_rows();
+
+}  // namespace hisa

@@ -1,0 +1,209 @@
+// Indexer scoring on CUDA cores (any supported shape, f32 or bf16 inputs), and the
+// block-mean representatives.
+//
+// score = sum_h relu(q_h . row) * scale * w_h, accumulated in f32
+// ([HiSA issue] "Flat selection (baseline path)"; the coarse stage applies the same
+// head combine to block means, the fine stage to the candidate rows, "HiSA decode
+// path"). One thread owns one scored row: it holds the row in registers and walks
+// the heads, with q broadcast from shared memory.
+#include "hisa_internal.cuh"
+
+namespace hisa {
+
+template <int D, typename T>
+__device__ __forceinline__ void load_row(const T *src, float (&v)[D]);
+
+template <int D>
+__device__ __forceinline__ void load_row(const float *src, float (&v)[D]) {
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll
+    for (int i = 0; i < D / 4; ++i) {
+        float4 x = __ldg(s4 + i);
+        v[4 * i + 0] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *src, float (&v)[D]) {
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+        uint4 x = __ldg(s4 + i);
+        const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&x);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float2 f = __bfloat1622float2(h2[e]);
+            v[8 * i + 2 * e] = f.x;
+            v[8 * i + 2 * e + 1] = f.y;
+        }
+    }
+}
+
+template <int D, typename QT, typename KT>
+__global__ void __launch_bounds__(256) k_scores_simt(ScoreParams p) {
+    extern __shared__ __align__(16) float smem[];
+    float *sq = smem;                      // [H_i][D] f32
+    float *sw = sq + p.H_i * D;            // [H_i] scaled weights
+    int *sblk = reinterpret_cast<int *>(sw + p.H_i);  // [keep] kept blocks, ascending
+
+    const int row = blockIdx.x;            // b * L + j
+    const int bq = row / p.L;
+    const int j = row - bq * p.L;
+    const int64_t k0 = p.key_off[bq];
+    const int64_t Np = p.key_off[bq + 1] - k0;
+    if (Np < 0 || Np > p.Np_max) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
+        return;
+    }
+    int64_t n;
+    if (p.mode == kFlat) {
+        n = Np;
+    } else {
+        if (Np < (int64_t)p.b * p.keep) {  // HiSA gate, per sequence
+            if (threadIdx.x == 0 && blockIdx.y == 0) flag(p.status, HISA_DEV_GATE);
+            return;
+        }
+        n = (p.mode == kCoarse) ? Np / p.b : (int64_t)p.keep * p.b;
+        if (p.mode == kCoarse && p.means_off[bq + 1] - p.means_off[bq] < n) {
+            if (threadIdx.x == 0 && blockIdx.y == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
+            return;
+        }
+    }
+    const int64_t i0 = (int64_t)blockIdx.y * blockDim.x;
+    if (i0 >= n) return;
+
+    const QT *qrow = reinterpret_cast<const QT *>(p.q) + (int64_t)row * p.H_i * D;
+    for (int e = threadIdx.x; e < p.H_i * D; e += blockDim.x) sq[e] = to_f32(qrow[e]);
+    for (int h = threadIdx.x; h < p.H_i; h += blockDim.x)
+        sw[h] = p.w[(int64_t)row * p.H_i + h] * p.head_scale;
+    if (p.mode == kFine && threadIdx.x == 0) {
+        const int32_t *tb = p.top_blk + (int64_t)row * p.keep;
+        for (int s = 0; s < p.keep; ++s) {  // insertion sort: candidates in ascending pos
+            int v = tb[s], u = s;
+            while (u > 0 && sblk[u - 1] > v) { sblk[u] = sblk[u - 1]; --u; }
+            sblk[u] = v;
+        }
+    }
+    __syncthreads();
+
+    const int64_t i = i0 + threadIdx.x;
+    if (i >= n) return;
+    const int64_t V = p.causal ? visible_len((int64_t)p.t0[bq] + j, p.r, Np) : Np;
+    int64_t pos, src;
+    if (p.mode == kFlat) {
+        pos = i;
+        src = k0 + i;
+    } else if (p.mode == kCoarse) {
+        pos = i * p.b;                     // a block is eligible iff its first row is visible
+        src = p.means_off[bq] + i;
+    } else {
+        const int blk = sblk[i / p.b];
+        if (blk < 0 || (int64_t)blk >= Np / p.b) {
+            flag(p.status, HISA_DEV_BAD_BLOCK);
+            p.out[(int64_t)row * p.ld_out + i] = kNeg;
+            return;
+        }
+        pos = (int64_t)blk * p.b + (i % p.b);
+        src = k0 + pos;
+    }
+    float result = kNeg;
+    if (pos < V) {
+        float kv[D];
+        load_row<D>(reinterpret_cast<const KT *>(p.rows) + src * D, kv);
+        float acc = 0.f;
+        for (int h = 0; h < p.H_i; ++h) {
+            const float4 *qh = reinterpret_cast<const float4 *>(sq + h * D);
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int d = 0; d < D / 4; ++d) {
+                float4 qv = qh[d];
+                a0 = fmaf(qv.x, kv[4 * d + 0], a0);
+                a1 = fmaf(qv.y, kv[4 * d + 1], a1);
+                a2 = fmaf(qv.z, kv[4 * d + 2], a2);
+                a3 = fmaf(qv.w, kv[4 * d + 3], a3);
+            }
+            const float dot = (a0 + a1) + (a2 + a3);
+            acc = fmaf(sw[h], fmaxf(dot, 0.f), acc);
+        }
+        result = acc;
+    }
+    p.out[(int64_t)row * p.ld_out + i] = result;
+}
+
+template <int D, typename QT, typename KT>
+static cudaError_t launch_scores_t(const ScoreParams &p, cudaStream_t s) {
+    const size_t smem = (size_t)p.H_i * D * 4 + (size_t)p.H_i * 4 + 64 * 4;
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        k_scores_simt<D, QT, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 128 * 4 + 1024);
+    if (attr != cudaSuccess) return attr;
+    const int64_t tiles = (p.n_max + 255) / 256;
+    if (tiles == 0) return cudaSuccess;
+    dim3 grid((unsigned)(p.B * p.L), (unsigned)tiles);
+    k_scores_simt<D, QT, KT><<<grid, 256, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_scores_d(const ScoreParams &p, cudaStream_t s) {
+    if (p.q_bf16) {
+        if (p.rows_bf16) return launch_scores_t<D, __nv_bfloat16, __nv_bfloat16>(p, s);
+        return launch_scores_t<D, __nv_bfloat16, float>(p, s);
+    }
+    if (p.rows_bf16) return launch_scores_t<D, float, __nv_bfloat16>(p, s);
+    return launch_scores_t<D, float, float>(p, s);
+}
+
+cudaError_t launch_scores_simt(const ScoreParams &p, cudaStream_t s) {
+    switch (p.D_i) {
+        case 32: return launch_scores_d<32>(p, s);
+        case 64: return launch_scores_d<64>(p, s);
+        case 128: return launch_scores_d<128>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// block means ([HiSA issue] "HiSA decode path": rep = mean of the b rows of a block)
+// ---------------------------------------------------------------------------
+template <typename KT>
+__global__ void k_block_means(MeansParams p) {
+    const int bq = blockIdx.y;
+    const int64_t k0 = p.key_off[bq];
+    const int64_t Np = p.key_off[bq + 1] - k0;
+    if (Np < 0 || Np > p.Np_max) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
+        return;
+    }
+    const int64_t nb = Np / p.b;
+    const int64_t m0 = p.means_off[bq];
+    if (p.means_off[bq + 1] - m0 < nb) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
+        return;
+    }
+    int64_t fb = p.first_block ? (int64_t)p.first_block[bq] : 0;
+    if (fb < 0) fb = 0;
+    const KT *keys = reinterpret_cast<const KT *>(p.keys);
+    const float inv_div = (float)p.b;
+    for (int64_t beta = fb + blockIdx.x; beta < nb; beta += gridDim.x) {
+        for (int d = threadIdx.x; d < p.D_i; d += blockDim.x) {
+            const KT *src = keys + (k0 + beta * p.b) * p.D_i + d;
+            float s = 0.f;
+            for (int i = 0; i < p.b; ++i) s += to_f32(src[(int64_t)i * p.D_i]);
+            p.means[(m0 + beta) * p.D_i + d] = s / inv_div;
+        }
+    }
+}
+
+cudaError_t launch_block_means(const MeansParams &p, int64_t nb_max, cudaStream_t s) {
+    if (nb_max <= 0) return cudaSuccess;
+    const unsigned gx = (unsigned)(nb_max < 2048 ? nb_max : 2048);
+    dim3 grid(gx, (unsigned)p.B);
+    const int threads = p.D_i;
+    if (p.keys_bf16)
+        k_block_means<__nv_bfloat16><<<grid, threads, 0, s>>>(p);
+    else
+        k_block_means<float><<<grid, threads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace hisa

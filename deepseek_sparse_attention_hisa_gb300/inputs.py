@@ -168,3 +168,49 @@ def small_workload(**kw) -> Workload:
                 key_dtype="f32", kv_dtype="f32", Np=(512,))
     base.update(kw)
     return Workload(**base)
+
+
+def generate_device(wl: Workload, device="cuda", seed: int | None = None) -> dict:
+    """Like generate(), but drawn on the device with torch's generator (for batches too
+    large to draw on the host). Same shapes, distributions and layout; different random
+    stream, so results are only comparable with the oracle on host copies of the draws.
+    Every sequence has wl.Np[0] pooled rows; returns torch tensors (bf16 as torch.bfloat16).
+    """
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(wl.seed if seed is None else seed)
+    B, Np = wl.B, int(wl.Np[0])
+    npb = np.full(B, Np, dtype=np.int64)
+    key_off = np.zeros(B + 1, dtype=np.int64)
+    key_off[1:] = np.cumsum(npb)
+    t0 = (wl.r * npb - 1).astype(np.int32) if wl.t0 is None else np.full(B, wl.t0, np.int32)
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+    def normal(shape, dtype, std=1.0, rows_per_draw=None):
+        out = torch.empty(shape, dtype=tdt[dtype], device=device)
+        flat = out.view(shape[0], -1)
+        step = rows_per_draw or shape[0]
+        for lo in range(0, shape[0], step):
+            hi = min(shape[0], lo + step)
+            z = torch.randn((hi - lo, flat.shape[1]), generator=g, device=device,
+                            dtype=torch.float32)
+            if std != 1.0:
+                z *= std
+            flat[lo:hi] = z.to(tdt[dtype])
+        return out
+
+    total = int(key_off[-1])
+    out = dict(wl=wl, Np=npb, key_off=key_off, t0=t0)
+    out["q_idx"] = normal((B, wl.L, wl.H_i, wl.D_i), wl.q_idx_dtype)
+    out["w"] = normal((B, wl.L, wl.H_i), "f32")
+    out["keys"] = normal((total, wl.D_i), wl.key_dtype, rows_per_draw=1 << 20)
+    if wl.with_attention:
+        W_rows = wl.window + (wl.L - 1)
+        out["q_attn"] = normal((B, wl.L, wl.H, wl.Dh), wl.kv_dtype)
+        out["local_kv"] = normal((B, W_rows, wl.Dh), wl.kv_dtype, std=wl.Dh ** -0.5)
+        out["local_len"] = np.full(B, W_rows, dtype=np.int32)
+        out["local_pos0"] = (t0.astype(np.int64) + (wl.L - 1) - (W_rows - 1)).astype(np.int32)
+        out["pooled_kv"] = normal((total, wl.Dh), wl.kv_dtype, std=wl.Dh ** -0.5,
+                                  rows_per_draw=1 << 17)
+        out["sinks"] = normal((wl.H,), "f32")
+    return out

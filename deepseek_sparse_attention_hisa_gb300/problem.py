@@ -1,0 +1,127 @@
+"""Device-resident state of one HiSA problem and the calls of the step, in order.
+
+Marshalling only: torch allocates the tensors and owns the stream; every stage is
+one libhisa entry point (include/hisa.h). Stages follow the page "feat(deepseek-v4):
+implement HiSA hierarchical sparse attention": block means -> coarse filter ->
+fine top-k (or the flat top-k) -> sparse combine.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import binding as hb
+
+
+def _i64(a, device):
+    import torch
+    return torch.as_tensor(np.asarray(a, dtype=np.int64), device=device)
+
+
+def _i32(a, device):
+    import torch
+    return torch.as_tensor(np.asarray(a, dtype=np.int32), device=device)
+
+
+class Problem:
+    """One batch of B sequences x L query rows, resident in device memory.
+
+    `data` is the dict returned by inputs.generate (numpy arrays; uint16 = bf16 bits).
+    """
+
+    def __init__(self, data: dict, device="cuda", index_keep: int | None = None):
+        import torch
+        wl = data["wl"]
+        self.wl = wl
+        self.device = device
+        self.B, self.L = wl.B, wl.L
+        self.b = wl.index_block
+        self.keep = wl.index_keep if index_keep is None else index_keep
+        self.k = wl.index_topk
+        Np = np.asarray(data["Np"], dtype=np.int64)
+        self.Np = Np
+        self.Np_max = int(Np.max()) if Np.size else 0
+        dev = device
+        self.q_idx = hb.to_device(data["q_idx"], dev)
+        self.w = hb.to_device(data["w"], dev)
+        self.keys = hb.to_device(data["keys"], dev)
+        self.key_off = _i64(data["key_off"], dev)
+        self.t0 = _i32(data["t0"], dev)
+        self.idesc = hb.IndexDesc(
+            B=wl.B, L=wl.L, H_i=wl.H_i, D_i=wl.D_i, r=wl.r, index_topk=wl.index_topk,
+            index_block=self.b, index_keep=self.keep, Np_max=self.Np_max,
+            q_dtype=hb.dtype_code(self.q_idx), k_dtype=hb.dtype_code(self.keys))
+        nb = Np // self.b if self.b > 0 else np.zeros_like(Np)
+        self.nb = nb
+        means_off = np.zeros(wl.B + 1, dtype=np.int64)
+        means_off[1:] = np.cumsum(nb)
+        self.means_off = _i64(means_off, dev)
+        self.means = torch.zeros((max(int(means_off[-1]), 1), wl.D_i), dtype=torch.float32,
+                                 device=dev)
+        rows = wl.B * wl.L
+        self.top_blk = torch.full((rows, max(self.keep, 1)), -7, dtype=torch.int32, device=dev)
+        self.I = torch.full((rows, self.k), -7, dtype=torch.int32, device=dev)
+        ops = [hb.OP_INDEX_SCORES, hb.OP_BLOCK_MEANS, hb.OP_FLAT_TOPK]
+        if self.b > 0 and self.keep > 0 and self.b * self.keep >= self.k:
+            ops += [hb.OP_BLOCK_FILTER, hb.OP_SELECT_TOPK]
+        need = max(hb.workspace_bytes(op, self.idesc) for op in ops)
+        self.has_attention = "q_attn" in data
+        if self.has_attention:
+            self.q_attn = hb.to_device(data["q_attn"], dev)
+            self.local_kv = hb.to_device(data["local_kv"], dev)
+            self.local_len = _i32(data["local_len"], dev)
+            self.local_pos0 = _i32(data["local_pos0"], dev)
+            self.pooled_kv = hb.to_device(data["pooled_kv"], dev)
+            self.sinks = hb.to_device(data["sinks"], dev)
+            self.adesc = hb.AttnDesc(
+                B=wl.B, L=wl.L, H=wl.H, Dh=wl.Dh, window=wl.window,
+                W_max=int(data["local_kv"].shape[1]), r=wl.r, k=self.k, Np_max=self.Np_max,
+                scale=0.0, q_dtype=hb.dtype_code(self.q_attn),
+                kv_dtype=hb.dtype_code(self.pooled_kv))
+            self.out = torch.empty((rows, wl.H, wl.Dh), dtype=torch.float32, device=dev)
+            need = max(need, hb.workspace_bytes(hb.OP_SPARSE_ATTEND, self.adesc))
+        if need == 0:
+            raise ValueError("descriptor rejected by hisa_workspace_bytes")
+        self.ws = hb.alloc_workspace(need, dev)
+
+    # ---- stages -------------------------------------------------------------
+    def block_means(self, first_block=None, stream=None):
+        fb = None if first_block is None else _i32(first_block, self.device)
+        hb.block_means(self.idesc, self.keys, self.key_off, self.means_off, fb, self.means,
+                       self.ws, stream)
+
+    def block_filter(self, cscores=None, stream=None):
+        ld = 0 if cscores is None else cscores.shape[1]
+        hb.block_filter(self.idesc, self.q_idx, self.w, self.means, self.means_off, self.key_off,
+                        self.t0, self.top_blk, self.ws, cscores, ld, stream)
+
+    def select_topk(self, fscores=None, top_blk=None, stream=None):
+        tb = self.top_blk if top_blk is None else top_blk
+        hb.select_topk(self.idesc, self.q_idx, self.w, self.keys, self.key_off, self.t0, tb,
+                       self.I, self.ws, fscores, stream)
+
+    def flat_topk(self, I=None, stream=None):
+        hb.flat_topk(self.idesc, self.q_idx, self.w, self.keys, self.key_off, self.t0,
+                     self.I if I is None else I, self.ws, stream)
+
+    def index_scores(self, scores, stream=None):
+        hb.index_scores(self.idesc, self.q_idx, self.w, self.keys, self.key_off, self.t0, scores,
+                        scores.shape[1], self.ws, stream)
+
+    def attend(self, I="selected", out=None, stream=None):
+        """I: 'selected' (self.I), None (dense branch over all pooled rows) or a tensor."""
+        sel = self.I if isinstance(I, str) else I
+        hb.sparse_attend(self.adesc, self.q_attn, self.local_kv, self.local_len, self.local_pos0,
+                         self.pooled_kv, self.key_off, sel, self.sinks, self.t0,
+                         self.out if out is None else out, self.ws, stream)
+
+    def hisa_step(self, first_block=None, stream=None):
+        """The HiSA step: newest block means, coarse filter, fine top-k, sparse combine."""
+        if first_block is not None:
+            self.block_means(first_block, stream)
+        self.block_filter(stream=stream)
+        self.select_topk(stream=stream)
+        if self.has_attention:
+            self.attend(stream=stream)
+
+    def status(self, stream=None) -> int:
+        return hb.device_status(self.ws, stream)

@@ -1,0 +1,213 @@
+/*
+ * hisa.h -- C ABI of the GB300 (sm_103a) HiSA sparse-attention step.
+ *
+ * The step is the one described on the page "feat(deepseek-v4): implement HiSA
+ * hierarchical sparse attention" (cited as [HiSA issue] with its section): score
+ * pooled indexer keys, select index_topk pooled rows (flat or hierarchical), gather
+ * the selected pooled KV rows and combine them with the local window and the
+ * per-head sinks in one split softmax.
+ *
+ * Conventions shared by every entry point
+ *  - Tensor pointers are DEVICE pointers owned by the caller; tensors are dense,
+ *    row-major, with the shapes written beside each argument. The library never
+ *    allocates, never frees, never synchronises the stream and keeps no state
+ *    between calls; it is safe to call from several host threads on different
+ *    streams with different workspaces.
+ *  - Ragged batches: sequence b owns pooled rows [key_off[b], key_off[b+1]) of the
+ *    packed key / KV arrays, so Np_b = key_off[b+1] - key_off[b] (int64, device).
+ *  - Positions: t0[b] (int32, device) is the absolute token position of query
+ *    row 0 of sequence b; row j sits at t = t0[b] + j ([HiSA issue] "Conventions").
+ *    The visible pooled prefix is V(t) = min(Np_b, floor((t+1)/r)) ([HiSA issue]
+ *    "The pooled stream and positions"). As on the page, the causal pooled mask
+ *    is applied only when L > 1; single-row calls treat all Np_b rows as visible.
+ *  - Head weights w are the RAW weights_proj(x) outputs (f32); the library applies
+ *    H_i^-1/2 * D_i^-1/2 once per head ([HiSA issue] "The indexer query and
+ *    per-head weights"). All selection scoring accumulates in f32.
+ *  - Selections are sets: entries of I / top_blk are written in ascending id order,
+ *    equal scores are broken by ascending id, -0.0 equals +0.0, and rows that have
+ *    fewer than k candidates are padded with -1.
+ *  - Host validation is synchronous: a bad argument returns HISA_EINVAL /
+ *    HISA_EDTYPE / HISA_EWORKSPACE before anything is enqueued. Kernels then run
+ *    asynchronously on `stream`; a failed launch returns HISA_ECUDA.
+ *  - Data the host cannot see (offsets, ids, per-sequence gates) is checked on the
+ *    device. A violation never faults: the kernel skips the access, writes -1 /
+ *    NEG where the page defines a neutral value, and ORs a HISA_DEV_* bit into the
+ *    status word held in the first 256 bytes of the workspace. Read it with
+ *    hisa_device_status(); clear it with hisa_workspace_init().
+ *  - Workspace: `ws` is device memory of at least hisa_workspace_bytes(op, desc)
+ *    bytes, 256-byte aligned. One workspace sized for the largest op may be shared
+ *    by consecutive calls on the same stream.
+ */
+#ifndef HISA_H
+#define HISA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define HISA_API __attribute__((visibility("default")))
+#else
+#define HISA_API
+#endif
+
+struct CUstream_st;                  /* the type behind cudaStream_t */
+typedef struct CUstream_st *hisa_stream_t;
+
+typedef enum {
+    HISA_OK = 0,
+    HISA_EINVAL = -1,     /* bad descriptor field, pointer, alignment or a host-checkable gate */
+    HISA_EDTYPE = -2,     /* dtype or shape combination without a kernel */
+    HISA_EWORKSPACE = -3, /* workspace missing, misaligned or too small */
+    HISA_ECUDA = -4,      /* a CUDA runtime call or a kernel launch failed */
+    HISA_EDEVICE = -5     /* hisa_device_status(): a kernel flagged bad data */
+} hisa_status;
+
+typedef enum { HISA_F32 = 0, HISA_BF16 = 1 } hisa_dtype;
+
+/* Bits of the device status word. */
+#define HISA_DEV_BAD_OFFSETS 0x1u /* offsets not monotone, Np_b > Np_max, or a capacity too small */
+#define HISA_DEV_GATE        0x2u /* a sequence failed Np_b >= index_block*index_keep; rows are -1 */
+#define HISA_DEV_BAD_ID      0x4u /* a selected id outside [-1, Np_b) reached the combine; skipped */
+#define HISA_DEV_NONFINITE   0x8u /* a select saw a non-finite score */
+#define HISA_DEV_BAD_BLOCK   0x10u /* a top_blk entry outside [0, nb_b); that row is written as -1 */
+
+/* Operation ids for hisa_workspace_bytes. */
+#define HISA_OP_INDEX_SCORES  0
+#define HISA_OP_BLOCK_MEANS   1
+#define HISA_OP_BLOCK_FILTER  2
+#define HISA_OP_SELECT_TOPK   3
+#define HISA_OP_FLAT_TOPK     4
+#define HISA_OP_SPARSE_ATTEND 5
+
+/* Indexer problem ([HiSA issue] "Configuration", "Flat selection", "HiSA decode path"). */
+typedef struct {
+    int32_t B;            /* sequences (>= 1) */
+    int32_t L;            /* query rows per sequence (>= 1; 1 = decode) */
+    int32_t H_i;          /* indexer heads, index_n_heads */
+    int32_t D_i;          /* indexer head dim, index_head_dim: 32, 64 or 128 */
+    int32_t r;            /* compress ratio (>= 1) */
+    int32_t index_topk;   /* k: pooled rows kept per query (1..2048) */
+    int32_t index_block;  /* b: HiSA block size in pooled rows (0 disables the hierarchy) */
+    int32_t index_keep;   /* keep: blocks kept by the coarse stage */
+    int64_t Np_max;       /* an upper bound of Np_b over the batch (sizes grids and workspace) */
+    int32_t q_dtype;      /* hisa_dtype of q: HISA_F32 or HISA_BF16 */
+    int32_t k_dtype;      /* hisa_dtype of the pooled indexer keys */
+} hisa_index_desc;
+
+/* Attention problem ([HiSA issue] "Consuming the selection: sparse combine"). */
+typedef struct {
+    int32_t B, L;         /* sequences, query rows per sequence */
+    int32_t H;            /* query heads sharing the single KV head: 8, 16 or 64 */
+    int32_t Dh;           /* head dim: 64, 128 or 512 (with H = 8, 16, 64 respectively) */
+    int32_t window;       /* sliding window: local row s is visible to t iff 0 <= t-s < window */
+    int32_t W_max;        /* rows allocated per sequence in local_kv */
+    int32_t r;            /* compress ratio, for V(t) */
+    int32_t k;            /* width of I (ignored when I == NULL) */
+    int64_t Np_max;       /* an upper bound of Np_b over the batch */
+    float scale;          /* softmax scale; <= 0 selects Dh^-1/2 */
+    int32_t q_dtype;      /* hisa_dtype of q; must equal kv_dtype */
+    int32_t kv_dtype;     /* hisa_dtype of local_kv and pooled_kv */
+} hisa_attn_desc;
+
+/* Bytes of device workspace `op` needs for `desc` (a hisa_index_desc* for ops 0-4,
+ * a hisa_attn_desc* for op 5). Always >= 256 for a valid desc; 0 for an invalid one.
+ * Pure host arithmetic: needs no GPU. */
+HISA_API size_t hisa_workspace_bytes(int32_t op, const void *desc);
+
+/* Clears the device status word of `ws` (asynchronous memset on `stream`). */
+HISA_API hisa_status hisa_workspace_init(void *ws, size_t ws_bytes, hisa_stream_t stream);
+
+/* Synchronises `stream`, then copies the status word of `ws` into *flags.
+ * Returns HISA_EDEVICE when any bit is set, HISA_OK otherwise. */
+HISA_API hisa_status hisa_device_status(const void *ws, hisa_stream_t stream, uint32_t *flags);
+
+/* A static, human-readable name for a status code. */
+HISA_API const char *hisa_status_string(int32_t status);
+
+/* Flat indexer scores ([HiSA issue] "Flat selection (baseline path)": s = relu(q.k),
+ * score = sum_h s * scale * w; NEG = -1e30 where p >= V(t0+j) when L > 1).
+ *   q      [B, L, H_i, D_i]  q_dtype      keys    [sum Np_b, D_i]  k_dtype
+ *   w      [B, L, H_i]       f32 raw      key_off [B+1] int64; t0 [B] int32
+ *   scores [B*L, ld_scores]  f32 out: row b*L+j holds Np_b scores; columns
+ *          [Np_b, ld_scores) are not written. ld_scores >= Np_max.
+ * With L > 1 this is the dense L x Np x (H_i*D_i) prefill contraction. */
+HISA_API hisa_status hisa_index_scores(const hisa_index_desc *desc, const void *q, const float *w,
+                              const void *keys, const int64_t *key_off, const int32_t *t0,
+                              float *scores, int64_t ld_scores, void *ws, size_t ws_bytes,
+                              hisa_stream_t stream);
+
+/* Block-mean representatives ([HiSA issue] "HiSA decode path": rep = mean over the
+ * index_block rows of each complete block; the tail [nb*b, Np) has no block).
+ *   means     [*, D_i] f32 out; sequence b's nb_b = floor(Np_b / b) means occupy rows
+ *             [means_off[b], means_off[b] + nb_b); means_off [B+1] int64 (device) must
+ *             leave room for nb_b rows (else HISA_DEV_BAD_OFFSETS and nothing is written).
+ *   first_block [B] int32 or NULL: blocks [first_block[b], nb_b) are (re)computed, so
+ *             a decode loop appends the newly completed blocks only. NULL = from 0.
+ * f32 sum in row order, divided by b. */
+HISA_API hisa_status hisa_block_means(const hisa_index_desc *desc, const void *keys,
+                             const int64_t *key_off, const int64_t *means_off,
+                             const int32_t *first_block, float *means, void *ws, size_t ws_bytes,
+                             hisa_stream_t stream);
+
+/* Coarse stage ([HiSA issue] "HiSA decode path" / "HiSA batched path": cscore over
+ * block means, top Kb = min(keep, nb) blocks; with L > 1 a block is eligible iff its
+ * first row is visible, else cscore = NEG).
+ *   means/means_off as written by hisa_block_means.
+ *   top_blk  [B, L, index_keep] int32 out, ascending block ids.
+ *   cscores  [B*L, ld_cscores] f32 out, optional (NULL): nb_b coarse scores per row.
+ * Host gate: index_block > 0 and index_block*index_keep >= index_topk, else
+ * HISA_EINVAL. Device gate: Np_b >= index_block*index_keep, else HISA_DEV_GATE and a
+ * row of -1. */
+HISA_API hisa_status hisa_block_filter(const hisa_index_desc *desc, const void *q, const float *w,
+                              const float *means, const int64_t *means_off,
+                              const int64_t *key_off, const int32_t *t0, int32_t *top_blk,
+                              float *cscores, int64_t ld_cscores, void *ws, size_t ws_bytes,
+                              hisa_stream_t stream);
+
+/* Fine stage ([HiSA issue] "HiSA decode path" / "HiSA batched path": candidates
+ * pos = top_blk[c / b]*b + c % b, exact rescoring, NEG where pos >= V(t0+j) when
+ * L > 1, top k, I = pos[sel]).
+ *   top_blk  [B, L, index_keep] int32 (any order; each entry in [0, nb_b)).
+ *   I        [B, L, index_topk] int32 out: absolute pooled ids, ascending.
+ *   fscores  [B*L, index_keep*index_block] f32 out, optional (NULL): candidate scores
+ *            in ascending pos order.
+ * Gates as hisa_block_filter. */
+HISA_API hisa_status hisa_select_topk(const hisa_index_desc *desc, const void *q, const float *w,
+                             const void *keys, const int64_t *key_off, const int32_t *t0,
+                             const int32_t *top_blk, int32_t *I, float *fscores, void *ws,
+                             size_t ws_bytes, hisa_stream_t stream);
+
+/* Flat selection ([HiSA issue] "Flat selection (baseline path)": top k = min(index_topk,
+ * Np_b) of the flat scores; the exact baseline and the path for 512 < Np < 1024).
+ *   I [B, L, index_topk] int32 out, ascending ids, -1 beyond min(index_topk, Np_b). */
+HISA_API hisa_status hisa_flat_topk(const hisa_index_desc *desc, const void *q, const float *w,
+                           const void *keys, const int64_t *key_off, const int32_t *t0,
+                           int32_t *I, void *ws, size_t ws_bytes, hisa_stream_t stream);
+
+/* Sparse combine ([HiSA issue] "Consuming the selection: sparse combine"): one softmax
+ * over the visible local rows, the gathered pooled rows P = pooled_kv[I] and the
+ * per-head sink, which joins the normaliser and carries no value; K = V.
+ *   q          [B, L, H, Dh]  q_dtype (already roped)
+ *   local_kv   [B, W_max, Dh] kv_dtype; local_len [B] int32 rows present (<= W_max);
+ *              local_pos0 [B] int32 absolute position of local row 0
+ *   pooled_kv  [sum Np_b, Dh] kv_dtype; kv_off [B+1] int64
+ *   I          [B, L, k] int32 pooled ids (-1 = skip), or NULL for the dense branch over
+ *              all Np_b rows. With L > 1 ids >= V(t0+j) are masked.
+ *   sinks      [H] f32;  t0 [B] int32
+ *   out        [B, L, H, Dh] f32 out
+ * Np_b == 0 gives local-only attention (branch 1 of the three-way branch). */
+HISA_API hisa_status hisa_sparse_attend(const hisa_attn_desc *desc, const void *q, const void *local_kv,
+                               const int32_t *local_len, const int32_t *local_pos0,
+                               const void *pooled_kv, const int64_t *kv_off, const int32_t *I,
+                               const float *sinks, const int32_t *t0, float *out, void *ws,
+                               size_t ws_bytes, hisa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HISA_H */

@@ -1,0 +1,272 @@
+"""GPU parity: every stage of the CUDA path against the oracle on seeded inputs.
+
+All calls go through the C ABI (libhisa.so via the ctypes binding). Comparison rules
+are those of oracle/parity.py: scores within 1e-5 * max(|o|, A), selections equal as
+sets up to near-ties of the k-th oracle score, attention max-abs 1e-2 (bf16 KV) /
+1e-4 (f32).
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from deepseek_sparse_attention_hisa_gb300 import binding as hb  # noqa: E402
+from deepseek_sparse_attention_hisa_gb300 import inputs  # noqa: E402
+from deepseek_sparse_attention_hisa_gb300.problem import Problem  # noqa: E402
+from oracle import hisa_oracle as O  # noqa: E402
+from oracle import parity as P  # noqa: E402
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from deepseek_sparse_attention_hisa_gb300 import build
+    build.build_library()
+    hb.lib()
+
+
+_CACHE = {}
+
+
+def gen(name):
+    if name not in _CACHE:
+        _CACHE.clear()
+        _CACHE[name] = inputs.generate(name)
+    return _CACHE[name]
+
+
+def np_(t):
+    return t.detach().cpu().numpy()
+
+
+def run_hisa(prob, with_scores=True):
+    """block means -> coarse -> fine -> combine; returns host copies of each stage."""
+    rows = prob.B * prob.L
+    nb_max = max(int(prob.nb.max()), 1)
+    cs = torch.full((rows, nb_max), 7.0, device="cuda") if with_scores else None
+    fs = torch.full((rows, prob.b * prob.keep), 7.0, device="cuda") if with_scores else None
+    prob.block_means()
+    prob.block_filter(cscores=cs)
+    prob.select_topk(fscores=fs)
+    if prob.has_attention:
+        prob.attend()
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    return dict(means=np_(prob.means), top_blk=np_(prob.top_blk), I=np_(prob.I),
+                cs=None if cs is None else np_(cs), fs=None if fs is None else np_(fs),
+                out=np_(prob.out) if prob.has_attention else None)
+
+
+def check_rows(data, prob, res, rows):
+    wl = data["wl"]
+    P.check_block_means(data, res["means"], np_(prob.means_off), wl.index_block)
+    for b, j in rows:
+        r = b * wl.L + j
+        P.check_coarse(data, b, j, res["top_blk"][r],
+                       None if res["cs"] is None else res["cs"][r], wl.index_block, prob.keep)
+        P.check_fine(data, b, j, res["top_blk"][r], res["I"][r],
+                     None if res["fs"] is None else res["fs"][r], wl.index_block, wl.index_topk)
+        if res["out"] is not None:
+            P.check_attend(data, b, j, res["out"][r], res["I"][r])
+
+
+def run_flat(prob, with_scores=True):
+    rows = prob.B * prob.L
+    sc = torch.full((rows, max(prob.Np_max, 1)), 7.0, device="cuda") if with_scores else None
+    if with_scores:
+        prob.index_scores(sc)
+    I = torch.full((rows, prob.k), -7, dtype=torch.int32, device="cuda")
+    prob.flat_topk(I=I)
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    return np_(I), None if sc is None else np_(sc)
+
+
+# ----------------------------------------------------------------------------
+# the five workloads
+# ----------------------------------------------------------------------------
+def test_tiny_decode_every_stage():
+    data = gen("tiny_decode")
+    prob = Problem(data)
+    res = run_hisa(prob)
+    check_rows(data, prob, res, [(0, 0)])
+    I, sc = run_flat(prob)
+    P.check_flat(data, 0, 0, I[0], 32, sc[0])
+    prob.attend(I=None)                        # dense branch over all 512 pooled rows
+    P.check_attend(data, 0, 0, np_(prob.out)[0], None)
+
+
+def test_v4flash_decode_every_stage():
+    data = gen("v4flash_decode")
+    prob = Problem(data)
+    res = run_hisa(prob)
+    check_rows(data, prob, res, [(0, 0)])
+    I, sc = run_flat(prob)
+    P.check_flat(data, 0, 0, I[0], 512, sc[0])
+    # the flat selection feeds the same combine
+    prob.attend(I=torch.as_tensor(I, device="cuda"))
+    P.check_attend(data, 0, 0, np_(prob.out)[0], I[0])
+
+
+def test_ragged_decode_all_sequences():
+    data = gen("ragged_decode")
+    prob = Problem(data)
+    res = run_hisa(prob)
+    check_rows(data, prob, res, [(b, 0) for b in range(data["wl"].B)])
+    I, _ = run_flat(prob, with_scores=False)
+    for b in (0, 7, 31):
+        P.check_flat(data, b, 0, I[b], 512)
+
+
+def test_prefill_sampled_rows():
+    data = gen("prefill")
+    prob = Problem(data)
+    res = run_hisa(prob, with_scores=True)
+    L = data["wl"].L
+    rng = np.random.default_rng(0)
+    rows = sorted({0, 1, 2, 255, 256, 511, 512, 2047, L - 2, L - 1} |
+                  set(rng.integers(0, L, 6).tolist()))
+    check_rows(data, prob, res, [(0, j) for j in rows])
+    # the dense L x Np x (H_i * D_i) contraction, sampled rows
+    sc = torch.empty((L, prob.Np_max), device="cuda")
+    prob.index_scores(sc)
+    torch.cuda.synchronize()
+    sc = np_(sc)
+    for j in rows[:6]:
+        q, w = data["q_idx"][0, j], data["w"][0, j]
+        o = O.flat_scores(q[None], w[None], data["keys"], int(data["t0"][0]) + j, 4, causal=True)[0]
+        P.check_scores(sc[j], o, O.error_scale(q, w, data["keys"]), what=f"prefill score row {j}")
+
+
+@pytest.mark.parametrize("keep", [16, 64])
+def test_long_context_flat_and_hisa(keep):
+    data = gen("long_context")
+    prob = Problem(data, index_keep=keep)
+    res = run_hisa(prob, with_scores=True)
+    check_rows(data, prob, res, [(0, 0)])
+    I, sc = run_flat(prob)
+    P.check_flat(data, 0, 0, I[0], 512, sc[0])
+    recall = len(set(res["I"][0].tolist()) & set(I[0].tolist())) / 512
+    print(f"long context keep={keep}: recall vs flat = {recall:.3f}")
+    assert recall > 0.0
+
+
+# ----------------------------------------------------------------------------
+# edge cases: several tiles, ragged tails, short sequences, L > 1 causality
+# ----------------------------------------------------------------------------
+def small(**kw):
+    return inputs.generate(inputs.small_workload(**kw))
+
+
+def test_ragged_tails_and_tiles():
+    # Np not a multiple of b, several 256-row score tiles, f32 and bf16 keys
+    for kd in ("f32", "bf16"):
+        data = small(B=3, Np=(700, 1000, 1333), key_dtype=kd, kv_dtype=kd, seed=5)
+        data["t0"][:] = 4 * data["Np"] - 1
+        prob = Problem(data)
+        res = run_hisa(prob)
+        check_rows(data, prob, res, [(b, 0) for b in range(3)])
+        for b in range(3):
+            assert np.all(res["I"][b] < (data["Np"][b] // 16) * 16)   # tail exclusion
+        I, sc = run_flat(prob)
+        for b in range(3):
+            P.check_flat(data, b, 0, I[b], 32, sc[b])
+
+
+def test_flat_pads_when_Np_below_k_and_dense_branch():
+    data = small(Np=(20,), seed=6)
+    prob = Problem(data)
+    I, sc = run_flat(prob)
+    assert np.all(I[0, 20:] == -1)
+    P.check_flat(data, 0, 0, I[0], 32, sc[0])
+    prob.attend(I=None)
+    P.check_attend(data, 0, 0, np_(prob.out)[0], None)
+    prob.attend(I=torch.as_tensor(I, device="cuda"))      # -1 padding is skipped
+    P.check_attend(data, 0, 0, np_(prob.out)[0], I[0])
+
+
+def test_local_only_attention():
+    data = small(Np=(0,), seed=7)
+    prob = Problem(data)
+    prob.attend(I=None)
+    torch.cuda.synchronize()
+    P.check_attend(data, 0, 0, np_(prob.out)[0], None)
+
+
+@pytest.mark.parametrize("t0", [60, 1900])
+def test_batched_rows_with_few_visible(t0):
+    # L > 1. With t0 = 60 every row sees fewer than k = 32 pooled rows and fewer than
+    # keep eligible blocks (masked ids are selected, then re-masked by the combine);
+    # with t0 = 1900 rows see partially visible blocks at the edge of V(t).
+    data = small(L=48, Np=(512,), seed=8, t0=t0)
+    prob = Problem(data)
+    res = run_hisa(prob)
+    check_rows(data, prob, res, [(0, j) for j in range(48)])
+    I, sc = run_flat(prob)
+    for j in range(0, 48, 5):
+        P.check_flat(data, 0, j, I[j], 32, sc[j])
+
+
+def test_device_gate_and_bad_ids_are_flagged_not_faulted():
+    data = small(B=2, Np=(512, 40), seed=9)   # sequence 1 fails Np >= b * keep = 64
+    prob = Problem(data)
+    prob.block_means()
+    prob.block_filter()
+    prob.select_topk()
+    torch.cuda.synchronize()
+    assert prob.status() & hb.DEV_GATE
+    assert np.all(np_(prob.top_blk)[1] == -1) and np.all(np_(prob.I)[1] == -1)
+    hb.workspace_init(prob.ws)
+    # out-of-range ids in I are skipped and flagged; in-range ones still attend
+    I = torch.as_tensor(np.array([[3, 5, 10 ** 6, -5] + [-1] * 28] * 2, dtype=np.int32),
+                        device="cuda")
+    prob.attend(I=I)
+    torch.cuda.synchronize()
+    assert prob.status() & hb.DEV_BAD_ID
+    clean = np.array([3, 5, -1, -1] + [-1] * 28)
+    P.check_attend(data, 0, 0, np_(prob.out)[0], clean)
+    hb.workspace_init(prob.ws)
+    tb = torch.as_tensor(np.array([[0, 1, 2, 99], [0, 1, 2, 3]], dtype=np.int32), device="cuda")
+    prob.select_topk(top_blk=tb)
+    torch.cuda.synchronize()
+    st = prob.status()
+    assert st & hb.DEV_BAD_BLOCK and np.all(np_(prob.I)[0] == -1)
+
+
+def test_host_validation_raises():
+    data = small(seed=10)
+    prob = Problem(data)
+    bad = hb.IndexDesc.from_buffer_copy(prob.idesc)
+    bad.D_i = 48
+    with pytest.raises(hb.HisaError) as e:
+        hb.flat_topk(bad, prob.q_idx, prob.w, prob.keys, prob.key_off, prob.t0, prob.I, prob.ws)
+    assert e.value.status == hb.HISA_EDTYPE
+    small_ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(hb.HisaError) as e:
+        hb.flat_topk(prob.idesc, prob.q_idx, prob.w, prob.keys, prob.key_off, prob.t0, prob.I,
+                     small_ws)
+    assert e.value.status == hb.HISA_EWORKSPACE
+
+
+def test_graph_capture_replays_the_step():
+    data = small(B=4, Np=(512, 600, 700, 1024), key_dtype="bf16", kv_dtype="bf16", seed=11)
+    data["t0"][:] = 4 * data["Np"] - 1
+    prob = Problem(data)
+    prob.block_means()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        prob.hisa_step(stream=s)                 # warm-up (sets kernel attributes)
+    torch.cuda.synchronize()
+    eager_I, eager_out = np_(prob.I).copy(), np_(prob.out).copy()
+    prob.I.fill_(-7)
+    prob.out.fill_(0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        prob.hisa_step(stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(np_(prob.I), eager_I)
+    assert np.array_equal(np_(prob.out), eager_out)
