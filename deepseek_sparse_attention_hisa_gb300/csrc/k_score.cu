@@ -196,7 +196,11 @@ __global__ void k_block_means(MeansParams p) {
 
 cudaError_t launch_block_means(const MeansParams &p, int64_t nb_max, cudaStream_t s) {
     if (nb_max <= 0) return cudaSuccess;
-    const unsigned gx = (unsigned)(nb_max < 2048 ? nb_max : 2048);
+    // Blocks [first_block, nb) are walked grid-stride; size the grid from the batch so
+    // an incremental update (few new blocks per sequence) launches few idle CTAs.
+    int64_t per_seq = (kTargetCtas + p.B - 1) / p.B;
+    if (per_seq > nb_max) per_seq = nb_max;
+    const unsigned gx = (unsigned)(per_seq < 1 ? 1 : per_seq);
     dim3 grid(gx, (unsigned)p.B);
     const int threads = p.D_i;
     if (p.keys_bf16)

@@ -95,14 +95,15 @@ def combined_scores(q: np.ndarray, w: np.ndarray, rows: np.ndarray) -> np.ndarra
 
 
 def error_scale(q: np.ndarray, w: np.ndarray, rows: np.ndarray) -> np.ndarray:
-    """A[p] = sum_h |w_h * scale| * relu(q_h . rows_p): the magnitude an f32 sum of
-    the same terms is rounded against. Used for tolerances only."""
+    """A[p] = sum_h |w_h * scale| * sum_d |q_hd * rows_pd|: the magnitude of every
+    product that enters score[p], which is what an f32 evaluation of the two nested
+    sums is rounded against (a head's dot product can cancel to near zero while its
+    terms stay large). Used for tolerances only."""
     q = to_f64(q)
     w = to_f64(w)
     rows = to_f64(rows)
     H_i, D_i = q.shape
-    s = np.maximum(q @ rows.T, 0.0)
-    return np.abs(w * head_scale(H_i, D_i)) @ s
+    return np.abs(w * head_scale(H_i, D_i)) @ (np.abs(q) @ np.abs(rows).T)
 
 
 # ----------------------------------------------------------------------------

@@ -1,9 +1,10 @@
 """Comparison rules between the CUDA path and the oracle (test infrastructure only).
 
 Tolerances (the numbers are those fixed for this path; the arithmetic behind them):
-  * scores: |g - o| <= 1e-5 * max(|o|, A), A = sum_h |w_h * scale| * relu(q_h . row):
-    the f32 sum of the head terms is rounded against A, not against |o|, which can
-    cancel (w has both signs). Masked entries must be exactly -1e30.
+  * scores: |g - o| <= 1e-5 * max(|o|, A), A = sum_h |w_h * scale| * sum_d |q_hd row_d|:
+    an f32 evaluation of the nested sums is rounded against the magnitude of its terms,
+    not against |o|, which can cancel (w has both signs, and a head's dot product can
+    sit near zero). Masked entries must be exactly -1e30.
   * selections (unordered sets): equal, except that an id may differ between the two
     sides when its oracle score lies within 1e-5 * max(|s_k|, A_k, A_id) of the k-th
     oracle score s_k (a near-tie that f32 rounding may order either way).
