@@ -17,7 +17,8 @@ LIB_PATH = os.path.join(_PKG, "libhisa.so")
 
 HISA_OK, HISA_EINVAL, HISA_EDTYPE, HISA_EWORKSPACE, HISA_ECUDA, HISA_EDEVICE = 0, -1, -2, -3, -4, -5
 HISA_F32, HISA_BF16 = 0, 1
-DEV_BAD_OFFSETS, DEV_GATE, DEV_BAD_ID, DEV_NONFINITE, DEV_BAD_BLOCK = 0x1, 0x2, 0x4, 0x8, 0x10
+DEV_BAD_OFFSETS, DEV_GATE, DEV_BAD_ID, DEV_NONFINITE, DEV_BAD_BLOCK, DEV_TIMEOUT = \
+    0x1, 0x2, 0x4, 0x8, 0x10, 0x20
 OP_INDEX_SCORES, OP_BLOCK_MEANS, OP_BLOCK_FILTER, OP_SELECT_TOPK, OP_FLAT_TOPK, OP_SPARSE_ATTEND = \
     range(6)
 

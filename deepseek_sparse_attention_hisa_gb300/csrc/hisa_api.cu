@@ -70,8 +70,11 @@ int pick_nsplit(int64_t queries, int64_t list_len, int64_t *rows_per_split) {
     return (int)(ns < 1 ? 1 : ns);
 }
 
+// Upper bound of the attended rows of one query row: the visible local window plus
+// the pooled rows (all of them for the dense branch).
 int64_t attn_list_len(const hisa_attn_desc *d, bool dense) {
-    return (int64_t)d->W_max + (dense ? d->Np_max : (int64_t)d->k);
+    const int64_t local = d->W_max < d->window ? d->W_max : d->window;
+    return local + (dense ? d->Np_max : (int64_t)d->k);
 }
 
 size_t attn_part_bytes(const hisa_attn_desc *d, bool dense) {
@@ -329,7 +332,9 @@ hisa_status hisa_sparse_attend(const hisa_attn_desc *d, const void *q, const voi
     p.rows_per_split = (int)per;
     p.kv_bf16 = d->kv_dtype == HISA_BF16;
     p.status = status_of(ws);
-    return from_cuda(launch_attend_simt(p, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (attend_tc_supported(d->H, d->Dh, p.kv_bf16)) return from_cuda(launch_attend_tc(p, s));
+    return from_cuda(launch_attend_simt(p, s));
 }
 
 }  // extern "C"

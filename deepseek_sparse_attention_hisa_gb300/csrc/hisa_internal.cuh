@@ -118,7 +118,10 @@ cudaError_t launch_scores_simt(const ScoreParams &p, cudaStream_t s);
 cudaError_t launch_select(const SelectParams &p, int64_t n_max, cudaStream_t s);
 cudaError_t launch_block_means(const MeansParams &p, int64_t nb_max, cudaStream_t s);
 cudaError_t launch_attend_simt(const AttnParams &p, cudaStream_t s);
+cudaError_t launch_attend_combine(const AttnParams &p, cudaStream_t s);
+cudaError_t launch_attend_tc(const AttnParams &p, cudaStream_t s);
 int attend_simt_supported(int H, int Dh);
+int attend_tc_supported(int H, int Dh, int kv_bf16);
 int attend_chunk_rows();
 
 }  // namespace hisa

@@ -77,16 +77,21 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend_simt(AttnParams p) {
         if (tid == 0 && split == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
         Np = 0;
     }
-    int nl = p.local_len[bq];
+    int64_t nl = p.local_len[bq];
     nl = nl < 0 ? 0 : (nl > p.W_max ? p.W_max : nl);
+    const int64_t pos0 = p.local_pos0[bq];
+    // only the visible local window [lo, hi) enters the list
+    int64_t lo = t - p.window + 1 - pos0, hi = t - pos0 + 1;
+    lo = lo < 0 ? 0 : lo;
+    hi = hi > nl ? nl : hi;
+    const int64_t nloc = hi > lo ? hi - lo : 0;
     const int64_t npool = p.I ? (int64_t)p.k : Np;
-    const int64_t ntot = nl + npool;
+    const int64_t ntot = nloc + npool;
     const int64_t e0 = (int64_t)split * p.rows_per_split;
     int64_t e1 = e0 + p.rows_per_split;
     if (e1 > ntot) e1 = ntot;
     const int64_t V = p.causal ? visible_len(t, p.r, Np) : Np;
-    const int64_t pos0 = p.local_pos0[bq];
-    const T *local = reinterpret_cast<const T *>(p.local_kv) + (int64_t)bq * p.W_max * DH;
+    const T *local = reinterpret_cast<const T *>(p.local_kv) + ((int64_t)bq * p.W_max + lo) * DH;
     const T *pooled = reinterpret_cast<const T *>(p.pooled_kv) + k0 * DH;
     const int32_t *Irow = p.I ? p.I + (int64_t)row * p.k : nullptr;
 
@@ -110,11 +115,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend_simt(AttnParams p) {
             const int64_t e = c0 + tid;
             const T *ptr = nullptr;
             if (e < e1) {
-                if (e < nl) {
-                    const int64_t d = t - (pos0 + e);
-                    if (d >= 0 && d < p.window) ptr = local + e * DH;
+                if (e < nloc) {
+                    ptr = local + e * DH;
                 } else {
-                    const int64_t kk = e - nl;
+                    const int64_t kk = e - nloc;
                     const int64_t id = Irow ? (int64_t)Irow[kk] : kk;
                     if (id >= Np || id < -1) {
                         flag(p.status, HISA_DEV_BAD_ID);
@@ -247,6 +251,17 @@ __global__ void k_attend_combine(AttnParams p) {
     }
 }
 
+cudaError_t launch_attend_combine(const AttnParams &p, cudaStream_t s) {
+    dim3 g2((unsigned)(p.B * p.L), (unsigned)p.H);
+    switch (p.Dh) {
+        case 64: k_attend_combine<64><<<g2, 64, 0, s>>>(p); break;
+        case 128: k_attend_combine<128><<<g2, 128, 0, s>>>(p); break;
+        case 512: k_attend_combine<512><<<g2, 256, 0, s>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 template <int H, int DH, typename T>
 static cudaError_t launch_attend_t(const AttnParams &p, cudaStream_t s) {
     using S = AttnSmem<H, DH, T>;
@@ -257,9 +272,7 @@ static cudaError_t launch_attend_t(const AttnParams &p, cudaStream_t s) {
     k_attend_simt<H, DH, T><<<grid, kAttnThreads, S::bytes, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.nsplit == 1) return e;
-    dim3 g2((unsigned)(p.B * p.L), (unsigned)H);
-    k_attend_combine<DH><<<g2, DH < 256 ? DH : 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_attend_combine(p, s);
 }
 
 int attend_simt_supported(int H, int Dh) {

@@ -1,0 +1,415 @@
+// Sparse combine on the sm_103a tensor cores for the DeepSeek-V4 shape (64 query heads
+// sharing one 512-dim bf16 KV head), ([HiSA issue] "Consuming the selection: sparse
+// combine").
+//
+// One CTA owns a range of one query row's attended-row list (the visible local window
+// rows, then the gathered pooled rows). The list streams through shared memory in tiles
+// of kTR rows; per tile:
+//   S  = Q . K^T      tcgen05, M = 64 heads, N = kTR rows, K = 512   (TMEM, 2 buffers)
+//   P  = exp2(S * scale*log2e - m) per head, in the thread that owns the head's TMEM lane
+//   O^T += V^T . P^T  tcgen05, M = 128 dims x 4, N = 64 heads, K = kTR  (TMEM, f32)
+// K = V, so the same staged tile is the B operand of the first product (K-major) and the
+// A operand of the second (MN-major). The running max m is lazy: O^T and l are rescaled
+// only when a tile's max exceeds m by more than 8 (log2 units), so p <= 256.
+// Warp roles: 0-3 softmax + epilogue (warp w reads TMEM lanes 32w..32w+31), 4 MMA issue
+// and TMEM owner, 5-6 producers (cp.async gather, 128-byte swizzle, zero-fill of rows
+// that are invisible or past the list). Every mbarrier wait is bounded; a timeout sets
+// HISA_DEV_TIMEOUT, raises a shared abort flag and the CTA drains and exits.
+#include "hisa_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace hisa {
+namespace {
+
+using namespace tc;
+
+constexpr int kH = 64, kDH = 512, kTR = 32, kSlots = 4;
+constexpr int kSoftWarps = 4, kMmaWarp = 4, kProdWarp0 = 5, kProdWarps = 2;
+constexpr int kThreads = 32 * (kSoftWarps + 1 + kProdWarps);
+constexpr uint32_t kQBytes = kH * kDH * 2;            // 64 KiB, K-major, 8 chunks of 64 dims
+constexpr uint32_t kSlotBytes = kTR * kDH * 2;        // 32 KiB per staged tile
+constexpr uint32_t kPBytes = kH * 128;                // P^T: 64 heads x (up to 64 rows) bf16
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffKV = kOffQ + kQBytes;
+constexpr uint32_t kOffP = kOffKV + kSlots * kSlotBytes;
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+// barriers: full[4] empty[4] s_full[2] s_free[2] p_full[2] p_free[2] q_full drain
+constexpr int kBarFull = 0, kBarEmpty = 4, kBarSFull = 8, kBarSFree = 10, kBarPFull = 12,
+              kBarPFree = 14, kBarQ = 16, kBarDrain = 17, kNumBars = 18;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffMisc + 1024 + 1024;  // misc + 1 KiB alignment slack
+constexpr uint32_t kTmemCols = 512;                   // S: cols [0,64), O^T: [64, 320)
+constexpr uint32_t kColO = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazy = 8.0f;
+
+struct Misc {
+    uint32_t tmem;
+    int abort;
+    uint32_t mask[kSlots];
+    float alpha[kH];
+    float factor[kH];
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    for (uint32_t i = 0; i < (1u << 22); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && *abort) return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void named_sync_soft() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t named_or_soft(uint32_t v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"(v) : "memory");
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    Misc *misc = reinterpret_cast<Misc *>(smem + kOffMisc);
+    volatile int *abort = &misc->abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = blockIdx.x, split = blockIdx.y;
+    const int bq = row / p.L, j = row - bq * p.L;
+    const int64_t t = (int64_t)p.t0[bq] + j;
+    const int64_t k0 = p.kv_off[bq];
+    int64_t Np = p.kv_off[bq + 1] - k0;
+    const bool bad_off = Np < 0 || Np > p.Np_max;
+    if (bad_off) Np = 0;
+    // visible local window rows [lo, hi) of this query row
+    int64_t nl = p.local_len[bq];
+    nl = nl < 0 ? 0 : (nl > p.W_max ? p.W_max : nl);
+    const int64_t pos0 = p.local_pos0[bq];
+    int64_t lo = t - p.window + 1 - pos0, hi = t - pos0 + 1;
+    lo = lo < 0 ? 0 : lo;
+    hi = hi > nl ? nl : hi;
+    const int64_t nloc = hi > lo ? hi - lo : 0;
+    const int64_t npool = p.I ? (int64_t)p.k : Np;
+    const int64_t ntot = nloc + npool;
+    const int64_t e0 = (int64_t)split * p.rows_per_split;
+    int64_t e1 = e0 + p.rows_per_split;
+    e1 = e1 > ntot ? ntot : e1;
+    const int T = e1 > e0 ? (int)((e1 - e0 + kTR - 1) / kTR) : 0;
+    const int64_t V = p.causal ? visible_len(t, p.r, Np) : Np;
+    const __nv_bfloat16 *local =
+        reinterpret_cast<const __nv_bfloat16 *>(p.local_kv) + ((int64_t)bq * p.W_max + lo) * kDH;
+    const __nv_bfloat16 *pooled = reinterpret_cast<const __nv_bfloat16 *>(p.pooled_kv) + k0 * kDH;
+    const int32_t *Irow = p.I ? p.I + (int64_t)row * p.k : nullptr;
+
+    if (tid == 0) {
+        for (int b = 0; b < kNumBars; ++b) {
+            uint32_t cnt = 1;
+            if (b >= kBarFull && b < kBarFull + kSlots) cnt = kProdWarps * 32 + 1;
+            if (b == kBarSFree || b == kBarSFree + 1 || b == kBarPFull || b == kBarPFull + 1)
+                cnt = kSoftWarps * 32;
+            if (b == kBarQ) cnt = kProdWarps * 32;
+            mbar_init(&bars[b], cnt);
+        }
+        mbar_fence_init();
+        misc->abort = 0;
+        if (bad_off && split == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&misc->tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = misc->tmem;
+
+    if (warp >= kProdWarp0) {
+        // ---------------- producers ----------------
+        const int pt = tid - kProdWarp0 * 32;                 // 0..63: one 16-byte unit per row
+        const uint32_t qb = sbase + kOffQ;
+        const __nv_bfloat16 *qrow = reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)row * kH * kDH;
+        for (int h = 0; h < kH; ++h)
+            cp_async16(qb + (pt >> 3) * (kH * 128) + sw128_offset(h, (pt & 7) * 8),
+                       qrow + h * kDH + pt * 8);
+        cp_async_arrive(&bars[kBarQ]);
+        bool ok = true;
+        for (int i = 0; i < T && ok; ++i) {
+            const int s = i % kSlots;
+            if (i >= kSlots && !wait_bar(&bars[kBarEmpty + s], ((i / kSlots) - 1) & 1, abort)) {
+                ok = false;
+                break;
+            }
+            // lane r resolves row r of the tile
+            const int64_t e = e0 + (int64_t)i * kTR + lane;
+            const __nv_bfloat16 *src = nullptr;
+            if (e < e1) {
+                if (e < nloc) {
+                    src = local + e * kDH;
+                } else {
+                    const int64_t kk = e - nloc;
+                    const int64_t id = Irow ? (int64_t)Irow[kk] : kk;
+                    if (id >= Np || id < -1) {
+                        if (pt < 32) flag(p.status, HISA_DEV_BAD_ID);
+                    } else if (id >= 0 && id < V) {
+                        src = pooled + id * kDH;
+                    }
+                }
+            }
+            const uint32_t valid = __ballot_sync(0xffffffffu, src != nullptr);
+            const uint32_t slot = sbase + kOffKV + s * kSlotBytes;
+            const uint32_t dst0 = slot + (pt >> 3) * (kTR * 128);
+            for (int r = 0; r < kTR; ++r) {
+                const __nv_bfloat16 *rs = reinterpret_cast<const __nv_bfloat16 *>(
+                    __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(src), r));
+                const bool v = (valid >> r) & 1u;
+                cp_async16_zfill(dst0 + sw128_offset(r, (pt & 7) * 8),
+                                 v ? static_cast<const void *>(rs + pt * 8) : p.q, v);
+            }
+            if (pt == 0) misc->mask[s] = valid;
+            cp_async_arrive(&bars[kBarFull + s]);
+            if (pt == 0) mbar_arrive(&bars[kBarFull + s]);
+        }
+        cp_async_wait_all();
+        if (!ok) {
+            *abort = 1;
+            flag(p.status, HISA_DEV_TIMEOUT);
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0 && T > 0) {
+            const uint32_t id_s = idesc_bf16_f32(64, kTR, 0, 0);
+            const uint32_t id_o = idesc_bf16_f32(128, 64, 1, 0);
+            const uint32_t qb = sbase + kOffQ;
+            bool ok = wait_bar(&bars[kBarQ], 0, abort);
+            auto issue_s = [&](int i) -> bool {
+                const int s = i % kSlots, sb = i & 1;
+                if (!wait_bar(&bars[kBarFull + s], (i / kSlots) & 1, abort)) return false;
+                if (i >= 2 && !wait_bar(&bars[kBarSFree + sb], ((i >> 1) - 1) & 1, abort)) return false;
+                fence_after_sync();
+                const uint32_t slot = sbase + kOffKV + s * kSlotBytes;
+#pragma unroll 1
+                for (int ks = 0; ks < kDH / 16; ++ks) {
+                    const uint32_t ko = (ks >> 2), kb = (ks & 3) * 32;
+                    const uint64_t a = smem_desc_sw128(qb + ko * (kH * 128) + kb, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(slot + ko * (kTR * 128) + kb, 16, 1024);
+                    mma_bf16(tmem + sb * 32, a, b, id_s, ks > 0);
+                }
+                mma_commit(&bars[kBarSFull + sb]);
+                return true;
+            };
+            auto issue_pv = [&](int i) -> bool {
+                const int s = i % kSlots, pb = i & 1;
+                if (!wait_bar(&bars[kBarPFull + pb], (i >> 1) & 1, abort)) return false;
+                fence_after_sync();
+                const uint32_t slot = sbase + kOffKV + s * kSlotBytes;
+                const uint32_t pbase = sbase + kOffP + pb * kPBytes;
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                    for (int ks = 0; ks < kTR / 16; ++ks) {
+                        const uint64_t a = smem_desc_sw128(slot + (2 * mt) * (kTR * 128) + ks * 2048,
+                                                           kTR * 128, 1024);
+                        const uint64_t b = smem_desc_sw128(pbase + ks * 32, 16, 1024);
+                        mma_bf16(tmem + kColO + mt * 64, a, b, id_o, (i > 0 || ks > 0) ? 1u : 0u);
+                    }
+                mma_commit(&bars[kBarEmpty + s]);
+                mma_commit(&bars[kBarPFree + pb]);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int i = 1; i < T && ok; ++i) {
+                ok = issue_s(i);
+                if (ok) ok = issue_pv(i - 1);
+            }
+            if (ok) ok = issue_pv(T - 1);
+            if (!ok) {
+                *abort = 1;
+                flag(p.status, HISA_DEV_TIMEOUT);
+            }
+            // drain: every MMA issued by this thread has completed before TMEM is freed
+            mma_commit(&bars[kBarDrain]);
+            wait_bar(&bars[kBarDrain], 0, abort);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- softmax + epilogue (warps 0-3) ----------------
+        const bool active = lane < 16;
+        const int h = warp * 16 + lane;                 // head owned by this lane (M = 64 layout)
+        const float c2 = p.scale * kLog2e;
+        const float sink2 = active ? p.sinks[h] * kLog2e : 0.f;
+        float m2 = -INFINITY, l = 0.f;
+        uint32_t pfree_seen[2] = {0u, 0u};
+        bool ok = true;
+        auto wait_pfree = [&](int buf, uint32_t phase) -> bool {   // PV of tile (2*phase + buf) done
+            while (pfree_seen[buf] <= phase) {
+                if (!wait_bar(&bars[kBarPFree + buf], pfree_seen[buf] & 1, abort)) return false;
+                ++pfree_seen[buf];
+            }
+            return true;
+        };
+        for (int i = 0; i < T && ok; ++i) {
+            const int s = i % kSlots, sb = i & 1;
+            if (!wait_bar(&bars[kBarFull + s], (i / kSlots) & 1, abort) ||
+                !wait_bar(&bars[kBarSFull + sb], (i >> 1) & 1, abort)) {
+                ok = false;
+                break;
+            }
+            fence_after_sync();
+            const uint32_t mask = misc->mask[s];
+            float v[kTR];
+            {
+                float a[16], b[16];
+                const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + sb * 32;
+                tmem_ld16(ta, a);
+                tmem_ld16(ta + 16, b);
+                tmem_ld_wait();
+#pragma unroll
+                for (int r = 0; r < 16; ++r) { v[r] = a[r]; v[16 + r] = b[r]; }
+            }
+            fence_before_sync();
+            mbar_arrive(&bars[kBarSFree + sb]);
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < kTR; ++r) {
+                v[r] = ((mask >> r) & 1u) ? v[r] * c2 : -INFINITY;
+                tmax = fmaxf(tmax, v[r]);
+            }
+            float alpha = 1.f;
+            uint32_t resc = 0;
+            if (active && tmax > m2 + kLazy) {
+                if (m2 != -INFINITY) {
+                    alpha = exp2f(m2 - tmax);
+                    resc = 1;
+                }
+                m2 = tmax;
+            }
+            // P buffer (i & 1) is free once PV(i - 2) has completed
+            if (i >= 2 && !wait_pfree(i & 1, (uint32_t)((i >> 1) - 1))) { ok = false; break; }
+            float sum = 0.f;
+            uint32_t packed[kTR / 2];
+#pragma unroll
+            for (int r = 0; r < kTR; r += 2) {
+                const float p0 = (v[r] == -INFINITY) ? 0.f : exp2f(v[r] - m2);
+                const float p1 = (v[r + 1] == -INFINITY) ? 0.f : exp2f(v[r + 1] - m2);
+                sum += p0 + p1;
+                __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
+                packed[r / 2] = *reinterpret_cast<uint32_t *>(&pr);
+            }
+            l = l * alpha + sum;
+            if (active) {
+                uint8_t *pb = smem + kOffP + (i & 1) * kPBytes;
+#pragma unroll
+                for (int u = 0; u < kTR / 8; ++u)
+                    *reinterpret_cast<uint4 *>(pb + sw128_offset(h, u * 8)) =
+                        make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+            }
+            if (named_or_soft(resc)) {
+                // rescale O^T columns of the heads whose reference max moved up
+                if (active) misc->alpha[h] = alpha;
+                named_sync_soft();
+                if (!wait_pfree((i - 1) & 1, (uint32_t)((i - 1) >> 1))) { ok = false; break; }
+                fence_after_sync();
+#pragma unroll 1
+                for (int mt = 0; mt < 4; ++mt)
+#pragma unroll 1
+                    for (int c = 0; c < 64; c += 16) {
+                        float o[16];
+                        const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + kColO + mt * 64 + c;
+                        tmem_ld16(ta, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) o[q] *= misc->alpha[c + q];
+                        tmem_st16(ta, o);
+                    }
+                tmem_st_wait();
+            }
+            fence_async_smem();
+            fence_before_sync();
+            mbar_arrive(&bars[kBarPFull + (i & 1)]);
+        }
+        // ---------------- epilogue ----------------
+        if (ok && T > 0) ok = wait_pfree((T - 1) & 1, (uint32_t)((T - 1) >> 1));
+        if (!ok) {
+            *abort = 1;
+            flag(p.status, HISA_DEV_TIMEOUT);
+        }
+        fence_after_sync();
+        const bool have_o = ok && T > 0;
+        if (p.nsplit == 1) {
+            if (active) {
+                const float M = fmaxf(m2, sink2);
+                const float wm = (m2 == -INFINITY) ? 0.f : exp2f(m2 - M);
+                misc->factor[h] = wm / (l * wm + exp2f(sink2 - M));
+            }
+            named_sync_soft();
+            float *out = p.out + (int64_t)row * kH * kDH;
+            for (int mt = 0; mt < 4; ++mt) {
+                const int d = mt * 128 + warp * 32 + lane;
+                for (int c = 0; c < 64; c += 16) {
+                    float o[16];
+                    if (have_o) {
+                        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + kColO + mt * 64 + c, o);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) o[q] = 0.f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) out[(c + q) * kDH + d] = o[q] * misc->factor[c + q];
+                }
+            }
+        } else {
+            float *base = p.part + ((int64_t)row * p.nsplit + split) * kH * (kDH + 2);
+            if (active) {
+                base[h * (kDH + 2)] = (m2 == -INFINITY) ? -INFINITY : m2 / kLog2e;
+                base[h * (kDH + 2) + 1] = l;
+            }
+            for (int mt = 0; mt < 4; ++mt) {
+                const int d = mt * 128 + warp * 32 + lane;
+                for (int c = 0; c < 64; c += 16) {
+                    float o[16];
+                    if (have_o) {
+                        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + kColO + mt * 64 + c, o);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) o[q] = 0.f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) base[(c + q) * (kDH + 2) + 2 + d] = o[q];
+                }
+            }
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+int attend_tc_supported(int H, int Dh, int kv_bf16) { return H == kH && Dh == kDH && kv_bf16; }
+
+cudaError_t launch_attend_tc(const AttnParams &p, cudaStream_t s) {
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        k_attend_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (attr != cudaSuccess) return attr;
+    dim3 grid((unsigned)(p.B * p.L), (unsigned)p.nsplit);
+    k_attend_tc<<<grid, kThreads, kSmemBytes, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.nsplit == 1) return e;
+    return launch_attend_combine(p, s);
+}
+
+}  // namespace hisa

@@ -74,6 +74,7 @@ typedef enum { HISA_F32 = 0, HISA_BF16 = 1 } hisa_dtype;
 #define HISA_DEV_BAD_ID      0x4u /* a selected id outside [-1, Np_b) reached the combine; skipped */
 #define HISA_DEV_NONFINITE   0x8u /* a select saw a non-finite score */
 #define HISA_DEV_BAD_BLOCK   0x10u /* a top_blk entry outside [0, nb_b); that row is written as -1 */
+#define HISA_DEV_TIMEOUT     0x20u /* a kernel gave up on a bounded wait; its outputs are incomplete */
 
 /* Operation ids for hisa_workspace_bytes. */
 #define HISA_OP_INDEX_SCORES  0

@@ -270,3 +270,47 @@ def test_graph_capture_replays_the_step():
     torch.cuda.synchronize()
     assert np.array_equal(np_(prob.I), eager_I)
     assert np.array_equal(np_(prob.out), eager_out)
+
+
+def v4_small(**kw):
+    base = dict(H_i=64, D_i=128, index_block=64, index_keep=16, index_topk=512, H=64, Dh=512,
+                window=128, q_idx_dtype="f32", key_dtype="bf16", kv_dtype="bf16")
+    base.update(kw)
+    return inputs.generate(inputs.small_workload(**base))
+
+
+def test_v4_combine_edges():
+    # the tensor-core combine (64 heads x 512, bf16): -1 padding (Np < k), local only
+    # (Np = 0), and the dense branch over 3000 rows split across many CTAs
+    data = v4_small(B=3, Np=(100, 0, 3000), seed=12)
+    data["t0"][:] = np.maximum(4 * data["Np"] - 1, 200)
+    data["local_pos0"][:] = data["t0"] - 127
+    prob = Problem(data)
+    I = np.full((3, 512), -1, dtype=np.int32)
+    I[0, :100] = np.arange(100)[::-1]
+    I[2] = np.random.default_rng(0).choice(3000, 512, replace=False)
+    prob.attend(I=torch.as_tensor(I, device="cuda"))
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    out = np_(prob.out)
+    for b in range(3):
+        P.check_attend(data, b, 0, out[b], I[b])
+    prob.attend(I=None)
+    torch.cuda.synchronize()
+    out = np_(prob.out)
+    for b in range(3):
+        P.check_attend(data, b, 0, out[b], None)
+
+
+def test_v4_combine_prefill_rows():
+    # L > 1 with the V4 shape: local window per row, causal re-mask of pooled ids
+    data = v4_small(L=40, Np=(2048,), seed=13, t0=3000, kv_dtype="bf16")
+    prob = Problem(data)
+    rng = np.random.default_rng(1)
+    I = np.stack([rng.choice(2048, 512, replace=False) for _ in range(40)]).astype(np.int32)
+    prob.attend(I=torch.as_tensor(I, device="cuda"))
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    out = np_(prob.out)
+    for j in range(0, 40, 3):
+        P.check_attend(data, 0, j, out[j], I[j])
