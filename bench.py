@@ -398,7 +398,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--R", type=int, default=256, help="independent decode queries per step")
+    ap.add_argument("--R", type=int, default=304,
+                    help="independent decode queries per step (2 x 152 SMs)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-queries", type=int, default=4, help="oracle queries per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
