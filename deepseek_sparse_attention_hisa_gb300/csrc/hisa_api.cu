@@ -117,6 +117,22 @@ ScoreParams score_params(const hisa_index_desc *d, int mode, const void *q, cons
     return p;
 }
 
+// Runs one scoring pass: the tcgen05 kernel for the V4 indexer shape, else CUDA cores.
+// With `sel` the tensor-core coarse / fine kernels also select (returns true in *fused).
+cudaError_t run_scores(const ScoreParams &p, int32_t *sel, int k_sel, bool *fused,
+                       cudaStream_t s) {
+    *fused = false;
+    if (score_tc_supported(p.mode, p.H_i, p.D_i, p.rows_bf16, p.n_max)) {
+        ScoreTcParams t{};
+        t.s = p;
+        t.sel = sel;
+        t.k_sel = k_sel;
+        *fused = p.mode != kFlat;
+        return launch_score_tc(t, s);
+    }
+    return launch_scores_simt(p, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -196,7 +212,8 @@ hisa_status hisa_index_scores(const hisa_index_desc *d, const void *q, const flo
     ScoreParams p = score_params(d, kFlat, q, w, keys, d->k_dtype == HISA_BF16, key_off, t0,
                                  scores, ld_scores, ws);
     p.n_max = d->Np_max;
-    return from_cuda(launch_scores_simt(p, reinterpret_cast<cudaStream_t>(stream)));
+    bool fused = false;
+    return from_cuda(run_scores(p, nullptr, 0, &fused, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 hisa_status hisa_block_means(const hisa_index_desc *d, const void *keys, const int64_t *key_off,
@@ -233,13 +250,16 @@ hisa_status hisa_block_filter(const hisa_index_desc *d, const void *q, const flo
     if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_BLOCK_FILTER, d))) != HISA_OK)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    float *buf = cscores ? cscores : scratch_of(ws);
+    const bool tc = score_tc_supported(kCoarse, d->H_i, d->D_i, 0, nb_max);
+    float *buf = cscores ? cscores : (tc ? nullptr : scratch_of(ws));
     const int64_t ld = cscores ? ld_cscores : (nb_max > 0 ? nb_max : 1);
     ScoreParams p = score_params(d, kCoarse, q, w, means, 0, key_off, t0, buf, ld, ws);
     p.means_off = means_off;
     p.n_max = nb_max;
-    cudaError_t e = launch_scores_simt(p, s);
+    bool fused = false;
+    cudaError_t e = run_scores(p, top_blk, d->index_keep, &fused, s);
     if (e != cudaSuccess) return HISA_ECUDA;
+    if (fused) return HISA_OK;
     SelectParams sp{};
     sp.mode = kCoarse; sp.B = d->B; sp.L = d->L; sp.b = d->index_block; sp.keep = d->index_keep;
     sp.k = d->index_keep;
@@ -261,13 +281,16 @@ hisa_status hisa_select_topk(const hisa_index_desc *d, const void *q, const floa
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t C = (int64_t)d->index_block * d->index_keep;
-    float *buf = fscores ? fscores : scratch_of(ws);
+    const bool tc = score_tc_supported(kFine, d->H_i, d->D_i, d->k_dtype == HISA_BF16, C);
+    float *buf = fscores ? fscores : (tc ? nullptr : scratch_of(ws));
     ScoreParams p = score_params(d, kFine, q, w, keys, d->k_dtype == HISA_BF16, key_off, t0, buf,
                                  C, ws);
     p.top_blk = top_blk;
     p.n_max = C;
-    cudaError_t e = launch_scores_simt(p, s);
+    bool fused = false;
+    cudaError_t e = run_scores(p, I, d->index_topk, &fused, s);
     if (e != cudaSuccess) return HISA_ECUDA;
+    if (fused) return HISA_OK;
     SelectParams sp{};
     sp.mode = kFine; sp.B = d->B; sp.L = d->L; sp.b = d->index_block; sp.keep = d->index_keep;
     sp.k = d->index_topk;
@@ -291,7 +314,8 @@ hisa_status hisa_flat_topk(const hisa_index_desc *d, const void *q, const float 
     ScoreParams p = score_params(d, kFlat, q, w, keys, d->k_dtype == HISA_BF16, key_off, t0, buf,
                                  ld, ws);
     p.n_max = d->Np_max;
-    cudaError_t e = launch_scores_simt(p, s);
+    bool fused = false;
+    cudaError_t e = run_scores(p, nullptr, 0, &fused, s);
     if (e != cudaSuccess) return HISA_ECUDA;
     SelectParams sp{};
     sp.mode = kFlat; sp.B = d->B; sp.L = d->L; sp.b = d->index_block; sp.keep = d->index_keep;

@@ -111,6 +111,16 @@ struct AttnParams {
     uint32_t *status;
 };
 
+// Tensor-core scoring (H_i = 64, D_i = 128): `s` describes the rows and inputs; the
+// coarse and fine modes also select (sel = top_blk or I, k_sel ids per query row); s.out
+// is optional for them (the scores of every row) and required for the flat mode.
+struct ScoreTcParams {
+    ScoreParams s;
+    int32_t *sel;
+    int k_sel;
+    int tiles_per_cta;        // flat: 128-row tiles per CTA (grid.y covers the row)
+};
+
 // ---------------------------------------------------------------------------
 // host launchers (one per kernel file); return the cudaGetLastError() of the launch
 // ---------------------------------------------------------------------------
@@ -123,5 +133,7 @@ cudaError_t launch_attend_tc(const AttnParams &p, cudaStream_t s);
 int attend_simt_supported(int H, int Dh);
 int attend_tc_supported(int H, int Dh, int kv_bf16);
 int attend_chunk_rows();
+cudaError_t launch_score_tc(const ScoreTcParams &p, cudaStream_t s);
+int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max);
 
 }  // namespace hisa

@@ -1,0 +1,409 @@
+// Indexer scoring on the sm_103a tensor cores for the DeepSeek-V4 indexer shape
+// (H_i = 64 heads, D_i = 128), with the top-k fused for the coarse and fine stages.
+//
+// score[row] = sum_h relu(q_h . row) * scale * w_h   ([HiSA issue] "Flat selection",
+// "HiSA decode path": the coarse stage scores block means, the fine stage the rows of
+// the kept blocks, the flat path every pooled row).
+//
+// Per tile of 128 scored rows: D[128 rows x 64 heads] = rows . q^T on tcgen05 (M = 128,
+// N = 64, K = 128), f32 accumulators in TMEM (two buffers). Scoring is f32 on the page,
+// so f32 operands are split exactly into three bf16 planes, x = x1 + x2 + x3 (each the
+// bf16 rounding of what the previous planes leave over): bf16 products are exact in the
+// f32 accumulator. bf16 keys need one plane; f32 q needs three (3 products per K step);
+// f32 block means against f32 q need the six plane pairs whose weight is above 2^-24.
+// The epilogue thread of TMEM lane r owns row r of the tile: it applies relu, the head
+// weights and the head sum in registers, with no cross-thread reduction.
+//
+// Warp roles: 0 MMA issue + TMEM owner, 1-4 epilogue (warp w reads TMEM lanes
+// 32*(w%4)..+31), 5-8 loaders (q planes; bf16 rows by cp.async with the 128-byte
+// swizzle, f32 rows through registers, split into planes). Coarse and fine CTAs own one
+// query row and finish with block_topk over the scores held in shared memory; flat CTAs
+// own a range of tiles of one query row and write scores to global memory.
+// Waits are bounded; a timeout raises HISA_DEV_TIMEOUT and the CTA drains and exits.
+#include "select_core.cuh"
+#include "tc_ptx.cuh"
+
+namespace hisa {
+namespace {
+
+using namespace tc;
+
+constexpr int kH = 64, kD = 128, kTile = 128;
+constexpr int kThreads = 288;                          // 9 warps
+constexpr int kMmaWarp = 0, kLoadWarp0 = 5;               // epilogue: warps 1-4
+constexpr int kLoaders = 128, kEpis = 128;
+constexpr uint32_t kPlaneQ = kH * kD * 2;              // 16 KiB: [64 heads x 128 dims] bf16
+constexpr uint32_t kPlaneRows = kTile * kD * 2;        // 32 KiB: [128 rows x 128 dims] bf16
+constexpr int kSlots = 3;                              // bf16 row tiles in flight
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffRows = kOffQ + 3 * kPlaneQ;     // 96 KiB: 3 slots, or 3 planes of 1 slot
+constexpr uint32_t kOffSc = kOffRows + 3 * kPlaneRows;
+constexpr int kMaxSel = 8192;                          // scores a fused select holds
+constexpr uint32_t kOffW = kOffSc + kMaxSel * 4;
+constexpr uint32_t kOffBlk = kOffW + kH * 4;
+constexpr uint32_t kOffBar = kOffBlk + 64 * 4;
+// barriers: full[3] empty[3] d_full[2] d_free[2] q_full drain
+constexpr int kBarFull = 0, kBarEmpty = 3, kBarDFull = 6, kBarDFree = 8, kBarQ = 10,
+              kBarDrain = 11, kNumBars = 12;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 128;                    // two 64-column accumulators
+
+struct Misc {
+    uint32_t tmem;
+    int abort;
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    for (uint32_t i = 0; i < (1u << 22); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && *abort) return false;
+    }
+    return false;
+}
+
+// Exact three-way split of 8 f32 values into bf16 planes, packed as 3 x uint4.
+__device__ __forceinline__ void split3(const float (&x)[8], uint4 (&pl)[3]) {
+    uint32_t w[3][4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        float r0 = x[e], r1 = x[e + 1];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(r0, r1);
+            w[k][e / 2] = *reinterpret_cast<const uint32_t *>(&b);
+            const float2 f = __bfloat1622float2(b);
+            r0 -= f.x;
+            r1 -= f.y;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k) pl[k] = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+}
+
+// Byte offset of the 16-byte unit u (dims 8u..8u+7) of row r in a K-major [rows x 128]
+// bf16 operand of `rows` rows: two 64-dim chunks of rows*128 bytes.
+__device__ __forceinline__ uint32_t unit_off(uint32_t r, uint32_t u, uint32_t rows) {
+    return (u >> 3) * (rows * 128u) + sw128_offset(r, (u & 7u) * 8u);
+}
+
+}  // namespace
+}  // namespace hisa
+
+namespace hisa {
+namespace {
+
+template <int MODE, bool QBF16>
+__global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant__ ScoreTcParams P) {
+    constexpr int NQ = QBF16 ? 1 : 3;                    // q planes
+    constexpr int NR = (MODE == kCoarse) ? 3 : 1;        // row planes
+    const ScoreParams &p = P.s;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ SelectShared<kThreads> sel_sh;
+    __shared__ int s_state;
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    Misc *misc = reinterpret_cast<Misc *>(smem + kOffMisc);
+    volatile int *abort = &misc->abort;
+    float *sc = reinterpret_cast<float *>(smem + kOffSc);
+    float *sw = reinterpret_cast<float *>(smem + kOffW);
+    int *blk = reinterpret_cast<int *>(smem + kOffBlk);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = blockIdx.x;
+    const int bq = row / p.L, j = row - bq * p.L;
+    const int64_t k0 = p.key_off[bq];
+    const int64_t Np = p.key_off[bq + 1] - k0;
+
+    // ---- per-row validity: uniform over the CTA ----
+    if (tid == 0) {
+        int st = 0;
+        const bool first = blockIdx.y == 0;
+        if (Np < 0 || Np > p.Np_max) {
+            st = 1;
+            if (first) flag(p.status, HISA_DEV_BAD_OFFSETS);
+        } else if (MODE != kFlat && Np < (int64_t)p.b * p.keep) {
+            st = 1;
+            flag(p.status, HISA_DEV_GATE);
+        } else if (MODE == kCoarse &&
+                   (p.means_off[bq + 1] - p.means_off[bq] < Np / p.b || Np / p.b > kMaxSel)) {
+            st = 1;
+            flag(p.status, HISA_DEV_BAD_OFFSETS);
+        } else if (MODE == kFine) {
+            const int32_t *tb = p.top_blk + (int64_t)row * p.keep;
+            for (int s = 0; s < p.keep; ++s) {     // insertion sort: candidates in ascending pos
+                int v = tb[s], u = s;
+                if (v < 0 || (int64_t)v >= Np / p.b) st = 1;
+                while (u > 0 && blk[u - 1] > v) { blk[u] = blk[u - 1]; --u; }
+                blk[u] = v;
+            }
+            if (st) flag(p.status, HISA_DEV_BAD_BLOCK);
+        }
+        s_state = st;
+    }
+    __syncthreads();
+    if (s_state) {
+        if (MODE != kFlat)
+            for (int e = tid; e < P.k_sel; e += kThreads) P.sel[(int64_t)row * P.k_sel + e] = -1;
+        return;
+    }
+    const int64_t n = MODE == kFlat ? Np : (MODE == kCoarse ? Np / p.b : (int64_t)p.keep * p.b);
+    const int T_all = (int)((n + kTile - 1) / kTile);
+    int t_begin = 0, t_end = T_all;
+    if (MODE == kFlat) {
+        t_begin = (int)blockIdx.y * P.tiles_per_cta;
+        t_end = t_begin + P.tiles_per_cta < T_all ? t_begin + P.tiles_per_cta : T_all;
+        if (t_begin >= t_end) return;
+    }
+    const int T = t_end - t_begin;
+    const int64_t V = p.causal ? visible_len((int64_t)p.t0[bq] + j, p.r, Np) : Np;
+
+    if (tid == 0) {
+        for (int b = 0; b < kNumBars; ++b) {
+            uint32_t cnt = 1;
+            if ((b >= kBarFull && b < kBarFull + kSlots) || b == kBarQ) cnt = kLoaders;
+            if (b == kBarDFree || b == kBarDFree + 1) cnt = kEpis;
+            mbar_init(&bars[b], cnt);
+        }
+        mbar_fence_init();
+        misc->abort = 0;
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&misc->tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = misc->tmem;
+    bool ok = true;
+
+    if (warp >= kLoadWarp0) {
+        // ---------------- loaders ----------------
+        const int lt = tid - kLoadWarp0 * 32;
+        for (int u = lt; u < kH * 16; u += kLoaders) {      // q planes and scaled weights
+            const int h = u >> 4, uu = u & 15;
+            const uint32_t off = unit_off(h, uu, kH);
+            if (QBF16) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
+                    reinterpret_cast<const __nv_bfloat16 *>(p.q) + ((int64_t)row * kH + h) * kD) + uu);
+                *reinterpret_cast<uint4 *>(smem + kOffQ + off) = v;
+            } else {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    reinterpret_cast<const float *>(p.q) + ((int64_t)row * kH + h) * kD + uu * 8);
+                const float4 a = __ldg(src), b = __ldg(src + 1);
+                const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                uint4 pl[3];
+                split3(x, pl);
+#pragma unroll
+                for (int k = 0; k < 3; ++k)
+                    *reinterpret_cast<uint4 *>(smem + kOffQ + k * kPlaneQ + off) = pl[k];
+            }
+        }
+        for (int h = lt; h < kH; h += kLoaders) sw[h] = p.w[(int64_t)row * kH + h] * p.head_scale;
+        fence_async_smem();
+        mbar_arrive(&bars[kBarQ]);
+        const int uu = lt & 15, r0 = lt >> 4;             // unit uu of rows r0 + 8m
+        if (MODE == kCoarse) {
+            const float *means = reinterpret_cast<const float *>(p.rows) + p.means_off[bq] * kD;
+            float4 reg[32];
+            auto load_tile = [&](int ti) {
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const int64_t c = (int64_t)ti * kTile + r0 + 8 * m;
+                    if (c < n) {
+                        const float4 *src = reinterpret_cast<const float4 *>(means + c * kD + uu * 8);
+                        reg[2 * m] = __ldg(src);
+                        reg[2 * m + 1] = __ldg(src + 1);
+                    } else {
+                        reg[2 * m] = reg[2 * m + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+            };
+            load_tile(t_begin);
+            for (int i = 0; i < T; ++i) {
+                if (i >= 1 && !wait_bar(&bars[kBarEmpty], (i - 1) & 1, abort)) { ok = false; break; }
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float4 a = reg[2 * m], b = reg[2 * m + 1];
+                    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                    uint4 pl[3];
+                    split3(x, pl);
+                    const uint32_t off = unit_off(r0 + 8 * m, uu, kTile);
+#pragma unroll
+                    for (int k = 0; k < 3; ++k)
+                        *reinterpret_cast<uint4 *>(smem + kOffRows + k * kPlaneRows + off) = pl[k];
+                }
+                fence_async_smem();
+                mbar_arrive(&bars[kBarFull]);
+                if (i + 1 < T) load_tile(t_begin + i + 1);
+            }
+        } else {
+            const __nv_bfloat16 *keys = reinterpret_cast<const __nv_bfloat16 *>(p.rows) + k0 * kD;
+            for (int i = 0; i < T; ++i) {
+                const int s = i % kSlots;
+                if (i >= kSlots && !wait_bar(&bars[kBarEmpty + s], ((i / kSlots) - 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t slot = sbase + kOffRows + s * kPlaneRows;
+#pragma unroll 4
+                for (int m = 0; m < 16; ++m) {
+                    const int r = r0 + 8 * m;
+                    const int64_t c = (int64_t)(t_begin + i) * kTile + r;
+                    const bool v = c < n;
+                    int64_t pos = c;
+                    if (MODE == kFine && v) pos = (int64_t)blk[c / p.b] * p.b + (c % p.b);
+                    const void *src = v ? static_cast<const void *>(keys + pos * kD + uu * 8) : p.rows;
+                    cp_async16_zfill(slot + unit_off(r, uu, kTile), src, v);
+                }
+                cp_async_arrive(&bars[kBarFull + s]);
+            }
+            cp_async_wait_all();
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+            ok = wait_bar(&bars[kBarQ], 0, abort);
+            for (int i = 0; i < T && ok; ++i) {
+                const int s = MODE == kCoarse ? 0 : i % kSlots;
+                const uint32_t ph = MODE == kCoarse ? (uint32_t)(i & 1) : (uint32_t)((i / kSlots) & 1);
+                const int db = i & 1;
+                if (!wait_bar(&bars[kBarFull + s], ph, abort) ||
+                    (i >= 2 && !wait_bar(&bars[kBarDFree + db], ((i >> 1) - 1) & 1, abort))) {
+                    ok = false;
+                    break;
+                }
+                fence_after_sync();
+                const uint32_t rbase = sbase + kOffRows + s * kPlaneRows;
+                uint32_t acc = 0;
+#pragma unroll 1
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t ko = ks >> 2, kb = (ks & 3) * 32;
+#pragma unroll
+                    for (int ra = 0; ra < NR; ++ra)
+#pragma unroll
+                        for (int qa = 0; qa < NQ; ++qa) {
+                            if (ra + qa > 2) continue;
+                            const uint64_t a = smem_desc_sw128(
+                                rbase + ra * kPlaneRows + ko * (kTile * 128) + kb, 16, 1024);
+                            const uint64_t b = smem_desc_sw128(
+                                sbase + kOffQ + qa * kPlaneQ + ko * (kH * 128) + kb, 16, 1024);
+                            mma_bf16(tmem + db * 64, a, b, idesc, acc);
+                            acc = 1;
+                        }
+                }
+                mma_commit(&bars[kBarEmpty + s]);
+                mma_commit(&bars[kBarDFull + db]);
+            }
+            mma_commit(&bars[kBarDrain]);
+            wait_bar(&bars[kBarDrain], 0, abort);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: one row per thread ----------------
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        ok = wait_bar(&bars[kBarQ], 0, abort);
+        for (int i = 0; i < T && ok; ++i) {
+            const int db = i & 1;
+            if (!wait_bar(&bars[kBarDFull + db], (i >> 1) & 1, abort)) { ok = false; break; }
+            fence_after_sync();
+            float v[4][16];
+            const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + db * 64;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld16(ta + c * 16, v[c]);
+            tmem_ld_wait();
+            fence_before_sync();
+            mbar_arrive(&bars[kBarDFree + db]);
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int q = 0; q < 16; ++q) acc = fmaf(sw[c * 16 + q], fmaxf(v[c][q], 0.f), acc);
+            const int64_t cidx = (int64_t)(t_begin + i) * kTile + r;
+            if (cidx < n) {
+                int64_t pos = cidx;
+                if (MODE == kCoarse) pos = cidx * p.b;   // a block is eligible iff its first row is visible
+                if (MODE == kFine) pos = (int64_t)blk[cidx / p.b] * p.b + (cidx % p.b);
+                const float score = pos < V ? acc : kNeg;
+                if (MODE != kFlat) sc[cidx] = score;
+                if (p.out) p.out[(int64_t)row * p.ld_out + cidx] = score;
+            }
+        }
+    }
+    if (!ok) {
+        *abort = 1;
+        flag(p.status, HISA_DEV_TIMEOUT);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (MODE != kFlat) {
+        int32_t *out = P.sel + (int64_t)row * P.k_sel;
+        const int aborted = misc->abort;
+        const int64_t kout = aborted ? 0 : (n < P.k_sel ? n : (int64_t)P.k_sel);
+        if (MODE == kFine) {
+            const int b = p.b;
+            block_topk<kThreads>(sc, n, kout, out,
+                                 [&](int64_t i) { return (int32_t)((int64_t)blk[i / b] * b + (i % b)); },
+                                 sel_sh, p.status);
+        } else {
+            block_topk<kThreads>(sc, n, kout, out, [](int64_t i) { return (int32_t)i; }, sel_sh,
+                                 p.status);
+        }
+        for (int64_t e = kout + tid; e < P.k_sel; e += kThreads) out[e] = -1;
+    }
+}
+
+}  // namespace
+}  // namespace hisa
+
+namespace hisa {
+
+int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max) {
+    if (H_i != kH || D_i != kD) return 0;
+    if (mode == kCoarse) return !rows_bf16 && n_max <= kMaxSel;
+    if (mode == kFine) return rows_bf16 && n_max <= kMaxSel;
+    return rows_bf16;
+}
+
+template <int MODE, bool QBF16>
+static cudaError_t launch_t(const ScoreTcParams &p, dim3 grid, cudaStream_t s) {
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        k_score_tc<MODE, QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (attr != cudaSuccess) return attr;
+    k_score_tc<MODE, QBF16><<<grid, kThreads, kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_score_tc(const ScoreTcParams &p_in, cudaStream_t s) {
+    ScoreTcParams p = p_in;
+    const int64_t rows = (int64_t)p.s.B * p.s.L;
+    dim3 grid((unsigned)rows, 1);
+    if (p.s.mode == kFlat) {
+        const int64_t tiles = (p.s.Np_max + kTile - 1) / kTile;
+        if (tiles == 0) return cudaSuccess;
+        int64_t tpc = (rows * tiles + kTargetCtas - 1) / kTargetCtas;
+        if (tpc < 1) tpc = 1;
+        if (tpc > tiles) tpc = tiles;
+        p.tiles_per_cta = (int)tpc;
+        grid.y = (unsigned)((tiles + tpc - 1) / tpc);
+    }
+    const bool qb = p.s.q_bf16 != 0;
+    switch (p.s.mode) {
+        case kFlat: return qb ? launch_t<kFlat, true>(p, grid, s) : launch_t<kFlat, false>(p, grid, s);
+        case kCoarse:
+            return qb ? launch_t<kCoarse, true>(p, grid, s) : launch_t<kCoarse, false>(p, grid, s);
+        case kFine: return qb ? launch_t<kFine, true>(p, grid, s) : launch_t<kFine, false>(p, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace hisa
