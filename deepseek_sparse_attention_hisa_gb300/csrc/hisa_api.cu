@@ -43,7 +43,8 @@ hisa_status check_hisa_gate(const hisa_index_desc *d) {
 
 hisa_status check_attn_desc(const hisa_attn_desc *d) {
     if (!d) return HISA_EINVAL;
-    if (d->B < 1 || d->L < 1 || d->window < 0 || d->W_max < 0 || d->r < 1 || d->k < 0)
+    if (d->B < 1 || d->L < 1 || d->window < 0 || d->W_max < 0 || d->r < 1 || d->k < 0 ||
+        d->k > kMaxTopk)
         return HISA_EINVAL;
     if (d->Np_max < 0 || d->Np_max > 0x7fffffffLL) return HISA_EINVAL;
     if ((int64_t)d->B * d->L > 0x7fffffffLL) return HISA_EINVAL;

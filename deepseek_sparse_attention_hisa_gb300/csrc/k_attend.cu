@@ -279,7 +279,8 @@ int attend_simt_supported(int H, int Dh) {
     return (H == 8 && Dh == 64) || (H == 16 && Dh == 128) || (H == 64 && Dh == 512);
 }
 
-int attend_chunk_rows() { return kChunk; }
+// Split ranges are cut in multiples of 64 rows: one tensor-core tile, two CUDA-core chunks.
+int attend_chunk_rows() { return 64; }
 
 cudaError_t launch_attend_simt(const AttnParams &p, cudaStream_t s) {
     const bool bf = p.kv_bf16 != 0;

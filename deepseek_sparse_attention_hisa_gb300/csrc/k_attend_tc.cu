@@ -4,7 +4,7 @@
 //
 // One CTA owns a range of one query row's attended-row list (the visible local window
 // rows, then the gathered pooled rows). The list streams through shared memory in tiles
-// of kTR rows; per tile:
+// of kTR = 32 rows (four slots); per tile:
 //   S  = Q . K^T      tcgen05, M = 64 heads, N = kTR rows, K = 512   (TMEM, 2 buffers)
 //   P  = exp2(S * scale*log2e - m) per head, in the thread that owns the head's TMEM lane
 //   O^T += V^T . P^T  tcgen05, M = 128 dims x 4, N = 64 heads, K = kTR  (TMEM, f32)
@@ -24,11 +24,12 @@ namespace {
 using namespace tc;
 
 constexpr int kH = 64, kDH = 512, kTR = 32, kSlots = 4;
+constexpr int kRPL = kTR / 32;                        // tile rows per producer lane
 constexpr int kSoftWarps = 4, kMmaWarp = 4, kProdWarp0 = 5, kProdWarps = 2;
 constexpr int kThreads = 32 * (kSoftWarps + 1 + kProdWarps);
 constexpr uint32_t kQBytes = kH * kDH * 2;            // 64 KiB, K-major, 8 chunks of 64 dims
 constexpr uint32_t kSlotBytes = kTR * kDH * 2;        // 32 KiB per staged tile
-constexpr uint32_t kPBytes = kH * 128;                // P^T: 64 heads x (up to 64 rows) bf16
+constexpr uint32_t kPBytes = kH * 128;                // P^T: 64 heads x 64 rows bf16
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kQBytes;
 constexpr uint32_t kOffP = kOffKV + kSlots * kSlotBytes;
@@ -37,16 +38,17 @@ constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
 constexpr int kBarFull = 0, kBarEmpty = 4, kBarSFull = 8, kBarSFree = 10, kBarPFull = 12,
               kBarPFree = 14, kBarQ = 16, kBarDrain = 17, kNumBars = 18;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffMisc + 1024 + 1024;  // misc + 1 KiB alignment slack
-constexpr uint32_t kTmemCols = 512;                   // S: cols [0,64), O^T: [64, 320)
-constexpr uint32_t kColO = 64;
+constexpr uint32_t kOffIds = kOffMisc + 1024;          // this CTA's slice of I (<= kMaxTopk)
+constexpr uint32_t kSmemBytes = kOffIds + kMaxTopk * 4 + 1024;  // + 1 KiB alignment slack
+constexpr uint32_t kTmemCols = 512;                   // S: cols [0,128), O^T: [128, 384)
+constexpr uint32_t kColO = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;
 
 struct Misc {
     uint32_t tmem;
     int abort;
-    uint32_t mask[kSlots];
+    uint64_t mask[kSlots];
     float alpha[kH];
     float factor[kH];
 };
@@ -57,6 +59,18 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
         if ((i & 255u) == 255u && *abort) return false;
     }
     return false;
+}
+
+// A wait taken by a whole warp; the result is made warp-uniform.
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort));
+}
+
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error <= 2^-22; -inf -> +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ void named_sync_soft() {
@@ -140,6 +154,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             cp_async16(qb + (pt >> 3) * (kH * 128) + sw128_offset(h, (pt & 7) * 8),
                        qrow + h * kDH + pt * 8);
         cp_async_arrive(&bars[kBarQ]);
+        // the selected ids of this CTA's range, staged once (8 loads in flight per thread)
+        int32_t *ids = reinterpret_cast<int32_t *>(smem + kOffIds);
+        const int64_t kk0 = e0 > nloc ? e0 - nloc : 0;
+        const int64_t kk1 = e1 > nloc ? e1 - nloc : 0;
+        if (Irow) {
+            for (int64_t base = kk0; base < kk1; base += 8 * 64) {
+                int32_t v[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int64_t kk = base + pt + 64 * m;
+                    v[m] = kk < kk1 ? Irow[kk] : -1;
+                }
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int64_t kk = base + pt + 64 * m;
+                    if (kk < kk1) ids[kk - kk0] = v[m];
+                }
+            }
+        }
+        asm volatile("bar.sync 2, 64;" ::: "memory");    // the two producer warps
         bool ok = true;
         for (int i = 0; i < T && ok; ++i) {
             const int s = i % kSlots;
@@ -147,33 +181,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 ok = false;
                 break;
             }
-            // lane r resolves row r of the tile
-            const int64_t e = e0 + (int64_t)i * kTR + lane;
-            const __nv_bfloat16 *src = nullptr;
-            if (e < e1) {
-                if (e < nloc) {
-                    src = local + e * kDH;
-                } else {
-                    const int64_t kk = e - nloc;
-                    const int64_t id = Irow ? (int64_t)Irow[kk] : kk;
-                    if (id >= Np || id < -1) {
-                        if (pt < 32) flag(p.status, HISA_DEV_BAD_ID);
-                    } else if (id >= 0 && id < V) {
-                        src = pooled + id * kDH;
+            // lane r resolves rows r, r + 32, ... of the tile
+            const __nv_bfloat16 *src[kRPL];
+            uint32_t valid[kRPL];
+#pragma unroll
+            for (int hlf = 0; hlf < kRPL; ++hlf) {
+                src[hlf] = nullptr;
+                const int64_t e = e0 + (int64_t)i * kTR + hlf * 32 + lane;
+                if (e < e1) {
+                    if (e < nloc) {
+                        src[hlf] = local + e * kDH;
+                    } else {
+                        const int64_t kk = e - nloc;
+                        const int64_t id = Irow ? (int64_t)ids[kk - kk0] : kk;
+                        if (id >= Np || id < -1) {
+                            if (pt < 32) flag(p.status, HISA_DEV_BAD_ID);
+                        } else if (id >= 0 && id < V) {
+                            src[hlf] = pooled + id * kDH;
+                        }
                     }
                 }
+                valid[hlf] = __ballot_sync(0xffffffffu, src[hlf] != nullptr);
             }
-            const uint32_t valid = __ballot_sync(0xffffffffu, src != nullptr);
             const uint32_t slot = sbase + kOffKV + s * kSlotBytes;
             const uint32_t dst0 = slot + (pt >> 3) * (kTR * 128);
+#pragma unroll 4
             for (int r = 0; r < kTR; ++r) {
-                const __nv_bfloat16 *rs = reinterpret_cast<const __nv_bfloat16 *>(
-                    __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(src), r));
-                const bool v = (valid >> r) & 1u;
+                const __nv_bfloat16 *rs = reinterpret_cast<const __nv_bfloat16 *>(__shfl_sync(
+                    0xffffffffu, reinterpret_cast<uintptr_t>(src[r >> 5]), r & 31));
+                const bool v = (valid[r >> 5] >> (r & 31)) & 1u;
                 cp_async16_zfill(dst0 + sw128_offset(r, (pt & 7) * 8),
                                  v ? static_cast<const void *>(rs + pt * 8) : p.q, v);
             }
-            if (pt == 0) misc->mask[s] = valid;
+            if (pt == 0) {
+                uint64_t m = 0;
+#pragma unroll
+                for (int hlf = 0; hlf < kRPL; ++hlf) m |= (uint64_t)valid[hlf] << (32 * hlf);
+                misc->mask[s] = m;
+            }
             cp_async_arrive(&bars[kBarFull + s]);
             if (pt == 0) mbar_arrive(&bars[kBarFull + s]);
         }
@@ -183,45 +228,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             flag(p.status, HISA_DEV_TIMEOUT);
         }
     } else if (warp == kMmaWarp) {
-        // ---------------- MMA issue (one thread) ----------------
-        if (lane == 0 && T > 0) {
-            const uint32_t id_s = idesc_bf16_f32(64, kTR, 0, 0);
+        // ---------------- MMA issue (warp-uniform loop, one elected lane issues) -------
+        if (T > 0) {
+            const uint32_t id_s = idesc_bf16_f32(64, kTR, 0, 0);   // N = kTR rows
             const uint32_t id_o = idesc_bf16_f32(128, 64, 1, 0);
-            const uint32_t qb = sbase + kOffQ;
-            bool ok = wait_bar(&bars[kBarQ], 0, abort);
+            const uint64_t qd = smem_desc_sw128(sbase + kOffQ, 16, 1024);
+            bool ok = wait_bar_warp(&bars[kBarQ], 0, abort);
             auto issue_s = [&](int i) -> bool {
                 const int s = i % kSlots, sb = i & 1;
-                if (!wait_bar(&bars[kBarFull + s], (i / kSlots) & 1, abort)) return false;
-                if (i >= 2 && !wait_bar(&bars[kBarSFree + sb], ((i >> 1) - 1) & 1, abort)) return false;
+                if (!wait_bar_warp(&bars[kBarFull + s], (i / kSlots) & 1, abort)) return false;
+                if (i >= 2 && !wait_bar_warp(&bars[kBarSFree + sb], ((i >> 1) - 1) & 1, abort)) return false;
                 fence_after_sync();
-                const uint32_t slot = sbase + kOffKV + s * kSlotBytes;
-#pragma unroll 1
+                const uint64_t bd = smem_desc_sw128(sbase + kOffKV + s * kSlotBytes, 16, 1024);
+                const uint32_t d = tmem + sb * kTR;
+#pragma unroll
                 for (int ks = 0; ks < kDH / 16; ++ks) {
                     const uint32_t ko = (ks >> 2), kb = (ks & 3) * 32;
-                    const uint64_t a = smem_desc_sw128(qb + ko * (kH * 128) + kb, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(slot + ko * (kTR * 128) + kb, 16, 1024);
-                    mma_bf16(tmem + sb * 32, a, b, id_s, ks > 0);
+                    mma_bf16_warp(d, desc_add(qd, ko * (kH * 128) + kb),
+                             desc_add(bd, ko * (kTR * 128) + kb), id_s, ks > 0);
                 }
-                mma_commit(&bars[kBarSFull + sb]);
+                mma_commit_warp(&bars[kBarSFull + sb]);
                 return true;
             };
             auto issue_pv = [&](int i) -> bool {
                 const int s = i % kSlots, pb = i & 1;
-                if (!wait_bar(&bars[kBarPFull + pb], (i >> 1) & 1, abort)) return false;
+                if (!wait_bar_warp(&bars[kBarPFull + pb], (i >> 1) & 1, abort)) return false;
                 fence_after_sync();
-                const uint32_t slot = sbase + kOffKV + s * kSlotBytes;
-                const uint32_t pbase = sbase + kOffP + pb * kPBytes;
+                const uint64_t ad = smem_desc_sw128(sbase + kOffKV + s * kSlotBytes, kTR * 128, 1024);
+                const uint64_t bd = smem_desc_sw128(sbase + kOffP + pb * kPBytes, 16, 1024);
+                const uint32_t first = i > 0 ? 1u : 0u;
 #pragma unroll
                 for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-                    for (int ks = 0; ks < kTR / 16; ++ks) {
-                        const uint64_t a = smem_desc_sw128(slot + (2 * mt) * (kTR * 128) + ks * 2048,
-                                                           kTR * 128, 1024);
-                        const uint64_t b = smem_desc_sw128(pbase + ks * 32, 16, 1024);
-                        mma_bf16(tmem + kColO + mt * 64, a, b, id_o, (i > 0 || ks > 0) ? 1u : 0u);
-                    }
-                mma_commit(&bars[kBarEmpty + s]);
-                mma_commit(&bars[kBarPFree + pb]);
+                    for (int ks = 0; ks < kTR / 16; ++ks)
+                        mma_bf16_warp(tmem + kColO + mt * 64, desc_add(ad, (2 * mt) * (kTR * 128) + ks * 2048),
+                                 desc_add(bd, ks * 32), id_o, ks > 0 ? 1u : first);
+                mma_commit_warp(&bars[kBarEmpty + s]);
+                mma_commit_warp(&bars[kBarPFree + pb]);
                 return true;
             };
             if (ok) ok = issue_s(0);
@@ -235,10 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 flag(p.status, HISA_DEV_TIMEOUT);
             }
             // drain: every MMA issued by this thread has completed before TMEM is freed
-            mma_commit(&bars[kBarDrain]);
-            wait_bar(&bars[kBarDrain], 0, abort);
+            mma_commit_warp(&bars[kBarDrain]);
+            wait_bar_warp(&bars[kBarDrain], 0, abort);
         }
-        __syncwarp();
     } else {
         // ---------------- softmax + epilogue (warps 0-3) ----------------
         const bool active = lane < 16;
@@ -263,46 +305,59 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 break;
             }
             fence_after_sync();
-            const uint32_t mask = misc->mask[s];
+            const uint64_t mask = misc->mask[s];
             float v[kTR];
             {
-                float a[16], b[16];
-                const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + sb * 32;
-                tmem_ld16(ta, a);
-                tmem_ld16(ta + 16, b);
+                float a[4][16];
+                const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + sb * kTR;
+#pragma unroll
+                for (int c = 0; c < kTR / 16; ++c) tmem_ld16(ta + c * 16, a[c]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int r = 0; r < 16; ++r) { v[r] = a[r]; v[16 + r] = b[r]; }
+                for (int c = 0; c < kTR / 16; ++c)
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) v[c * 16 + r] = a[c][r];
             }
             fence_before_sync();
             mbar_arrive(&bars[kBarSFree + sb]);
-            float tmax = -INFINITY;
 #pragma unroll
-            for (int r = 0; r < kTR; ++r) {
-                v[r] = ((mask >> r) & 1u) ? v[r] * c2 : -INFINITY;
-                tmax = fmaxf(tmax, v[r]);
-            }
+            for (int r = 0; r < kTR; ++r) v[r] = ((mask >> r) & 1ull) ? v[r] * c2 : -INFINITY;
+            float mx[kTR / 2];                              // pairwise tree: short dependency chains
+#pragma unroll
+            for (int r = 0; r < kTR / 2; ++r) mx[r] = fmaxf(v[2 * r], v[2 * r + 1]);
+#pragma unroll
+            for (int w = kTR / 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int r = 0; r < w; ++r) mx[r] = fmaxf(mx[r], mx[r + w]);
+            const float tmax = mx[0];
             float alpha = 1.f;
             uint32_t resc = 0;
             if (active && tmax > m2 + kLazy) {
                 if (m2 != -INFINITY) {
-                    alpha = exp2f(m2 - tmax);
+                    alpha = ex2_approx(m2 - tmax);
                     resc = 1;
                 }
                 m2 = tmax;
             }
-            // P buffer (i & 1) is free once PV(i - 2) has completed
-            if (i >= 2 && !wait_pfree(i & 1, (uint32_t)((i >> 1) - 1))) { ok = false; break; }
-            float sum = 0.f;
+            // exp2(-inf - m) = +0 in the hardware approximation; m2 is finite once any row
+            // of this head was visible, and rows are only ever -inf when masked
+            const float msub = m2 == -INFINITY ? 0.f : m2;
+            float pr[kTR];
+#pragma unroll
+            for (int r = 0; r < kTR; ++r) pr[r] = ex2_approx(v[r] - msub);
             uint32_t packed[kTR / 2];
 #pragma unroll
             for (int r = 0; r < kTR; r += 2) {
-                const float p0 = (v[r] == -INFINITY) ? 0.f : exp2f(v[r] - m2);
-                const float p1 = (v[r + 1] == -INFINITY) ? 0.f : exp2f(v[r + 1] - m2);
-                sum += p0 + p1;
-                __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
-                packed[r / 2] = *reinterpret_cast<uint32_t *>(&pr);
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(pr[r], pr[r + 1]);
+                packed[r / 2] = *reinterpret_cast<uint32_t *>(&b2);
             }
+#pragma unroll
+            for (int w = kTR / 2; w >= 1; w >>= 1)
+#pragma unroll
+                for (int r = 0; r < w; ++r) pr[r] += pr[r + w];
+            const float sum = pr[0];
+            // P buffer (i & 1) is free once PV(i - 2) has completed
+            if (i >= 2 && !wait_pfree(i & 1, (uint32_t)((i >> 1) - 1))) { ok = false; break; }
             l = l * alpha + sum;
             if (active) {
                 uint8_t *pb = smem + kOffP + (i & 1) * kPBytes;

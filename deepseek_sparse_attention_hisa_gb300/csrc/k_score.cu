@@ -187,8 +187,17 @@ __global__ void k_block_means(MeansParams p) {
     for (int64_t beta = fb + blockIdx.x; beta < nb; beta += gridDim.x) {
         for (int d = threadIdx.x; d < p.D_i; d += blockDim.x) {
             const KT *src = keys + (k0 + beta * p.b) * p.D_i + d;
+            // f32 sum in row order; loads are issued 16 rows at a time
             float s = 0.f;
-            for (int i = 0; i < p.b; ++i) s += to_f32(src[(int64_t)i * p.D_i]);
+            int i = 0;
+            for (; i + 16 <= p.b; i += 16) {
+                float v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) v[u] = to_f32(src[(int64_t)(i + u) * p.D_i]);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) s += v[u];
+            }
+            for (; i < p.b; ++i) s += to_f32(src[(int64_t)i * p.D_i]);
             p.means[(m0 + beta) * p.D_i + d] = s / inv_div;
         }
     }

@@ -10,7 +10,8 @@
 // so f32 operands are split exactly into three bf16 planes, x = x1 + x2 + x3 (each the
 // bf16 rounding of what the previous planes leave over): bf16 products are exact in the
 // f32 accumulator. bf16 keys need one plane; f32 q needs three (3 products per K step);
-// f32 block means against f32 q need the six plane pairs whose weight is above 2^-24.
+// f32 block means against f32 q use all nine plane pairs. The q planes are stacked along
+// N (N = 64 * planes), so one MMA per rows plane and K step covers every q plane.
 // The epilogue thread of TMEM lane r owns row r of the tile: it applies relu, the head
 // weights and the head sum in registers, with no cross-thread reduction.
 //
@@ -47,7 +48,7 @@ constexpr int kBarFull = 0, kBarEmpty = 3, kBarDFull = 6, kBarDFree = 8, kBarQ =
               kBarDrain = 11, kNumBars = 12;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 128;                    // two 64-column accumulators
+constexpr uint32_t kTmemCols = 512;                    // two accumulators of 64 * (q planes) columns
 
 struct Misc {
     uint32_t tmem;
@@ -60,6 +61,11 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
         if ((i & 255u) == 255u && *abort) return false;
     }
     return false;
+}
+
+// A wait taken by a whole warp; the result is made warp-uniform.
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort));
 }
 
 // Exact three-way split of 8 f32 values into bf16 planes, packed as 3 x uint4.
@@ -79,6 +85,13 @@ __device__ __forceinline__ void split3(const float (&x)[8], uint4 (&pl)[3]) {
     }
 #pragma unroll
     for (int k = 0; k < 3; ++k) pl[k] = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+}
+
+// Byte offset of unit u (dims 8u..8u+7) of head h of q plane `plane` when the nq planes
+// are stacked along N: per 64-dim chunk, plane 0's 64 heads, then plane 1's, ... so one
+// MMA with N = 64 * nq multiplies a row tile by every plane at once.
+__device__ __forceinline__ uint32_t q_off(uint32_t plane, uint32_t h, uint32_t u, uint32_t nq) {
+    return (u >> 3) * (nq * kH * 128u) + plane * (kH * 128u) + sw128_offset(h, (u & 7u) * 8u);
 }
 
 // Byte offset of the 16-byte unit u (dims 8u..8u+7) of row r in a K-major [rows x 128]
@@ -118,6 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
     const int64_t Np = p.key_off[bq + 1] - k0;
 
     // ---- per-row validity: uniform over the CTA ----
+    if (MODE == kFine)
+        for (int e = tid; e < p.keep; e += kThreads) blk[e] = p.top_blk[(int64_t)row * p.keep + e];
+    __syncthreads();
     if (tid == 0) {
         int st = 0;
         const bool first = blockIdx.y == 0;
@@ -132,13 +148,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
             st = 1;
             flag(p.status, HISA_DEV_BAD_OFFSETS);
         } else if (MODE == kFine) {
-            const int32_t *tb = p.top_blk + (int64_t)row * p.keep;
-            for (int s = 0; s < p.keep; ++s) {     // insertion sort: candidates in ascending pos
-                int v = tb[s], u = s;
-                if (v < 0 || (int64_t)v >= Np / p.b) st = 1;
+            for (int s = 1; s < p.keep; ++s) {     // insertion sort: candidates in ascending pos
+                const int v = blk[s];
+                int u = s;
                 while (u > 0 && blk[u - 1] > v) { blk[u] = blk[u - 1]; --u; }
                 blk[u] = v;
             }
+            for (int s = 0; s < p.keep; ++s)
+                if (blk[s] < 0 || (int64_t)blk[s] >= Np / p.b) st = 1;
             if (st) flag(p.status, HISA_DEV_BAD_BLOCK);
         }
         s_state = st;
@@ -183,23 +200,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
     if (warp >= kLoadWarp0) {
         // ---------------- loaders ----------------
         const int lt = tid - kLoadWarp0 * 32;
-        for (int u = lt; u < kH * 16; u += kLoaders) {      // q planes and scaled weights
-            const int h = u >> 4, uu = u & 15;
-            const uint32_t off = unit_off(h, uu, kH);
-            if (QBF16) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const __nv_bfloat16 *>(p.q) + ((int64_t)row * kH + h) * kD) + uu);
-                *reinterpret_cast<uint4 *>(smem + kOffQ + off) = v;
-            } else {
-                const float4 *src = reinterpret_cast<const float4 *>(
-                    reinterpret_cast<const float *>(p.q) + ((int64_t)row * kH + h) * kD + uu * 8);
-                const float4 a = __ldg(src), b = __ldg(src + 1);
-                const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        // q planes: all loads of this thread first (8 units in flight), then the splits
+        constexpr int kQU = kH * 16 / kLoaders;                    // 16-byte q units per thread
+        if (QBF16) {
+            uint4 v[kQU];
+            const uint4 *q16 = reinterpret_cast<const uint4 *>(
+                reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)row * kH * kD);
+#pragma unroll
+            for (int m = 0; m < kQU; ++m) v[m] = __ldg(q16 + lt + m * kLoaders);
+#pragma unroll
+            for (int m = 0; m < kQU; ++m) {
+                const int u = lt + m * kLoaders;
+                *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(0, u >> 4, u & 15, NQ)) = v[m];
+            }
+        } else {
+            float4 v[2 * kQU];
+            const float4 *q4 = reinterpret_cast<const float4 *>(
+                reinterpret_cast<const float *>(p.q) + (int64_t)row * kH * kD);
+#pragma unroll
+            for (int m = 0; m < kQU; ++m) {
+                v[2 * m] = __ldg(q4 + 2 * (lt + m * kLoaders));
+                v[2 * m + 1] = __ldg(q4 + 2 * (lt + m * kLoaders) + 1);
+            }
+#pragma unroll
+            for (int m = 0; m < kQU; ++m) {
+                const int u = lt + m * kLoaders;
+                const float x[8] = {v[2 * m].x, v[2 * m].y, v[2 * m].z, v[2 * m].w,
+                                    v[2 * m + 1].x, v[2 * m + 1].y, v[2 * m + 1].z, v[2 * m + 1].w};
                 uint4 pl[3];
                 split3(x, pl);
 #pragma unroll
                 for (int k = 0; k < 3; ++k)
-                    *reinterpret_cast<uint4 *>(smem + kOffQ + k * kPlaneQ + off) = pl[k];
+                    *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(k, u >> 4, u & 15, NQ)) = pl[k];
             }
         }
         for (int h = lt; h < kH; h += kLoaders) sw[h] = p.w[(int64_t)row * kH + h] * p.head_scale;
@@ -255,7 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
                     const int64_t c = (int64_t)(t_begin + i) * kTile + r;
                     const bool v = c < n;
                     int64_t pos = c;
-                    if (MODE == kFine && v) pos = (int64_t)blk[c / p.b] * p.b + (c % p.b);
+                    if (MODE == kFine && v) {             // n <= kMaxSel: 32-bit math is exact
+                        const uint32_t c32 = (uint32_t)c, b32 = (uint32_t)p.b, q32 = c32 / b32;
+                        pos = (int64_t)blk[q32] * p.b + (c32 - q32 * b32);
+                    }
                     const void *src = v ? static_cast<const void *>(keys + pos * kD + uu * 8) : p.rows;
                     cp_async16_zfill(slot + unit_off(r, uu, kTile), src, v);
                 }
@@ -264,45 +299,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
             cp_async_wait_all();
         }
     } else if (warp == kMmaWarp) {
-        // ---------------- MMA issue (one thread) ----------------
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
-            ok = wait_bar(&bars[kBarQ], 0, abort);
-            for (int i = 0; i < T && ok; ++i) {
-                const int s = MODE == kCoarse ? 0 : i % kSlots;
-                const uint32_t ph = MODE == kCoarse ? (uint32_t)(i & 1) : (uint32_t)((i / kSlots) & 1);
-                const int db = i & 1;
-                if (!wait_bar(&bars[kBarFull + s], ph, abort) ||
-                    (i >= 2 && !wait_bar(&bars[kBarDFree + db], ((i >> 1) - 1) & 1, abort))) {
-                    ok = false;
-                    break;
-                }
-                fence_after_sync();
-                const uint32_t rbase = sbase + kOffRows + s * kPlaneRows;
-                uint32_t acc = 0;
-#pragma unroll 1
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t ko = ks >> 2, kb = (ks & 3) * 32;
-#pragma unroll
-                    for (int ra = 0; ra < NR; ++ra)
-#pragma unroll
-                        for (int qa = 0; qa < NQ; ++qa) {
-                            if (ra + qa > 2) continue;
-                            const uint64_t a = smem_desc_sw128(
-                                rbase + ra * kPlaneRows + ko * (kTile * 128) + kb, 16, 1024);
-                            const uint64_t b = smem_desc_sw128(
-                                sbase + kOffQ + qa * kPlaneQ + ko * (kH * 128) + kb, 16, 1024);
-                            mma_bf16(tmem + db * 64, a, b, idesc, acc);
-                            acc = 1;
-                        }
-                }
-                mma_commit(&bars[kBarEmpty + s]);
-                mma_commit(&bars[kBarDFull + db]);
+        // ---------------- MMA issue (warp-uniform loop, one elected lane issues) -------
+        // N = 64 * NQ: every q plane in one instruction; each rows plane is one MMA per
+        // K step (the coarse stage's 3 x 3 plane pairs all accumulate, the smallest
+        // ones below 2^-24 of the product included).
+        const uint32_t idesc = idesc_bf16_f32(128, 64 * NQ, 0, 0);
+        const uint64_t qd = smem_desc_sw128(sbase + kOffQ, 16, 1024);
+        ok = wait_bar_warp(&bars[kBarQ], 0, abort);
+        for (int i = 0; i < T && ok; ++i) {
+            const int s = MODE == kCoarse ? 0 : i % kSlots;
+            const uint32_t ph = MODE == kCoarse ? (uint32_t)(i & 1) : (uint32_t)((i / kSlots) & 1);
+            const int db = i & 1;
+            if (!wait_bar_warp(&bars[kBarFull + s], ph, abort) ||
+                (i >= 2 && !wait_bar_warp(&bars[kBarDFree + db], ((i >> 1) - 1) & 1, abort))) {
+                ok = false;
+                break;
             }
-            mma_commit(&bars[kBarDrain]);
-            wait_bar(&bars[kBarDrain], 0, abort);
+            fence_after_sync();
+            const uint64_t rd = smem_desc_sw128(sbase + kOffRows + s * kPlaneRows, 16, 1024);
+            const uint32_t d = tmem + db * (64 * NQ);
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const uint32_t ko = ks >> 2, kb = (ks & 3) * 32;
+#pragma unroll
+                for (int ra = 0; ra < NR; ++ra)
+                    mma_bf16_warp(d, desc_add(rd, ra * kPlaneRows + ko * (kTile * 128) + kb),
+                                  desc_add(qd, ko * (NQ * kH * 128) + kb), idesc,
+                                  (ks > 0 || ra > 0) ? 1u : 0u);
+            }
+            mma_commit_warp(&bars[kBarEmpty + s]);
+            mma_commit_warp(&bars[kBarDFull + db]);
         }
-        __syncwarp();
+        mma_commit_warp(&bars[kBarDrain]);
+        wait_bar_warp(&bars[kBarDrain], 0, abort);
     } else {
         // ---------------- epilogue: one row per thread ----------------
         const int quad = warp & 3;
@@ -312,23 +341,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
             const int db = i & 1;
             if (!wait_bar(&bars[kBarDFull + db], (i >> 1) & 1, abort)) { ok = false; break; }
             fence_after_sync();
-            float v[4][16];
-            const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + db * 64;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld16(ta + c * 16, v[c]);
-            tmem_ld_wait();
-            fence_before_sync();
-            mbar_arrive(&bars[kBarDFree + db]);
+            const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + db * (64 * NQ);
             float acc = 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c) {           // 16 heads at a time: dot = sum over q planes
+                float v[NQ][16];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) acc = fmaf(sw[c * 16 + q], fmaxf(v[c][q], 0.f), acc);
+                for (int qa = 0; qa < NQ; ++qa) tmem_ld16(ta + qa * 64 + c * 16, v[qa]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    float dot = v[0][q];
+#pragma unroll
+                    for (int qa = 1; qa < NQ; ++qa) dot += v[qa][q];
+                    acc = fmaf(sw[c * 16 + q], fmaxf(dot, 0.f), acc);
+                }
+            }
+            fence_before_sync();
+            mbar_arrive(&bars[kBarDFree + db]);
             const int64_t cidx = (int64_t)(t_begin + i) * kTile + r;
             if (cidx < n) {
                 int64_t pos = cidx;
                 if (MODE == kCoarse) pos = cidx * p.b;   // a block is eligible iff its first row is visible
-                if (MODE == kFine) pos = (int64_t)blk[cidx / p.b] * p.b + (cidx % p.b);
+                if (MODE == kFine) {
+                    const uint32_t c32 = (uint32_t)cidx, b32 = (uint32_t)p.b, q32 = c32 / b32;
+                    pos = (int64_t)blk[q32] * p.b + (c32 - q32 * b32);
+                }
                 const float score = pos < V ? acc : kNeg;
                 if (MODE != kFlat) sc[cidx] = score;
                 if (p.out) p.out[(int64_t)row * p.ld_out + cidx] = score;
@@ -350,9 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
         const int aborted = misc->abort;
         const int64_t kout = aborted ? 0 : (n < P.k_sel ? n : (int64_t)P.k_sel);
         if (MODE == kFine) {
-            const int b = p.b;
+            const uint32_t b = (uint32_t)p.b;
             block_topk<kThreads>(sc, n, kout, out,
-                                 [&](int64_t i) { return (int32_t)((int64_t)blk[i / b] * b + (i % b)); },
+                                 [&](int64_t i) {
+                                     const uint32_t q32 = (uint32_t)i / b;
+                                     return (int32_t)((uint32_t)blk[q32] * b + ((uint32_t)i - q32 * b));
+                                 },
                                  sel_sh, p.status);
         } else {
             block_topk<kThreads>(sc, n, kout, out, [](int64_t i) { return (int32_t)i; }, sel_sh,

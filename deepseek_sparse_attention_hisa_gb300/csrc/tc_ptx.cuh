@@ -39,6 +39,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// The start address is the low 14-bit field (address >> 4); shared memory is < 256 KiB,
+// so moving a descriptor by a byte offset is an add of offset >> 4 with no carry out.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_offset) {
+    return desc + (uint64_t)(byte_offset >> 4);
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, f32 accumulator.
 // a_mn / b_mn select MN-major (transposed) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
@@ -84,6 +90,27 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         "setp.ne.u32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Warp-wide: the whole warp passes the same (warp-uniform) operands and one lane,
+// chosen by elect.sync, issues the MMA. Keeping the issue loop warp-uniform lets the
+// descriptors live in uniform registers instead of being moved there per instruction.
+__device__ __forceinline__ void mma_bf16_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Warp-wide: one elected lane commits (see mma_commit).
+__device__ __forceinline__ void mma_commit_warp(uint64_t *mbar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        :: "r"(smem_u32(mbar)) : "memory");
 }
 
 // One thread: arrive (once) on an mbarrier when all previously issued MMAs complete.
