@@ -33,15 +33,15 @@ class IndexDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("L", ctypes.c_int32), ("H_i", ctypes.c_int32),
                 ("D_i", ctypes.c_int32), ("r", ctypes.c_int32), ("index_topk", ctypes.c_int32),
                 ("index_block", ctypes.c_int32), ("index_keep", ctypes.c_int32),
-                ("Np_max", ctypes.c_int64), ("q_dtype", ctypes.c_int32),
-                ("k_dtype", ctypes.c_int32)]
+                ("Np_max", ctypes.c_int64), ("keys_rows", ctypes.c_int64),
+                ("q_dtype", ctypes.c_int32), ("k_dtype", ctypes.c_int32)]
 
 
 class AttnDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("L", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("Dh", ctypes.c_int32), ("window", ctypes.c_int32), ("W_max", ctypes.c_int32),
                 ("r", ctypes.c_int32), ("k", ctypes.c_int32), ("Np_max", ctypes.c_int64),
-                ("scale", ctypes.c_float), ("q_dtype", ctypes.c_int32),
+                ("kv_rows", ctypes.c_int64), ("scale", ctypes.c_float), ("q_dtype", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32)]
 
 

@@ -25,6 +25,7 @@ hisa_status check_index_desc(const hisa_index_desc *d) {
     if (d->index_topk < 1 || d->index_topk > kMaxTopk) return HISA_EINVAL;
     if (d->index_block < 0 || d->index_keep < 0 || d->index_keep > 64) return HISA_EINVAL;
     if (d->Np_max < 0 || d->Np_max > (int64_t)65535 * 256) return HISA_EINVAL;
+    if (d->keys_rows < 0 || d->keys_rows > 0x7fffffffLL) return HISA_EINVAL;
     if ((int64_t)d->B * d->L > 0x7fffffffLL) return HISA_EINVAL;
     if (!dtype_ok(d->q_dtype) || !dtype_ok(d->k_dtype)) return HISA_EDTYPE;
     if (d->D_i != 32 && d->D_i != 64 && d->D_i != 128) return HISA_EDTYPE;
@@ -47,6 +48,7 @@ hisa_status check_attn_desc(const hisa_attn_desc *d) {
         d->k > kMaxTopk)
         return HISA_EINVAL;
     if (d->Np_max < 0 || d->Np_max > 0x7fffffffLL) return HISA_EINVAL;
+    if (d->kv_rows < 0 || d->kv_rows > 0x7fffffffLL) return HISA_EINVAL;
     if ((int64_t)d->B * d->L > 0x7fffffffLL) return HISA_EINVAL;
     if (!dtype_ok(d->q_dtype) || !dtype_ok(d->kv_dtype) || d->q_dtype != d->kv_dtype)
         return HISA_EDTYPE;
@@ -114,6 +116,7 @@ ScoreParams score_params(const hisa_index_desc *d, int mode, const void *q, cons
     p.key_off = key_off; p.t0 = t0;
     p.out = out; p.ld_out = ld;
     p.Np_max = d->Np_max;
+    p.keys_rows = d->keys_rows;
     p.status = status_of(ws);
     return p;
 }
@@ -123,7 +126,8 @@ ScoreParams score_params(const hisa_index_desc *d, int mode, const void *q, cons
 cudaError_t run_scores(const ScoreParams &p, int32_t *sel, int k_sel, bool *fused,
                        cudaStream_t s) {
     *fused = false;
-    if (score_tc_supported(p.mode, p.H_i, p.D_i, p.rows_bf16, p.n_max)) {
+    if (score_tc_supported(p.mode, p.H_i, p.D_i, p.rows_bf16, p.n_max, p.b) &&
+        (p.mode == kCoarse || p.keys_rows > 0)) {
         ScoreTcParams t{};
         t.s = p;
         t.sel = sel;
@@ -231,7 +235,7 @@ hisa_status hisa_block_means(const hisa_index_desc *d, const void *keys, const i
     p.B = d->B; p.D_i = d->D_i; p.b = d->index_block;
     p.keys = keys; p.keys_bf16 = d->k_dtype == HISA_BF16;
     p.key_off = key_off; p.means_off = means_off; p.first_block = first_block;
-    p.means = means; p.Np_max = d->Np_max; p.status = status_of(ws);
+    p.means = means; p.Np_max = d->Np_max; p.keys_rows = d->keys_rows; p.status = status_of(ws);
     return from_cuda(launch_block_means(p, d->Np_max / d->index_block,
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -251,7 +255,7 @@ hisa_status hisa_block_filter(const hisa_index_desc *d, const void *q, const flo
     if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_BLOCK_FILTER, d))) != HISA_OK)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool tc = score_tc_supported(kCoarse, d->H_i, d->D_i, 0, nb_max);
+    const bool tc = score_tc_supported(kCoarse, d->H_i, d->D_i, 0, nb_max, d->index_block);
     float *buf = cscores ? cscores : (tc ? nullptr : scratch_of(ws));
     const int64_t ld = cscores ? ld_cscores : (nb_max > 0 ? nb_max : 1);
     ScoreParams p = score_params(d, kCoarse, q, w, means, 0, key_off, t0, buf, ld, ws);
@@ -265,7 +269,7 @@ hisa_status hisa_block_filter(const hisa_index_desc *d, const void *q, const flo
     sp.mode = kCoarse; sp.B = d->B; sp.L = d->L; sp.b = d->index_block; sp.keep = d->index_keep;
     sp.k = d->index_keep;
     sp.scores = buf; sp.ld = ld; sp.key_off = key_off; sp.out = top_blk;
-    sp.Np_max = d->Np_max; sp.status = status_of(ws);
+    sp.Np_max = d->Np_max; sp.keys_rows = d->keys_rows; sp.status = status_of(ws);
     return from_cuda(launch_select(sp, nb_max, s));
 }
 
@@ -282,7 +286,8 @@ hisa_status hisa_select_topk(const hisa_index_desc *d, const void *q, const floa
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t C = (int64_t)d->index_block * d->index_keep;
-    const bool tc = score_tc_supported(kFine, d->H_i, d->D_i, d->k_dtype == HISA_BF16, C);
+    const bool tc = score_tc_supported(kFine, d->H_i, d->D_i, d->k_dtype == HISA_BF16, C,
+                                       d->index_block) && d->keys_rows > 0;
     float *buf = fscores ? fscores : (tc ? nullptr : scratch_of(ws));
     ScoreParams p = score_params(d, kFine, q, w, keys, d->k_dtype == HISA_BF16, key_off, t0, buf,
                                  C, ws);
@@ -296,7 +301,7 @@ hisa_status hisa_select_topk(const hisa_index_desc *d, const void *q, const floa
     sp.mode = kFine; sp.B = d->B; sp.L = d->L; sp.b = d->index_block; sp.keep = d->index_keep;
     sp.k = d->index_topk;
     sp.scores = buf; sp.ld = C; sp.key_off = key_off; sp.top_blk = top_blk; sp.out = I;
-    sp.Np_max = d->Np_max; sp.status = status_of(ws);
+    sp.Np_max = d->Np_max; sp.keys_rows = d->keys_rows; sp.status = status_of(ws);
     return from_cuda(launch_select(sp, C, s));
 }
 
@@ -322,7 +327,7 @@ hisa_status hisa_flat_topk(const hisa_index_desc *d, const void *q, const float 
     sp.mode = kFlat; sp.B = d->B; sp.L = d->L; sp.b = d->index_block; sp.keep = d->index_keep;
     sp.k = d->index_topk;
     sp.scores = buf; sp.ld = ld; sp.key_off = key_off; sp.out = I;
-    sp.Np_max = d->Np_max; sp.status = status_of(ws);
+    sp.Np_max = d->Np_max; sp.keys_rows = d->keys_rows; sp.status = status_of(ws);
     return from_cuda(launch_select(sp, d->Np_max, s));
 }
 
@@ -347,6 +352,7 @@ hisa_status hisa_sparse_attend(const hisa_attn_desc *d, const void *q, const voi
     p.r = d->r; p.k = dense ? 0 : d->k;
     p.causal = d->L > 1;
     p.Np_max = d->Np_max;
+    p.kv_rows = d->kv_rows;
     p.scale = d->scale > 0.f ? d->scale : (float)(1.0 / std::sqrt((double)d->Dh));
     p.q = q; p.local_kv = local_kv; p.local_len = local_len; p.local_pos0 = local_pos0;
     p.pooled_kv = pooled_kv; p.kv_off = kv_off; p.I = I; p.sinks = sinks; p.t0 = t0;

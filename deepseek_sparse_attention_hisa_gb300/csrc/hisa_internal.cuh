@@ -2,6 +2,7 @@
 // Nothing here is part of the C ABI (see include/hisa.h).
 #pragma once
 
+#include <cuda.h>              // CUtensorMap (the encoder is fetched from the driver at run time)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -34,6 +35,13 @@ __device__ __forceinline__ int64_t visible_len(int64_t t, int r, int64_t Np) {
     return v < Np ? v : Np;
 }
 
+// Sequence b's pooled rows [off[b], off[b+1]) are usable iff they are ordered, fit Np_max
+// and lie inside the allocation of `rows` rows.
+__device__ __forceinline__ bool seq_ok(const int64_t *off, int b, int64_t Np_max, int64_t rows) {
+    const int64_t a = off[b], e = off[b + 1];
+    return a >= 0 && e >= a && e - a <= Np_max && e <= rows;
+}
+
 // Orderable key of an f32 score: larger float -> larger key; -0.0 == +0.0.
 __device__ __forceinline__ uint32_t order_key(float s) {
     uint32_t u = __float_as_uint(s);
@@ -62,6 +70,7 @@ struct ScoreParams {
     int64_t ld_out;
     int64_t n_max;            // max scored rows per query row (grid.x extent)
     int64_t Np_max;
+    int64_t keys_rows;        // rows allocated in the key array
     uint32_t *status;
 };
 
@@ -74,6 +83,7 @@ struct SelectParams {
     const int32_t *top_blk;   // fine: [B*L, keep]
     int32_t *out;             // [B*L, k]
     int64_t Np_max;
+    int64_t keys_rows;        // rows allocated in the key array (the scored rows' bound)
     uint32_t *status;
 };
 
@@ -86,6 +96,7 @@ struct MeansParams {
     const int32_t *first_block;
     float *means;
     int64_t Np_max;
+    int64_t keys_rows;
     uint32_t *status;
 };
 
@@ -93,6 +104,7 @@ struct AttnParams {
     int B, L, H, Dh, window, W_max, r, k;
     int causal;
     int64_t Np_max;
+    int64_t kv_rows;          // rows allocated in pooled_kv
     float scale;
     const void *q;            // [B*L, H, Dh]
     const void *local_kv;     // [B, W_max, Dh]
@@ -115,11 +127,18 @@ struct AttnParams {
 // coarse and fine modes also select (sel = top_blk or I, k_sel ids per query row); s.out
 // is optional for them (the scores of every row) and required for the flat mode.
 struct ScoreTcParams {
+    CUtensorMap keys_map;     // bf16 keys [keys_rows, 128], box 64 dims x 64 rows, 128B swizzle
     ScoreParams s;
     int32_t *sel;
     int k_sel;
     int tiles_per_cta;        // flat: 128-row tiles per CTA (grid.y covers the row)
 };
+
+// Encodes a 2-D bf16 tensor map over [rows, cols] (row-major) with a box of box_cols x
+// box_rows and the 128-byte swizzle. Returns false if the driver has no encoder or
+// rejects the map.
+bool encode_bf16_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                     uint32_t box_cols, uint32_t box_rows);
 
 // ---------------------------------------------------------------------------
 // host launchers (one per kernel file); return the cudaGetLastError() of the launch
@@ -134,6 +153,6 @@ int attend_simt_supported(int H, int Dh);
 int attend_tc_supported(int H, int Dh, int kv_bf16);
 int attend_chunk_rows();
 cudaError_t launch_score_tc(const ScoreTcParams &p, cudaStream_t s);
-int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max);
+int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b);
 
 }  // namespace hisa

@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend_simt(AttnParams p) {
     const int64_t t = (int64_t)p.t0[bq] + j;
     const int64_t k0 = p.kv_off[bq];
     int64_t Np = p.kv_off[bq + 1] - k0;
-    if (Np < 0 || Np > p.Np_max) {
+    if (!seq_ok(p.kv_off, bq, p.Np_max, p.kv_rows)) {
         if (tid == 0 && split == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
         Np = 0;
     }

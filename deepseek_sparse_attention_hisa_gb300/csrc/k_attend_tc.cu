@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
     const int64_t t = (int64_t)p.t0[bq] + j;
     const int64_t k0 = p.kv_off[bq];
     int64_t Np = p.kv_off[bq + 1] - k0;
-    const bool bad_off = Np < 0 || Np > p.Np_max;
+    const bool bad_off = !seq_ok(p.kv_off, bq, p.Np_max, p.kv_rows);
     if (bad_off) Np = 0;
     // visible local window rows [lo, hi) of this query row
     int64_t nl = p.local_len[bq];

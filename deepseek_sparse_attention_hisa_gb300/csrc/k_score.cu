@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(256) k_scores_simt(ScoreParams p) {
     const int j = row - bq * p.L;
     const int64_t k0 = p.key_off[bq];
     const int64_t Np = p.key_off[bq + 1] - k0;
-    if (Np < 0 || Np > p.Np_max) {
+    if (!seq_ok(p.key_off, bq, p.Np_max, p.keys_rows)) {
         if (threadIdx.x == 0 && blockIdx.y == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
         return;
     }
@@ -170,7 +170,7 @@ __global__ void k_block_means(MeansParams p) {
     const int bq = blockIdx.y;
     const int64_t k0 = p.key_off[bq];
     const int64_t Np = p.key_off[bq + 1] - k0;
-    if (Np < 0 || Np > p.Np_max) {
+    if (!seq_ok(p.key_off, bq, p.Np_max, p.keys_rows)) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
         return;
     }

@@ -16,8 +16,8 @@
 // weights and the head sum in registers, with no cross-thread reduction.
 //
 // Warp roles: 0 MMA issue + TMEM owner, 1-4 epilogue (warp w reads TMEM lanes
-// 32*(w%4)..+31), 5-8 loaders (q planes; bf16 rows by cp.async with the 128-byte
-// swizzle, f32 rows through registers, split into planes). Coarse and fine CTAs own one
+// 32*(w%4)..+31), 5-8 loaders (q planes; bf16 rows by TMA with the 128-byte swizzle,
+// f32 rows through registers, split into planes). Coarse and fine CTAs own one
 // query row and finish with block_topk over the scores held in shared memory; flat CTAs
 // own a range of tiles of one query row and write scores to global memory.
 // Waits are bounded; a timeout raises HISA_DEV_TIMEOUT and the CTA drains and exits.
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
     if (tid == 0) {
         int st = 0;
         const bool first = blockIdx.y == 0;
-        if (Np < 0 || Np > p.Np_max) {
+        if (!seq_ok(p.key_off, bq, p.Np_max, p.keys_rows)) {
             st = 1;
             if (first) flag(p.status, HISA_DEV_BAD_OFFSETS);
         } else if (MODE != kFlat && Np < (int64_t)p.b * p.keep) {
@@ -180,7 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) {
             uint32_t cnt = 1;
-            if ((b >= kBarFull && b < kBarFull + kSlots) || b == kBarQ) cnt = kLoaders;
+            if (b >= kBarFull && b < kBarFull + kSlots) cnt = MODE == kCoarse ? kLoaders : 1;
+            if (b == kBarQ) cnt = kLoaders;
             if (b == kBarDFree || b == kBarDFree + 1) cnt = kEpis;
             mbar_init(&bars[b], cnt);
         }
@@ -272,8 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
                 mbar_arrive(&bars[kBarFull]);
                 if (i + 1 < T) load_tile(t_begin + i + 1);
             }
-        } else {
-            const __nv_bfloat16 *keys = reinterpret_cast<const __nv_bfloat16 *>(p.rows) + k0 * kD;
+        } else if (lt == 0) {
+            // bf16 rows: one loader thread streams each 128-row tile as up to 4 TMA boxes
+            // (two 64-row halves x two 64-dim chunks) with the 128-byte swizzle. A fine
+            // tile's halves are two kept blocks (index_block = 64); a flat tile's halves
+            // are consecutive rows. Rows past Np or past the allocation are never scored.
+            int issued = 0;
             for (int i = 0; i < T; ++i) {
                 const int s = i % kSlots;
                 if (i >= kSlots && !wait_bar(&bars[kBarEmpty + s], ((i / kSlots) - 1) & 1, abort)) {
@@ -281,22 +286,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
                     break;
                 }
                 const uint32_t slot = sbase + kOffRows + s * kPlaneRows;
-#pragma unroll 4
-                for (int m = 0; m < 16; ++m) {
-                    const int r = r0 + 8 * m;
-                    const int64_t c = (int64_t)(t_begin + i) * kTile + r;
-                    const bool v = c < n;
-                    int64_t pos = c;
-                    if (MODE == kFine && v) {             // n <= kMaxSel: 32-bit math is exact
-                        const uint32_t c32 = (uint32_t)c, b32 = (uint32_t)p.b, q32 = c32 / b32;
-                        pos = (int64_t)blk[q32] * p.b + (c32 - q32 * b32);
-                    }
-                    const void *src = v ? static_cast<const void *>(keys + pos * kD + uu * 8) : p.rows;
-                    cp_async16_zfill(slot + unit_off(r, uu, kTile), src, v);
+                const int64_t c0 = (int64_t)(t_begin + i) * kTile;
+                const int nbox = c0 + 64 < n ? 2 : 1;
+                mbar_arrive_expect_tx(&bars[kBarFull + s], (uint32_t)nbox * 2u * 8192u);
+                for (int hb = 0; hb < nbox; ++hb) {
+                    const int64_t c = c0 + hb * 64;
+                    const int64_t y = MODE == kFine ? k0 + (int64_t)blk[c >> 6] * 64 : k0 + c;
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch)
+                        tma_load_2d(slot + ch * (kTile * 128) + hb * 8192, &P.keys_map, ch * 64, (int32_t)y,
+                                    &bars[kBarFull + s]);
                 }
-                cp_async_arrive(&bars[kBarFull + s]);
+                ++issued;
             }
-            cp_async_wait_all();
+            if (!ok) {   // let the copies already in flight land before the CTA can exit
+                for (int i = issued - 1; i >= 0 && i >= issued - kSlots; --i)
+                    wait_bar(&bars[kBarFull + i % kSlots], (i / kSlots) & 1, abort);
+            }
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (warp-uniform loop, one elected lane issues) -------
@@ -408,10 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
 
 namespace hisa {
 
-int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max) {
+int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b) {
     if (H_i != kH || D_i != kD) return 0;
     if (mode == kCoarse) return !rows_bf16 && n_max <= kMaxSel;
-    if (mode == kFine) return rows_bf16 && n_max <= kMaxSel;
+    if (mode == kFine) return rows_bf16 && n_max <= kMaxSel && b == 64;
     return rows_bf16;
 }
 
@@ -427,6 +433,9 @@ static cudaError_t launch_t(const ScoreTcParams &p, dim3 grid, cudaStream_t s) {
 cudaError_t launch_score_tc(const ScoreTcParams &p_in, cudaStream_t s) {
     ScoreTcParams p = p_in;
     const int64_t rows = (int64_t)p.s.B * p.s.L;
+    if (p.s.mode != kCoarse &&
+        !encode_bf16_map(&p.keys_map, p.s.rows, (uint64_t)p.s.keys_rows, kD, 64, 64))
+        return cudaErrorInvalidValue;
     dim3 grid((unsigned)rows, 1);
     if (p.s.mode == kFlat) {
         const int64_t tiles = (p.s.Np_max + kTile - 1) / kTile;

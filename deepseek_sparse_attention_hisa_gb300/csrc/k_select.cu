@@ -18,7 +18,7 @@ __global__ void __launch_bounds__(NT) k_select(SelectParams p) {
 
     const int64_t k0 = p.key_off[bq];
     const int64_t Np = p.key_off[bq + 1] - k0;
-    bool ok = Np >= 0 && Np <= p.Np_max;
+    bool ok = seq_ok(p.key_off, bq, p.Np_max, p.keys_rows);
     int64_t n = 0;
     if (!ok) {
         if (tid == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);

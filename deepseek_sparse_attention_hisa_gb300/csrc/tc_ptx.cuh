@@ -184,6 +184,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity,
     return false;
 }
 
+// ---- TMA ------------------------------------------------------------------------
+// Arrive on mbar and add `bytes` to the transaction count its current phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *mbar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\t"
+                 "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 :: "r"(smem_u32(mbar)), "r"(bytes) : "memory");
+}
+// One thread: load the box at element coordinates (x, y) of the 2-D tensor map `tmap`
+// (a __grid_constant__ kernel parameter) into shared memory at dst; completion is
+// counted in bytes on mbar. x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int32_t x, int32_t y,
+                                            uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(mbar))
+        : "memory");
+}
+
 // ---- cp.async (16-byte global -> shared copies) ---------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void *g) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(saddr), "l"(g) : "memory");

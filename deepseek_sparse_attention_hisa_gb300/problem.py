@@ -49,6 +49,7 @@ class Problem:
         self.idesc = hb.IndexDesc(
             B=wl.B, L=wl.L, H_i=wl.H_i, D_i=wl.D_i, r=wl.r, index_topk=wl.index_topk,
             index_block=self.b, index_keep=self.keep, Np_max=self.Np_max,
+            keys_rows=int(self.keys.shape[0]),
             q_dtype=hb.dtype_code(self.q_idx), k_dtype=hb.dtype_code(self.keys))
         nb = Np // self.b if self.b > 0 else np.zeros_like(Np)
         self.nb = nb
@@ -75,7 +76,7 @@ class Problem:
             self.adesc = hb.AttnDesc(
                 B=wl.B, L=wl.L, H=wl.H, Dh=wl.Dh, window=wl.window,
                 W_max=int(data["local_kv"].shape[1]), r=wl.r, k=self.k, Np_max=self.Np_max,
-                scale=0.0, q_dtype=hb.dtype_code(self.q_attn),
+                kv_rows=int(self.pooled_kv.shape[0]), scale=0.0, q_dtype=hb.dtype_code(self.q_attn),
                 kv_dtype=hb.dtype_code(self.pooled_kv))
             self.out = torch.empty((rows, wl.H, wl.Dh), dtype=torch.float32, device=dev)
             need = max(need, hb.workspace_bytes(hb.OP_SPARSE_ATTEND, self.adesc))

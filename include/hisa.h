@@ -69,7 +69,8 @@ typedef enum {
 typedef enum { HISA_F32 = 0, HISA_BF16 = 1 } hisa_dtype;
 
 /* Bits of the device status word. */
-#define HISA_DEV_BAD_OFFSETS 0x1u /* offsets not monotone, Np_b > Np_max, or a capacity too small */
+#define HISA_DEV_BAD_OFFSETS 0x1u /* offsets not monotone, past keys_rows / kv_rows, Np_b > Np_max,
+                                    or a capacity too small; the sequence is skipped */
 #define HISA_DEV_GATE        0x2u /* a sequence failed Np_b >= index_block*index_keep; rows are -1 */
 #define HISA_DEV_BAD_ID      0x4u /* a selected id outside [-1, Np_b) reached the combine; skipped */
 #define HISA_DEV_NONFINITE   0x8u /* a select saw a non-finite score */
@@ -95,6 +96,7 @@ typedef struct {
     int32_t index_block;  /* b: HiSA block size in pooled rows (0 disables the hierarchy) */
     int32_t index_keep;   /* keep: blocks kept by the coarse stage */
     int64_t Np_max;       /* an upper bound of Np_b over the batch (sizes grids and workspace) */
+    int64_t keys_rows;    /* rows allocated in keys (>= key_off[B]); no key read goes past it */
     int32_t q_dtype;      /* hisa_dtype of q: HISA_F32 or HISA_BF16 */
     int32_t k_dtype;      /* hisa_dtype of the pooled indexer keys */
 } hisa_index_desc;
@@ -109,6 +111,7 @@ typedef struct {
     int32_t r;            /* compress ratio, for V(t) */
     int32_t k;            /* width of I (ignored when I == NULL) */
     int64_t Np_max;       /* an upper bound of Np_b over the batch */
+    int64_t kv_rows;      /* rows allocated in pooled_kv (>= kv_off[B]); no read goes past it */
     float scale;          /* softmax scale; <= 0 selects Dh^-1/2 */
     int32_t q_dtype;      /* hisa_dtype of q; must equal kv_dtype */
     int32_t kv_dtype;     /* hisa_dtype of local_kv and pooled_kv */

@@ -314,3 +314,31 @@ def test_v4_combine_prefill_rows():
     out = np_(prob.out)
     for j in range(0, 40, 3):
         P.check_attend(data, 0, j, out[j], I[j])
+
+
+def test_offsets_past_the_allocation_are_skipped():
+    # keys_rows / kv_rows bound every read: a sequence whose rows end past them is
+    # skipped (-1 rows, zero output) and flagged, and the others are unaffected.
+    data = v4_small(B=2, Np=(2048, 2048), seed=14)
+    prob = Problem(data)
+    prob.block_means()
+    torch.cuda.synchronize()
+    short = hb.IndexDesc.from_buffer_copy(prob.idesc)
+    short.keys_rows = 3000
+    I = torch.full_like(prob.I, -7)
+    hb.flat_topk(short, prob.q_idx, prob.w, prob.keys, prob.key_off, prob.t0, I, prob.ws)
+    hb.select_topk(short, prob.q_idx, prob.w, prob.keys, prob.key_off, prob.t0, prob.top_blk,
+                   prob.I, prob.ws)
+    torch.cuda.synchronize()
+    assert prob.status() & hb.DEV_BAD_OFFSETS
+    assert np.all(np_(I)[1] == -1) and np.all(np_(prob.I)[1] == -1)
+    P.check_flat(data, 0, 0, np_(I)[0], 512)
+    hb.workspace_init(prob.ws)
+    a = hb.AttnDesc.from_buffer_copy(prob.adesc)
+    a.kv_rows = 3000
+    out = torch.full_like(prob.out, 5.0)
+    hb.sparse_attend(a, prob.q_attn, prob.local_kv, prob.local_len, prob.local_pos0,
+                     prob.pooled_kv, prob.key_off, None, prob.sinks, prob.t0, out, prob.ws)
+    torch.cuda.synchronize()
+    assert prob.status() & hb.DEV_BAD_OFFSETS
+    P.check_attend(data, 0, 0, np_(out)[0], None)
