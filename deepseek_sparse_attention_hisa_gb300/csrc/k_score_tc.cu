@@ -29,26 +29,29 @@ namespace {
 
 using namespace tc;
 
-constexpr int kH = 64, kD = 128, kTile = 128;
+// Two CTAs share an SM (one's set-up and select overlap the other's loads): 64-row tiles
+// (M = 64: row r of a tile sits in TMEM lane r % 16 of quadrant r / 16), one 192-column
+// accumulator (256 TMEM columns per CTA), about 100 KiB of shared memory.
+constexpr int kH = 64, kD = 128, kTile = 64;
 constexpr int kThreads = 288;                          // 9 warps
 constexpr int kMmaWarp = 0, kLoadWarp0 = 5;               // epilogue: warps 1-4
 constexpr int kLoaders = 128, kEpis = 128;
 constexpr uint32_t kPlaneQ = kH * kD * 2;              // 16 KiB: [64 heads x 128 dims] bf16
-constexpr uint32_t kPlaneRows = kTile * kD * 2;        // 32 KiB: [128 rows x 128 dims] bf16
+constexpr uint32_t kPlaneRows = kTile * kD * 2;        // 16 KiB: [64 rows x 128 dims] bf16
 constexpr int kSlots = 3;                              // bf16 row tiles in flight
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffRows = kOffQ + 3 * kPlaneQ;     // 96 KiB: 3 slots, or 3 planes of 1 slot
-constexpr uint32_t kOffSc = kOffRows + 3 * kPlaneRows;
-constexpr int kMaxSel = 8192;                          // scores a fused select holds
-constexpr uint32_t kOffW = kOffSc + kMaxSel * 4;
+constexpr uint32_t kOffRows = kOffQ + 3 * kPlaneQ;     // 48 KiB: 3 slots, or 3 planes of 1 slot
+constexpr uint32_t kOffW = kOffRows + 3 * kPlaneRows;
 constexpr uint32_t kOffBlk = kOffW + kH * 4;
 constexpr uint32_t kOffBar = kOffBlk + 64 * 4;
-// barriers: full[3] empty[3] d_full[2] d_free[2] q_full drain
-constexpr int kBarFull = 0, kBarEmpty = 3, kBarDFull = 6, kBarDFree = 8, kBarQ = 10,
-              kBarDrain = 11, kNumBars = 12;
+// barriers: full[3] empty[3] d_full d_free q_full drain
+constexpr int kBarFull = 0, kBarEmpty = 3, kBarDFull = 6, kBarDFree = 7, kBarQ = 8,
+              kBarDrain = 9, kNumBars = 10;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 512;                    // two accumulators of 64 * (q planes) columns
+constexpr uint32_t kOffSc = kOffMisc + 64;             // scores of the fused select: n floats
+constexpr int kMaxSel = 8192;                          // largest n a fused select holds
+constexpr uint32_t kSmemFixed = kOffSc + 1024;         // + alignment slack
+constexpr uint32_t kTmemCols = 256;                    // one accumulator of 64 * (q planes) columns
 
 struct Misc {
     uint32_t tmem;
@@ -107,7 +110,7 @@ namespace hisa {
 namespace {
 
 template <int MODE, bool QBF16>
-__global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant__ ScoreTcParams P) {
+__global__ void __launch_bounds__(kThreads, 2) k_score_tc(const __grid_constant__ ScoreTcParams P) {
     constexpr int NQ = QBF16 ? 1 : 3;                    // q planes
     constexpr int NR = (MODE == kCoarse) ? 3 : 1;        // row planes
     const ScoreParams &p = P.s;
@@ -130,10 +133,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
     const int64_t k0 = p.key_off[bq];
     const int64_t Np = p.key_off[bq + 1] - k0;
 
-    // ---- per-row validity: uniform over the CTA ----
+    // ---- every independent global load first: kept blocks, q, weights, offsets ----
+    constexpr int kQU = kH * 16 / kLoaders;                    // 16-byte q units per loader
+    const int lt = tid - kLoadWarp0 * 32;                      // loader index (warps 5-8)
+    float4 qf[QBF16 ? 1 : 2 * kQU];
+    uint4 qh[QBF16 ? kQU : 1];
+    float wv = 0.f;
     if (MODE == kFine)
         for (int e = tid; e < p.keep; e += kThreads) blk[e] = p.top_blk[(int64_t)row * p.keep + e];
+    if (warp >= kLoadWarp0) {
+        if (QBF16) {
+            const uint4 *q16 = reinterpret_cast<const uint4 *>(
+                reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)row * kH * kD);
+#pragma unroll
+            for (int m = 0; m < kQU; ++m) qh[m] = __ldg(q16 + lt + m * kLoaders);
+        } else {
+            const float4 *q4 = reinterpret_cast<const float4 *>(
+                reinterpret_cast<const float *>(p.q) + (int64_t)row * kH * kD);
+#pragma unroll
+            for (int m = 0; m < kQU; ++m) {
+                qf[2 * m] = __ldg(q4 + 2 * (lt + m * kLoaders));
+                qf[2 * m + 1] = __ldg(q4 + 2 * (lt + m * kLoaders) + 1);
+            }
+        }
+        if (lt < kH) wv = __ldg(p.w + (int64_t)row * kH + lt);
+    }
     __syncthreads();
+
+    // ---- per-row validity (uniform over the CTA) and barrier set-up ----
     if (tid == 0) {
         int st = 0;
         const bool first = blockIdx.y == 0;
@@ -158,6 +185,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
                 if (blk[s] < 0 || (int64_t)blk[s] >= Np / p.b) st = 1;
             if (st) flag(p.status, HISA_DEV_BAD_BLOCK);
         }
+        for (int b = 0; b < kNumBars; ++b) {
+            uint32_t cnt = 1;
+            if (b >= kBarFull && b < kBarFull + kSlots) cnt = MODE == kCoarse ? kLoaders : 1;
+            if (b == kBarQ) cnt = kLoaders;
+            if (b == kBarDFree) cnt = kEpis;
+            mbar_init(&bars[b], cnt);
+        }
+        mbar_fence_init();
+        misc->abort = 0;
         s_state = st;
     }
     __syncthreads();
@@ -177,20 +213,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
     const int T = t_end - t_begin;
     const int64_t V = p.causal ? visible_len((int64_t)p.t0[bq] + j, p.r, Np) : Np;
 
-    if (tid == 0) {
-        for (int b = 0; b < kNumBars; ++b) {
-            uint32_t cnt = 1;
-            if (b >= kBarFull && b < kBarFull + kSlots) cnt = MODE == kCoarse ? kLoaders : 1;
-            if (b == kBarQ) cnt = kLoaders;
-            if (b == kBarDFree || b == kBarDFree + 1) cnt = kEpis;
-            mbar_init(&bars[b], cnt);
-        }
-        mbar_fence_init();
-        misc->abort = 0;
-    }
+    // bf16 rows: one loader thread streams each 64-row tile as two TMA boxes (64 rows x
+    // 64 dims, 128-byte swizzle). A fine tile is one kept block (index_block = 64); a flat
+    // tile is 64 consecutive rows. Rows past Np or past the allocation are loaded as zeros
+    // or never scored.
+    auto issue_tile = [&](int i) {
+        const int s = i % kSlots;
+        const uint32_t slot = sbase + kOffRows + s * kPlaneRows;
+        const int64_t c0 = (int64_t)(t_begin + i) * kTile;
+        const int64_t y = MODE == kFine ? k0 + (int64_t)blk[c0 >> 6] * 64 : k0 + c0;
+        mbar_arrive_expect_tx(&bars[kBarFull + s], 2u * 8192u);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch)
+            tma_load_2d(slot + ch * (kTile * 128), &P.keys_map, ch * 64, (int32_t)y, &bars[kBarFull + s]);
+    };
+    const int pre = MODE == kCoarse ? 0 : (T < kSlots ? T : kSlots);   // tiles issued up front
+    if (MODE != kCoarse && warp >= kLoadWarp0 && lt == 0)
+        for (int i = 0; i < pre; ++i) issue_tile(i);
     if (warp == kMmaWarp) {
         tmem_alloc(&misc->tmem, kTmemCols);
         tmem_relinquish();
+    }
+    if (warp >= kLoadWarp0) {
+        // q planes from the registers loaded above
+        if (QBF16) {
+#pragma unroll
+            for (int m = 0; m < kQU; ++m) {
+                const int u = lt + m * kLoaders;
+                *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(0, u >> 4, u & 15, NQ)) = qh[m];
+            }
+        } else {
+#pragma unroll
+            for (int m = 0; m < kQU; ++m) {
+                const int u = lt + m * kLoaders;
+                const float x[8] = {qf[2 * m].x, qf[2 * m].y, qf[2 * m].z, qf[2 * m].w,
+                                    qf[2 * m + 1].x, qf[2 * m + 1].y, qf[2 * m + 1].z, qf[2 * m + 1].w};
+                uint4 pl[3];
+                split3(x, pl);
+#pragma unroll
+                for (int k = 0; k < 3; ++k)
+                    *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(k, u >> 4, u & 15, NQ)) = pl[k];
+            }
+        }
+        if (lt < kH) sw[lt] = wv * p.head_scale;
+        fence_async_smem();
+        mbar_arrive(&bars[kBarQ]);
     }
     fence_before_sync();
     __syncthreads();
@@ -200,51 +267,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
 
     if (warp >= kLoadWarp0) {
         // ---------------- loaders ----------------
-        const int lt = tid - kLoadWarp0 * 32;
-        // q planes: all loads of this thread first (8 units in flight), then the splits
-        constexpr int kQU = kH * 16 / kLoaders;                    // 16-byte q units per thread
-        if (QBF16) {
-            uint4 v[kQU];
-            const uint4 *q16 = reinterpret_cast<const uint4 *>(
-                reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)row * kH * kD);
-#pragma unroll
-            for (int m = 0; m < kQU; ++m) v[m] = __ldg(q16 + lt + m * kLoaders);
-#pragma unroll
-            for (int m = 0; m < kQU; ++m) {
-                const int u = lt + m * kLoaders;
-                *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(0, u >> 4, u & 15, NQ)) = v[m];
-            }
-        } else {
-            float4 v[2 * kQU];
-            const float4 *q4 = reinterpret_cast<const float4 *>(
-                reinterpret_cast<const float *>(p.q) + (int64_t)row * kH * kD);
-#pragma unroll
-            for (int m = 0; m < kQU; ++m) {
-                v[2 * m] = __ldg(q4 + 2 * (lt + m * kLoaders));
-                v[2 * m + 1] = __ldg(q4 + 2 * (lt + m * kLoaders) + 1);
-            }
-#pragma unroll
-            for (int m = 0; m < kQU; ++m) {
-                const int u = lt + m * kLoaders;
-                const float x[8] = {v[2 * m].x, v[2 * m].y, v[2 * m].z, v[2 * m].w,
-                                    v[2 * m + 1].x, v[2 * m + 1].y, v[2 * m + 1].z, v[2 * m + 1].w};
-                uint4 pl[3];
-                split3(x, pl);
-#pragma unroll
-                for (int k = 0; k < 3; ++k)
-                    *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(k, u >> 4, u & 15, NQ)) = pl[k];
-            }
-        }
-        for (int h = lt; h < kH; h += kLoaders) sw[h] = p.w[(int64_t)row * kH + h] * p.head_scale;
-        fence_async_smem();
-        mbar_arrive(&bars[kBarQ]);
         const int uu = lt & 15, r0 = lt >> 4;             // unit uu of rows r0 + 8m
         if (MODE == kCoarse) {
             const float *means = reinterpret_cast<const float *>(p.rows) + p.means_off[bq] * kD;
-            float4 reg[32];
+            float4 reg[16];
             auto load_tile = [&](int ti) {
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
+                for (int m = 0; m < 8; ++m) {
                     const int64_t c = (int64_t)ti * kTile + r0 + 8 * m;
                     if (c < n) {
                         const float4 *src = reinterpret_cast<const float4 *>(means + c * kD + uu * 8);
@@ -259,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
             for (int i = 0; i < T; ++i) {
                 if (i >= 1 && !wait_bar(&bars[kBarEmpty], (i - 1) & 1, abort)) { ok = false; break; }
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
+                for (int m = 0; m < 8; ++m) {
                     const float4 a = reg[2 * m], b = reg[2 * m + 1];
                     const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
                     uint4 pl[3];
@@ -274,29 +303,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
                 if (i + 1 < T) load_tile(t_begin + i + 1);
             }
         } else if (lt == 0) {
-            // bf16 rows: one loader thread streams each 128-row tile as up to 4 TMA boxes
-            // (two 64-row halves x two 64-dim chunks) with the 128-byte swizzle. A fine
-            // tile's halves are two kept blocks (index_block = 64); a flat tile's halves
-            // are consecutive rows. Rows past Np or past the allocation are never scored.
-            int issued = 0;
-            for (int i = 0; i < T; ++i) {
-                const int s = i % kSlots;
-                if (i >= kSlots && !wait_bar(&bars[kBarEmpty + s], ((i / kSlots) - 1) & 1, abort)) {
+            int issued = pre;
+            for (int i = pre; i < T; ++i) {
+                if (!wait_bar(&bars[kBarEmpty + i % kSlots], ((i / kSlots) - 1) & 1, abort)) {
                     ok = false;
                     break;
                 }
-                const uint32_t slot = sbase + kOffRows + s * kPlaneRows;
-                const int64_t c0 = (int64_t)(t_begin + i) * kTile;
-                const int nbox = c0 + 64 < n ? 2 : 1;
-                mbar_arrive_expect_tx(&bars[kBarFull + s], (uint32_t)nbox * 2u * 8192u);
-                for (int hb = 0; hb < nbox; ++hb) {
-                    const int64_t c = c0 + hb * 64;
-                    const int64_t y = MODE == kFine ? k0 + (int64_t)blk[c >> 6] * 64 : k0 + c;
-#pragma unroll
-                    for (int ch = 0; ch < 2; ++ch)
-                        tma_load_2d(slot + ch * (kTile * 128) + hb * 8192, &P.keys_map, ch * 64, (int32_t)y,
-                                    &bars[kBarFull + s]);
-                }
+                issue_tile(i);
                 ++issued;
             }
             if (!ok) {   // let the copies already in flight land before the CTA can exit
@@ -309,21 +322,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
         // N = 64 * NQ: every q plane in one instruction; each rows plane is one MMA per
         // K step (the coarse stage's 3 x 3 plane pairs all accumulate, the smallest
         // ones below 2^-24 of the product included).
-        const uint32_t idesc = idesc_bf16_f32(128, 64 * NQ, 0, 0);
+        const uint32_t idesc = idesc_bf16_f32(64, 64 * NQ, 0, 0);
         const uint64_t qd = smem_desc_sw128(sbase + kOffQ, 16, 1024);
         ok = wait_bar_warp(&bars[kBarQ], 0, abort);
         for (int i = 0; i < T && ok; ++i) {
             const int s = MODE == kCoarse ? 0 : i % kSlots;
             const uint32_t ph = MODE == kCoarse ? (uint32_t)(i & 1) : (uint32_t)((i / kSlots) & 1);
-            const int db = i & 1;
             if (!wait_bar_warp(&bars[kBarFull + s], ph, abort) ||
-                (i >= 2 && !wait_bar_warp(&bars[kBarDFree + db], ((i >> 1) - 1) & 1, abort))) {
+                (i >= 1 && !wait_bar_warp(&bars[kBarDFree], (i - 1) & 1, abort))) {
                 ok = false;
                 break;
             }
             fence_after_sync();
             const uint64_t rd = smem_desc_sw128(sbase + kOffRows + s * kPlaneRows, 16, 1024);
-            const uint32_t d = tmem + db * (64 * NQ);
+            const uint32_t d = tmem;
 #pragma unroll
             for (int ks = 0; ks < kD / 16; ++ks) {
                 const uint32_t ko = ks >> 2, kb = (ks & 3) * 32;
@@ -334,20 +346,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
                                   (ks > 0 || ra > 0) ? 1u : 0u);
             }
             mma_commit_warp(&bars[kBarEmpty + s]);
-            mma_commit_warp(&bars[kBarDFull + db]);
+            mma_commit_warp(&bars[kBarDFull]);
         }
         mma_commit_warp(&bars[kBarDrain]);
         wait_bar_warp(&bars[kBarDrain], 0, abort);
     } else {
         // ---------------- epilogue: one row per thread ----------------
         const int quad = warp & 3;
-        const int r = quad * 32 + lane;
+        const int r = quad * 16 + lane;                 // valid for lane < 16 (M = 64 layout)
         ok = wait_bar(&bars[kBarQ], 0, abort);
         for (int i = 0; i < T && ok; ++i) {
-            const int db = i & 1;
-            if (!wait_bar(&bars[kBarDFull + db], (i >> 1) & 1, abort)) { ok = false; break; }
+            if (!wait_bar(&bars[kBarDFull], i & 1, abort)) { ok = false; break; }
             fence_after_sync();
-            const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + db * (64 * NQ);
+            const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16);
             float acc = 0.f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {           // 16 heads at a time: dot = sum over q planes
@@ -364,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_tc(const __grid_constant_
                 }
             }
             fence_before_sync();
-            mbar_arrive(&bars[kBarDFree + db]);
+            mbar_arrive(&bars[kBarDFree]);
             const int64_t cidx = (int64_t)(t_begin + i) * kTile + r;
-            if (cidx < n) {
+            if (lane < 16 && cidx < n) {
                 int64_t pos = cidx;
                 if (MODE == kCoarse) pos = cidx * p.b;   // a block is eligible iff its first row is visible
                 if (MODE == kFine) {
@@ -424,9 +435,12 @@ int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max,
 template <int MODE, bool QBF16>
 static cudaError_t launch_t(const ScoreTcParams &p, dim3 grid, cudaStream_t s) {
     static const cudaError_t attr = cudaFuncSetAttribute(
-        k_score_tc<MODE, QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        k_score_tc<MODE, QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)(kSmemFixed + kMaxSel * 4));
     if (attr != cudaSuccess) return attr;
-    k_score_tc<MODE, QBF16><<<grid, kThreads, kSmemBytes, s>>>(p);
+    // the fused select keeps n scores in shared memory; the flat mode keeps none
+    const size_t smem = kSmemFixed + (MODE == kFlat ? 0 : (size_t)p.s.n_max * 4);
+    k_score_tc<MODE, QBF16><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 

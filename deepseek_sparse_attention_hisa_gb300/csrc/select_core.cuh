@@ -1,24 +1,108 @@
 // Block-wide top-k of one row of f32 scores, as a set, by radix select over orderable
 // 32-bit keys ([HiSA issue] "Conventions": argpartition returns an unordered top-k set).
 //
-// Four 8-bit passes (most significant digit first) find the k-th largest key T and how
-// many elements equal to T are still needed; a final pass emits, in ascending column
-// order, every element above T plus the lowest-indexed elements equal to T. Equal
-// scores therefore fall to the lower column; -0.0 equals +0.0. All NT threads of the
-// CTA take part; `sc` may point to global or shared memory.
+// Scores of one row cluster in value, so their float bits share most high bits and a
+// digit of the raw bits would put nearly every score in one bin. Instead, pass 1 bins
+// the unmasked scores linearly in value over their [min, max] (256 bins; the binning is
+// non-decreasing, so a higher bin holds strictly larger scores and equal scores share a
+// bin; one shared atomic per distinct bin per warp), finds the bin of the k-th largest
+// score, compacts that bin's elements and resolves them exactly by one warp: up to 32 by
+// direct ranking, more by a radix select over their keys. When the k-th score is masked
+// or the range degenerates, a block-wide four-pass radix select over the keys is used.
+// The final pass emits, in ascending column order, every element above the k-th key T
+// plus the lowest-indexed elements equal to T: each warp owns a contiguous segment of
+// columns, so one block-wide prefix over warps fixes every output position. Equal
+// scores therefore fall to the lower column; -0.0 equals +0.0. `sc` may point to global
+// or shared memory.
 #pragma once
 
 #include "hisa_internal.cuh"
 
 namespace hisa {
 
+constexpr int kCand = 1024;
+
 template <int NT>
 struct SelectShared {
     uint32_t hist[256];
     uint32_t wg[NT / 32], we[NT / 32];
-    uint32_t prefix, kk, tg, te;
+    uint32_t prefix, kk, ncand;
     int nonfinite;
+    int32_t cand[kCand];
 };
+
+// One warp: find the digit (at `shift`) of the kk-th largest key among the keys counted
+// in hist; writes the extended prefix and the remaining rank to *prefix_out / *kk_out.
+__device__ __forceinline__ void warp_find_digit(const uint32_t *hist, uint32_t prefix,
+                                                uint32_t kk, int shift, uint32_t *prefix_out,
+                                                uint32_t *kk_out) {
+    const int lane = threadIdx.x & 31;
+    // lane l owns bins 255-8l .. 248-8l (descending); scan counts over lanes
+    uint32_t c[8], tot = 0u;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) { c[t] = hist[255 - 8 * lane - t]; tot += c[t]; }
+    uint32_t incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const uint32_t excl = incl - tot;
+    if (excl < kk && kk <= incl) {
+        uint32_t cum = excl;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (cum + c[t] >= kk) {
+                *prefix_out = prefix | ((255u - 8u * lane - t) << shift);
+                *kk_out = kk - cum;
+                break;
+            }
+            cum += c[t];
+        }
+    }
+}
+
+// hist[digit] += 1 for every lane of the warp with valid == true, one atomic per distinct
+// digit per warp (scores cluster, so many lanes share a bin).
+__device__ __forceinline__ void warp_hist_add(uint32_t *hist, bool valid, uint32_t digit) {
+    const uint32_t active = __ballot_sync(0xffffffffu, valid);
+    if (valid) {
+        const uint32_t peers = __match_any_sync(active, digit);
+        if ((threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[digit], __popc(peers));
+    }
+}
+
+__device__ __forceinline__ float key_to_float(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// Scores at or below this are selection masks (NEG = -1e30), kept out of the value range.
+constexpr float kMaskedBelow = -1e29f;
+
+// Block-wide radix select over the full keys: four 8-bit passes; resolves any input.
+// Leaves the k-th key in sh.prefix and the count of its equals to take in sh.kk.
+template <int NT>
+__device__ void block_radix_threshold(const float *sc, int64_t n, uint32_t kout,
+                                      SelectShared<NT> &sh) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t prefix = 0u, mask = 0u, kk = kout;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int e = tid; e < 256; e += NT) sh.hist[e] = 0u;
+        __syncthreads();
+        for (int64_t base = (int64_t)warp * 32; base < n; base += NT) {
+            const int64_t i = base + lane;
+            const uint32_t key = i < n ? order_key(sc[i]) : 0u;
+            warp_hist_add(sh.hist, i < n && (key & mask) == prefix, (key >> shift) & 255u);
+        }
+        __syncthreads();
+        if (warp == 0) warp_find_digit(sh.hist, prefix, kk, shift, &sh.prefix, &sh.kk);
+        __syncthreads();
+        prefix = sh.prefix;
+        kk = sh.kk;
+        mask |= 255u << shift;
+        __syncthreads();
+    }
+}
 
 // Writes the kout selected columns, mapped through map(i), to out[0..kout) in ascending
 // column order. Caller guarantees 0 <= kout <= n. Contains __syncthreads(): every thread
@@ -29,86 +113,163 @@ __device__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *ou
     constexpr int NW = NT / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (kout <= 0) return;
-    if (tid == 0) sh.nonfinite = 0;
-    uint32_t prefix = 0u, mask = 0u, kk = (uint32_t)kout;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int e = tid; e < 256; e += NT) sh.hist[e] = 0u;
-        __syncthreads();
-        for (int64_t i = tid; i < n; i += NT) {
-            const float v = sc[i];
-            if (shift == 24 && !isfinite(v)) sh.nonfinite = 1;
+
+    // ---- range of the unmasked finite scores (as keys: integer min / max) ----
+    uint32_t kmin = 0xffffffffu, kmax = 0u, nfree = 0u;
+    int nonfinite = 0;
+    for (int64_t i = tid; i < n; i += NT) {
+        const float v = sc[i];
+        const bool fin = isfinite(v);
+        nonfinite |= !fin;
+        if (fin && v > kMaskedBelow) {
             const uint32_t key = order_key(v);
-            if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
+            kmin = key < kmin ? key : kmin;
+            kmax = key > kmax ? key : kmax;
+            ++nfree;
+        }
+    }
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    nfree = __reduce_add_sync(0xffffffffu, nfree);
+    nonfinite = __reduce_or_sync(0xffffffffu, nonfinite);
+    if (lane == 0) { sh.wg[warp] = kmin; sh.we[warp] = kmax; sh.cand[warp] = (int32_t)nfree; }
+    if (tid == 0) { sh.nonfinite = 0; sh.ncand = 0u; }
+    for (int e = tid; e < 256; e += NT) sh.hist[e] = 0u;
+    __syncthreads();
+    if (lane == 0 && nonfinite) sh.nonfinite = 1;
+    kmin = 0xffffffffu;
+    kmax = 0u;
+    nfree = 0u;
+    for (int w = 0; w < NW; ++w) {
+        kmin = sh.wg[w] < kmin ? sh.wg[w] : kmin;
+        kmax = sh.we[w] > kmax ? sh.we[w] : kmax;
+        nfree += (uint32_t)sh.cand[w];
+    }
+    __syncthreads();
+    const float smin = key_to_float(kmin), smax = key_to_float(kmax);
+    const float scale = 255.0f / (smax - smin);
+    if (nfree < (uint64_t)kout || !(smax > smin) || !isfinite(scale)) {
+        // the k-th score is masked, or the unmasked scores are (nearly) all equal
+        block_radix_threshold<NT>(sc, n, (uint32_t)kout, sh);
+    } else {
+        // value bins: bin(s) is non-decreasing in s, so a higher bin holds strictly
+        // larger scores and equal scores share a bin
+        auto bin_of = [&](float v) -> uint32_t {
+            if (!(v >= smin)) return 0u;
+            if (!(v < smax)) return 255u;
+            const int b = (int)((v - smin) * scale);
+            return (uint32_t)(b < 0 ? 0 : (b > 254 ? 254 : b));
+        };
+        for (int64_t base = (int64_t)warp * 32; base < n; base += NT) {
+            const int64_t i = base + lane;
+            const float v = i < n ? sc[i] : 0.f;
+            warp_hist_add(sh.hist, i < n, bin_of(v));
         }
         __syncthreads();
-        if (warp == 0) {
-            // lane l owns bins 255-8l .. 248-8l (descending); scan counts over lanes
-            uint32_t c[8], tot = 0u;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) { c[t] = sh.hist[255 - 8 * lane - t]; tot += c[t]; }
-            uint32_t incl = tot;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
+        // the bin of the k-th largest score; sh.kk = its rank inside that bin
+        if (warp == 0) warp_find_digit(sh.hist, 0u, (uint32_t)kout, 0, &sh.prefix, &sh.kk);
+        __syncthreads();
+        const uint32_t dbin = sh.prefix;
+        uint32_t kk = sh.kk;
+        for (int64_t base = (int64_t)warp * 32; base < n; base += NT) {
+            const int64_t i = base + lane;
+            const bool c = i < n && bin_of(sc[i]) == dbin;
+            const uint32_t bal = __ballot_sync(0xffffffffu, c);
+            uint32_t at = 0u;
+            if (lane == 0 && bal) at = atomicAdd(&sh.ncand, (uint32_t)__popc(bal));
+            at = __shfl_sync(0xffffffffu, at, 0) + __popc(bal & ((1u << lane) - 1u));
+            if (c && at < (uint32_t)kCand) sh.cand[at] = (int32_t)i;
+        }
+        __syncthreads();
+        const uint32_t m = sh.ncand;
+        if (m <= 32u) {
+            if (warp == 0) {                   // few candidates: rank them directly
+                const bool have = (uint32_t)lane < m;
+                const int32_t idx = have ? sh.cand[lane] : 0x7fffffff;
+                const uint32_t key = have ? order_key(sc[idx]) : 0u;
+                uint32_t rank = 0u;            // candidates ahead in (key desc, column asc)
+                for (int j = 0; j < 32; ++j) {
+                    const uint32_t kj = __shfl_sync(0xffffffffu, key, j);
+                    const int32_t ij = __shfl_sync(0xffffffffu, idx, j);
+                    rank += ((uint32_t)j < m && (kj > key || (kj == key && ij < idx))) ? 1u : 0u;
+                }
+                if (have && rank == kk - 1u) sh.prefix = key;   // the last one selected
+                __syncwarp();
+                const uint32_t t = sh.prefix;
+                const uint32_t above = __popc(__ballot_sync(0xffffffffu, have && key > t));
+                if (lane == 0) sh.kk = kk - above;
             }
-            const uint32_t excl = incl - tot;
-            if (excl < kk && kk <= incl) {
-                uint32_t cum = excl;
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    if (cum + c[t] >= kk) {
-                        sh.prefix = prefix | ((255u - 8u * lane - t) << shift);
-                        sh.kk = kk - cum;
-                        break;
+        } else if (m <= (uint32_t)kCand) {
+            if (warp == 0) {                   // radix over the candidates' keys, one warp
+                uint32_t prefix = 0u, mask = 0u;
+                for (int sft = 24; sft >= 0; sft -= 8) {
+                    for (int e = lane; e < 256; e += 32) sh.hist[e] = 0u;
+                    __syncwarp();
+                    for (uint32_t c = lane; c < m; c += 32) {
+                        const uint32_t key = order_key(sc[sh.cand[c]]);
+                        if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> sft) & 255u], 1u);
                     }
-                    cum += c[t];
+                    __syncwarp();
+                    warp_find_digit(sh.hist, prefix, kk, sft, &sh.prefix, &sh.kk);
+                    __syncwarp();
+                    prefix = sh.prefix;
+                    kk = sh.kk;
+                    mask |= 255u << sft;
+                    __syncwarp();
                 }
             }
+        } else {
+            block_radix_threshold<NT>(sc, n, (uint32_t)kout, sh);
         }
-        __syncthreads();
-        prefix = sh.prefix;
-        kk = sh.kk;
-        mask |= 255u << shift;
-        __syncthreads();
     }
+    __syncthreads();
     if (tid == 0 && sh.nonfinite) flag(status, HISA_DEV_NONFINITE);
+    const uint32_t T = sh.prefix;
+    const uint32_t kk = sh.kk;
 
-    const uint32_t T = prefix;
+    // ---- emit: warp w owns columns [lo, hi) ----
     const uint32_t lt = (1u << lane) - 1u;
-    uint32_t base_g = 0u, base_e = 0u;
-    for (int64_t start = 0; start < n; start += NT) {
-        const int64_t i = start + tid;
-        uint32_t key = 0u;
-        const bool valid = i < n;
-        if (valid) key = order_key(sc[i]);
-        const bool g = valid && key > T;
-        const bool e = valid && key == T;
+    const int64_t seg = (n + NW - 1) / NW;
+    const int64_t lo = warp * seg, hi = lo + seg < n ? lo + seg : n;
+    uint32_t cg = 0u, ce = 0u;
+    for (int64_t start = lo; start < hi; start += 32) {
+        const int64_t i = start + lane;
+        const uint32_t key = i < hi ? order_key(sc[i]) : 0u;
+        cg += __popc(__ballot_sync(0xffffffffu, i < hi && key > T));
+        ce += __popc(__ballot_sync(0xffffffffu, i < hi && key == T));
+    }
+    if (lane == 0) { sh.wg[warp] = cg; sh.we[warp] = ce; }
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t vg = lane < NW ? sh.wg[lane] : 0u;
+        const uint32_t ve = lane < NW ? sh.we[lane] : 0u;
+        uint32_t ig = vg, ie = ve;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t a = __shfl_up_sync(0xffffffffu, ig, o);
+            const uint32_t b = __shfl_up_sync(0xffffffffu, ie, o);
+            if (lane >= o) { ig += a; ie += b; }
+        }
+        if (lane < NW) { sh.wg[lane] = ig - vg; sh.we[lane] = ie - ve; }
+    }
+    __syncthreads();
+    uint32_t base_g = sh.wg[warp], base_e = sh.we[warp];
+    for (int64_t start = lo; start < hi; start += 32) {
+        const int64_t i = start + lane;
+        const uint32_t key = i < hi ? order_key(sc[i]) : 0u;
+        const bool g = i < hi && key > T;
+        const bool e = i < hi && key == T;
         const uint32_t bg = __ballot_sync(0xffffffffu, g);
         const uint32_t be = __ballot_sync(0xffffffffu, e);
-        if (lane == 0) { sh.wg[warp] = __popc(bg); sh.we[warp] = __popc(be); }
-        __syncthreads();
-        if (warp == 0) {
-            const uint32_t vg = lane < NW ? sh.wg[lane] : 0u;
-            const uint32_t ve = lane < NW ? sh.we[lane] : 0u;
-            uint32_t ig = vg, ie = ve;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t a = __shfl_up_sync(0xffffffffu, ig, o);
-                const uint32_t b = __shfl_up_sync(0xffffffffu, ie, o);
-                if (lane >= o) { ig += a; ie += b; }
-            }
-            if (lane < NW) { sh.wg[lane] = ig - vg; sh.we[lane] = ie - ve; }
-            if (lane == 31) { sh.tg = ig; sh.te = ie; }
-        }
-        __syncthreads();
-        const uint32_t pg = base_g + sh.wg[warp] + __popc(bg & lt);
-        const uint32_t pe = base_e + sh.we[warp] + __popc(be & lt);
-        if (g || (e && pe < kk)) out[pg + (pe < kk ? pe : kk)] = map(i);
-        base_g += sh.tg;
-        base_e += sh.te;
-        __syncthreads();
+        const uint32_t pg = base_g + __popc(bg & lt);
+        const uint32_t pe = base_e + __popc(be & lt);
+        const uint32_t at = pg + (pe < kk ? pe : kk);
+        // at < kout for finite scores; the guard keeps non-finite input (flagged) in bounds
+        if ((g || (e && pe < kk)) && at < (uint64_t)kout) out[at] = map(i);
+        base_g += __popc(bg);
+        base_e += __popc(be);
     }
+    __syncthreads();
 }
 
 }  // namespace hisa
