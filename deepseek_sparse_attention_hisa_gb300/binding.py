@@ -19,6 +19,7 @@ HISA_OK, HISA_EINVAL, HISA_EDTYPE, HISA_EWORKSPACE, HISA_ECUDA, HISA_EDEVICE = 0
 HISA_F32, HISA_BF16 = 0, 1
 DEV_BAD_OFFSETS, DEV_GATE, DEV_BAD_ID, DEV_NONFINITE, DEV_BAD_BLOCK, DEV_TIMEOUT = \
     0x1, 0x2, 0x4, 0x8, 0x10, 0x20
+FLAT_NOALLOC_MAX_SCORES = 1 << 22
 OP_INDEX_SCORES, OP_BLOCK_MEANS, OP_BLOCK_FILTER, OP_SELECT_TOPK, OP_FLAT_TOPK, OP_SPARSE_ATTEND = \
     range(6)
 
@@ -58,6 +59,7 @@ _SIG = {
     "hisa_block_filter": (ctypes.c_int32, [_P] * 9 + [ctypes.c_int64, _P, ctypes.c_size_t, _P]),
     "hisa_select_topk": (ctypes.c_int32, [_P] * 10 + [ctypes.c_size_t, _P]),
     "hisa_flat_topk": (ctypes.c_int32, [_P] * 8 + [ctypes.c_size_t, _P]),
+    "hisa_flat_topk_noalloc": (ctypes.c_int32, [_P] * 9),
     "hisa_sparse_attend": (ctypes.c_int32, [_P] * 12 + [ctypes.c_size_t, _P]),
 }
 
@@ -174,6 +176,15 @@ def flat_topk(desc, q, w, keys, key_off, t0, I, ws, stream=None):
     _check(lib().hisa_flat_topk(ctypes.byref(desc), _ptr(q), _ptr(w), _ptr(keys), _ptr(key_off),
                                 _ptr(t0), _ptr(I), _ptr(ws), ws.numel(), _stream(stream)),
            "hisa_flat_topk")
+
+
+def flat_topk_noalloc(desc, q, w, keys, key_off, t0, I, dev_status=None, stream=None):
+    """hisa_flat_topk without a workspace: the library's own fixed device array holds the
+    scores (B * L * Np_max <= FLAT_NOALLOC_MAX_SCORES). dev_status: optional int32 device
+    tensor of one element that receives the call's HISA_DEV_* bits."""
+    _check(lib().hisa_flat_topk_noalloc(ctypes.byref(desc), _ptr(q), _ptr(w), _ptr(keys),
+                                        _ptr(key_off), _ptr(t0), _ptr(I), _ptr(dev_status),
+                                        _stream(stream)), "hisa_flat_topk_noalloc")
 
 
 def sparse_attend(desc, q, local_kv, local_len, local_pos0, pooled_kv, kv_off, I, sinks, t0, out,

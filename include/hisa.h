@@ -192,6 +192,30 @@ HISA_API hisa_status hisa_flat_topk(const hisa_index_desc *desc, const void *q, 
                            const void *keys, const int64_t *key_off, const int32_t *t0,
                            int32_t *I, void *ws, size_t ws_bytes, hisa_stream_t stream);
 
+/* Allocation-free flat selection. The paper has no counterpart: this entry point exists
+ * for callers that cannot allocate device memory (hosts whose runtime owns all device
+ * memory through its own pool, plugins that may not allocate outside the framework's
+ * allocator, loops where cudaMalloc / cudaFree would synchronise the device) and so
+ * cannot pass the workspace hisa_flat_topk needs. It computes exactly what
+ * hisa_flat_topk computes, with the same arguments and errors, but keeps the scores in
+ * a fixed array of device memory declared inside libhisa (16 MiB + 256 bytes), which
+ * every GPU that loads the library holds until the process exits. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   B * L * Np_max must not exceed HISA_FLAT_NOALLOC_MAX_SCORES, else HISA_EWORKSPACE
+ *   before anything is enqueued.
+ *   dev_status: optional (NULL) device pointer to one uint32 that receives this call's
+ *   HISA_DEV_* bits (the status is cleared at the start of every call).
+ * Runs on the current device. The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls on one device share the one array: calls that may overlap on the GPU (on
+ * different streams, or from several host threads without ordering) race and give
+ * undefined results; order them on one stream. */
+#define HISA_FLAT_NOALLOC_MAX_SCORES 4194304
+HISA_API hisa_status hisa_flat_topk_noalloc(const hisa_index_desc *desc, const void *q,
+                                   const float *w, const void *keys, const int64_t *key_off,
+                                   const int32_t *t0, int32_t *I, uint32_t *dev_status,
+                                   hisa_stream_t stream);
+
 /* Sparse combine ([HiSA issue] "Consuming the selection: sparse combine"): one softmax
  * over the visible local rows, the gathered pooled rows P = pooled_kv[I] and the
  * per-head sink, which joins the normaliser and carries no value; K = V.
