@@ -65,58 +65,136 @@ def stage_bytes(wl, nb):
 # clocks during the timed region
 # ----------------------------------------------------------------------------
 class ClockSampler:
+    """SM clock, power and clock-event reasons of one GPU, polled every ~1 ms through NVML
+    (read-only queries) while the timed region runs; nvidia-smi at 20 ms if NVML is not
+    loadable. Only samples taken between mark_start() and mark_stop() are summarised."""
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
+    def __init__(self, cuda_index: int):
+        self.cuda_index = cuda_index
+        self.samples = []          # (time, sm_mhz, reasons set)
+        self.sm_max = None
+        self.source = None
+        self.t0 = self.t1 = None
+        self._stop = threading.Event()
         self.proc = None
-        self.lines = []
+        self.thread = None
+
+    # -- device handle ---------------------------------------------------------
+    def _nvml_handle(self, nv):
+        import ctypes
+        h = ctypes.c_void_p()
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.cuda_index).uuid)
+            key = ("GPU-" + uuid if not uuid.startswith("GPU-") else uuid).encode()
+            if nv.nvmlDeviceGetHandleByUUID(key, ctypes.byref(h)) == 0:
+                return h
+        except Exception:
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        idx = self.cuda_index
+        if ids and self.cuda_index < len(ids):
+            if ids[self.cuda_index].isdigit():
+                idx = int(ids[self.cuda_index])
+            elif nv.nvmlDeviceGetHandleByUUID(ids[self.cuda_index].encode(),
+                                              ctypes.byref(h)) == 0:
+                return h
+        if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) == 0:
+            return h
+        return None
+
+    def _nvml_loop(self, nv, h):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    nv.nvmlDeviceGetCurrentClocksThrottleReasons(h, ctypes.byref(rs)) == 0:
+                names = {n for bit, n in self.REASONS.items() if rs.value & bit}
+                self.samples.append((t, float(clk.value), names))
+            time.sleep(0.001)
+
+    def _smi_loop(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.proc.stdout:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm, smax = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            self.sm_max = smax
+            rs = {n for n, v in zip(names, parts[4:8]) if v.lower().startswith("active")}
+            self.samples.append((time.perf_counter(), sm, rs))
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = self._nvml_handle(nv)
+            if h is None:
+                raise OSError("no NVML handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.sm_max = float(mx.value)
+            self.source = "nvml 1 ms"
+            self.thread = threading.Thread(target=self._nvml_loop, args=(nv, h), daemon=True)
             self.thread.start()
         except Exception:
-            self.proc = None
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.cuda_index), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi 20 ms"
+                self.thread = threading.Thread(target=self._smi_loop, daemon=True)
+                self.thread.start()
+                deadline = time.perf_counter() + 5.0   # wait for the first sample
+                while not self.samples and time.perf_counter() < deadline:
+                    time.sleep(0.01)
+            except Exception:
+                self.proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_stop(self):
+        self.t1 = time.perf_counter()
 
     def __exit__(self, *a):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        t0 = self.t0 if self.t0 is not None else -1e30
+        t1 = self.t1 if self.t1 is not None else 1e30
+        inside = [(sm, rs) for t, sm, rs in self.samples if t0 <= t <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.sm_max, "reasons": ["unsampled"],
+                    "samples": 0, "source": self.source}
+        reasons = set()
+        for _, rs in inside:
+            reasons |= rs
+        return {"sm_mhz": statistics.median(sm for sm, _ in inside), "sm_max_mhz": self.sm_max,
+                "reasons": sorted(reasons), "samples": len(inside), "source": self.source}
 
 
 # ----------------------------------------------------------------------------
@@ -297,6 +375,7 @@ def run_gpu(args, wl, R):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.mark_start()
         t_wall = time.perf_counter()
         with torch.cuda.stream(stream):
             for i in range(K):
@@ -304,6 +383,7 @@ def run_gpu(args, wl, R):
                 step(evs[i])
         stream.synchronize()
         t_wall = time.perf_counter() - t_wall
+        clk.mark_stop()
     torch.cuda.synchronize()
     step_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(K)]
     stage_ms = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]
@@ -345,8 +425,8 @@ def run_gpu(args, wl, R):
     stage_avg = {n: statistics.mean(v) for n, v in stage_ms.items()}
     dom = max(stage_avg, key=stage_avg.get)
     achieved = per_stage_bytes[dom] * R / (stage_avg[dom] / 1e3) / 1e9
-    kernel_of = {"block_means": "k_block_means", "block_filter": "k_scores_simt",
-                 "select_topk": "k_scores_simt", "sparse_attend": "k_attend_simt"}
+    kernel_of = {"block_means": "k_block_means", "block_filter": "k_score_tc (coarse)",
+                 "select_topk": "k_score_tc (fine)", "sparse_attend": "k_attend_tc"}
     traffic = traffic_from_profile(kernel_of[dom])
 
     line = {
@@ -385,17 +465,19 @@ def run_gpu(args, wl, R):
 
 
 def launches_per_step(prob):
-    """Kernels this library launches per step: means 1, filter 2, select 2, attend 1 or 2."""
+    """Kernels this library launches per step for the V4 decode shape: block means 1, the
+    coarse filter 1 and the fine top-k 1 (each scores and selects in one tcgen05 kernel),
+    the combine 1, plus the split-K merge when the combine is split."""
     from deepseek_sparse_attention_hisa_gb300 import binding as hb
     ws_need = hb.workspace_bytes(hb.OP_SPARSE_ATTEND, prob.adesc)
     attend = 2 if ws_need > 256 else 1
-    return 1 + 2 + 2 + attend
+    return 1 + 1 + 1 + attend
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--R", type=int, default=304,
