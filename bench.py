@@ -306,6 +306,22 @@ def traffic_from_profile(kernel):
         return None
 
 
+def max_over_ranks(ms, device):
+    """The slowest rank's time (every rank gets it); the value itself at world size 1."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, R, K, total_ms):
+    """Whole-job queries/s: every rank runs R independent queries per step (weak scaling)."""
+    return world * R * K / (total_ms / 1e3)
+
+
 def run_gpu(args, wl, R):
     import torch
     import torch.distributed as dist
@@ -388,13 +404,9 @@ def run_gpu(args, wl, R):
     step_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(K)]
     stage_ms = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]
                 for j, name in enumerate(stages)}
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / K
-    value = world * R * K / (total_ms / 1e3)
+    value = job_value(world, R, K, total_ms)
 
     # e2e: the same step through the public API from pinned host buffers, with the
     # per-step query inputs copied in and the results (out, I) copied back.
@@ -417,7 +429,7 @@ def run_gpu(args, wl, R):
             host_out["I"].copy_(prob.I, non_blocking=True)
             e2e_ev[i][1].record(stream)
     stream.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / K
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / K, dev)
     assert prob.status(stream) == 0, "device status flags set during the timed region"
 
     per_stage_bytes, step_bytes = stage_bytes(wl, nb)
@@ -445,7 +457,7 @@ def run_gpu(args, wl, R):
                      "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic},
         "gpu_launches": K * launches_per_step(prob),
-        "e2e": {"value": world * R / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_value(world, R, 1, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "wall_s": t_wall,
     }
