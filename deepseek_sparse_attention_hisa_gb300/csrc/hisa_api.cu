@@ -121,11 +121,22 @@ ScoreParams score_params(const hisa_index_desc *d, int mode, const void *q, cons
     return p;
 }
 
-// Runs one scoring pass: the tcgen05 kernel for the V4 indexer shape, else CUDA cores.
-// With `sel` the tensor-core coarse / fine kernels also select (returns true in *fused).
+// Runs one scoring pass: for the V4 indexer shape the persistent tcgen05 pipeline (coarse
+// and fine, which also select) or the per-query tcgen05 kernel, else CUDA cores. With
+// `sel` the tensor-core coarse / fine kernels also select (returns true in *fused).
 cudaError_t run_scores(const ScoreParams &p, int32_t *sel, int k_sel, bool *fused,
                        cudaStream_t s) {
     *fused = false;
+    if (sel && p.mode != kFlat &&
+        score_pipe_supported(p.mode, p.H_i, p.D_i, p.rows_bf16, p.n_max, p.b, p.keep) &&
+        (p.mode == kCoarse || p.keys_rows > 0)) {
+        ScoreTcParams t{};
+        t.s = p;
+        t.sel = sel;
+        t.k_sel = k_sel;
+        *fused = true;
+        return launch_score_pipe(t, s);
+    }
     if (score_tc_supported(p.mode, p.H_i, p.D_i, p.rows_bf16, p.n_max, p.b) &&
         (p.mode == kCoarse || p.keys_rows > 0)) {
         ScoreTcParams t{};

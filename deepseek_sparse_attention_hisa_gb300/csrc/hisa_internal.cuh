@@ -154,5 +154,8 @@ int attend_tc_supported(int H, int Dh, int kv_bf16);
 int attend_chunk_rows();
 cudaError_t launch_score_tc(const ScoreTcParams &p, cudaStream_t s);
 int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b);
+// Persistent coarse / fine scoring + select pipeline (one CTA per SM over all query rows).
+cudaError_t launch_score_pipe(const ScoreTcParams &p, cudaStream_t s);
+int score_pipe_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b, int keep);
 
 }  // namespace hisa

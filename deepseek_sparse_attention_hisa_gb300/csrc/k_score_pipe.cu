@@ -1,0 +1,651 @@
+// Coarse and fine indexer stages of the DeepSeek-V4 indexer shape (H_i = 64, D_i = 128) as
+// one persistent, warp-specialised tcgen05 pipeline per SM: score, then select, for a
+// stream of query rows ([HiSA issue] "HiSA decode path" and "HiSA batched path": the
+// coarse stage scores the block means and keeps the top Kb blocks, the fine stage scores
+// the rows of the kept blocks and keeps the top k).
+//
+//   score[c] = sum_h relu(q_h . row_c) * w_h * H_i^-1/2 * D_i^-1/2, NEG past visibility.
+//
+// One CTA per SM walks the query rows blockIdx.x, blockIdx.x + gridDim.x, ... Its warps
+// form a pipeline, so that one query's set-up and top-k overlap the next query's
+// streaming and only the first set-up and the last top-k are exposed:
+//   warp 0      MMA issue (one elected lane) and TMEM owner
+//   warp 1      fine: TMA producer of the kept blocks' bf16 key tiles
+//   warps 2-5   epilogue: TMEM -> relu, head weights, head sum -> scores in shared memory
+//   warps 6-9   builders: per-query checks, kept blocks, head weights, q planes
+//   warps 10-13 select: block top-k over the finished query's scores (named barrier 1)
+//   warps 14-17 coarse: converters, f32 block means -> three bf16 planes
+//
+// A tile is 128 scored rows, D[128 rows x 64 * planes] = rows . q^T (M = 128, K = 128) in
+// one of two TMEM accumulators. Scoring is f32 on the page; f32 operands are split
+// exactly into bf16 planes x = x1 + x2 + x3 (each the bf16 rounding of the remainder), so
+// every bf16 product is exact in the f32 accumulator. The q planes are stacked along N.
+// bf16 keys take one MMA per K step over all q planes. f32 block means take six of the
+// nine plane products (x1 y1, x1 y2, x1 y3, x2 y1, x2 y2, x3 y1): since |x2| <= 2^-8 |x|
+// and |x3| <= 2^-16 |x|, the three left out (x2 y3, x3 y2, x3 y3) add up to at most about
+// 2^-23 of |x y|, the size of one f32 rounding of the product.
+// Every wait is bounded; a timeout raises HISA_DEV_TIMEOUT, and the CTA drains and exits.
+#include "select_core.cuh"
+#include "tc_ptx.cuh"
+
+namespace hisa {
+namespace {
+
+using namespace tc;
+
+constexpr int kH = 64, kD = 128, kM = 128;
+constexpr int kWarpMma = 0, kWarpTma = 1, kWarpEpi = 2, kWarpBld = 6, kWarpSel = 10, kWarpCvt = 14;
+constexpr int kGroup = 128;                               // threads of each 4-warp role
+constexpr int kBarSel = 1, kBarBld = 2;                   // named barriers (0 = __syncthreads)
+
+template <int MODE>
+constexpr int pipe_threads() { return MODE == kCoarse ? 18 * 32 : 14 * 32; }
+
+// ---- shared memory (offsets from the 1024-aligned base) ----
+constexpr uint32_t kQPlane = kH * kD * 2;                 // [64 heads x 128 dims] bf16, 16 KiB
+constexpr uint32_t kOffQ = 0;                             // up to 3 planes, stacked along N
+constexpr uint32_t kOffReg = 3 * kQPlane;                 // streaming region
+constexpr int kFineSlots = 4;
+constexpr uint32_t kTileBytes = kM * kD * 2;              // fine: one [128 x 128] bf16 key tile
+constexpr uint32_t kRawBytes = kM * 64 * 4;               // coarse: f32 means, 128 rows x 64 dims
+constexpr uint32_t kHalfPlane = kM * 128;                 // [128 rows x 64 dims] bf16, 16 KiB
+constexpr uint32_t kPlaneSet = 3 * kHalfPlane;            // its three planes
+template <int MODE>
+constexpr uint32_t region_bytes() {
+    return MODE == kCoarse ? 2 * kRawBytes + 2 * kPlaneSet : kFineSlots * kTileBytes;
+}
+
+struct QMeta {            // one query row, double-buffered
+    int row;              // b * L + j
+    int state;            // 0: score it; else its selection is all -1
+    int n;                // scored rows: blocks (coarse) or candidates (fine)
+    int T;                // tiles of kM rows
+    long long base;       // first pooled row (fine) / first block-mean row (coarse)
+    long long V;          // visible pooled rows of this query row
+    int blk[64];          // kept blocks, ascending (fine)
+    float w[kH];          // w_h * H_i^-1/2 * D_i^-1/2
+};
+
+// barriers
+constexpr int kBarMetaFull = 0, kBarSlotFree = 2, kBarQFull = 4, kBarQEmpty = 5,
+              kBarAccFull = 6, kBarAccEmpty = 8, kBarScFull = 10, kBarDrain = 12,
+              kBarFull = 13,                                // fine: kFineSlots; coarse: 2 planes
+              kBarEmpty = kBarFull + kFineSlots, kNumBars = kBarEmpty + kFineSlots;
+
+template <int MODE>
+struct Layout {
+    static constexpr uint32_t meta = kOffReg + region_bytes<MODE>();
+    static constexpr uint32_t bars = meta + 2 * sizeof(QMeta);
+    static constexpr uint32_t misc = bars + kNumBars * 8;
+    static constexpr uint32_t sc = (misc + 64 + 15) & ~15u;   // 2 x n_cap floats
+    static constexpr uint32_t fixed = sc + 1024;                // + alignment slack
+};
+
+// Largest scored-row count one query may have: shared memory holds two score rows.
+constexpr int kPipeMaxCoarse = 1024;
+constexpr int kPipeMaxFine = 64 * 64;
+static_assert(kPipeMaxFine <= kSmallMax && kPipeMaxCoarse <= kSmallMax, "select capacity");
+
+struct Misc {
+    uint32_t tmem;
+    int abort;
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    for (uint32_t i = 0; i < (1u << 22); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && *abort) return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort));
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Exact three-way split of 8 f32 values into bf16 planes, packed as 3 x uint4.
+__device__ __forceinline__ void split3(const float (&x)[8], uint4 (&pl)[3]) {
+    uint32_t w[3][4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        float r0 = x[e], r1 = x[e + 1];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(r0, r1);
+            w[k][e / 2] = *reinterpret_cast<const uint32_t *>(&b);
+            if (k < 2) {
+                const float2 f = __bfloat1622float2(b);
+                r0 -= f.x;
+                r1 -= f.y;
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k) pl[k] = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+}
+
+// Byte offset of 16-byte unit u (dims 8u..8u+7) of head h of q plane `plane` when nq
+// planes are stacked along N: per 64-dim chunk, plane 0's 64 heads, then plane 1's, ...
+__device__ __forceinline__ uint32_t q_off(uint32_t plane, uint32_t h, uint32_t u, uint32_t nq) {
+    return (u >> 3) * (nq * kH * 128u) + plane * (kH * 128u) + sw128_offset(h, (u & 7u) * 8u);
+}
+
+}  // namespace
+}  // namespace hisa
+
+namespace hisa {
+namespace {
+
+// True on every participating thread iff v is true on all of them (named barrier id).
+__device__ __forceinline__ bool group_all(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
+        : "memory");
+    return r != 0u;
+}
+
+// Registers: 14 or 18 warps spread over the SM's four 16K-register sub-partitions,
+// so at most 128 (fine) or 96 (coarse) registers per thread.
+template <int MODE, bool QBF16>
+__global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
+    k_score_pipe(const __grid_constant__ ScoreTcParams P) {
+    constexpr int NQ = QBF16 ? 1 : 3;                       // q planes
+    using Lay = Layout<MODE>;
+    const ScoreParams &p = P.s;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ SelectShared<kGroup> sel_sh;
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::bars);
+    QMeta *meta = reinterpret_cast<QMeta *>(smem + Lay::meta);
+    Misc *misc = reinterpret_cast<Misc *>(smem + Lay::misc);
+    volatile int *abort = &misc->abort;
+    float *scb = reinterpret_cast<float *>(smem + Lay::sc);
+    const int n_cap = (int)p.n_max;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rows = p.B * p.L;
+    const int nql = (int)blockIdx.x < rows ? (rows - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+
+    if (tid == 0) {
+        for (int b = 0; b < kNumBars; ++b) {
+            uint32_t cnt = 1;
+            if (b == kBarQFull || b == kBarAccEmpty || b == kBarAccEmpty + 1 || b == kBarScFull ||
+                b == kBarScFull + 1)
+                cnt = kGroup;
+            if (MODE == kCoarse && (b == kBarFull || b == kBarFull + 1)) cnt = kGroup;
+            mbar_init(&bars[b], cnt);
+        }
+        mbar_fence_init();
+        misc->abort = 0;
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(&misc->tmem, 512);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = misc->tmem;
+    bool ok = true;
+    auto fail = [&]() {
+        ok = false;
+        *abort = 1;
+    };
+
+    if (warp >= kWarpBld && warp < kWarpBld + 4) {
+        // ---------------- builders: checks, kept blocks, weights, q planes ----------------
+        const int bt = tid - kWarpBld * 32;
+        constexpr int kQU = kH * 16 / kGroup;                 // 16-byte q units per thread
+        for (int i = 0; i < nql; ++i) {
+            const int qb = i & 1;
+            const int row = (int)blockIdx.x + i * (int)gridDim.x;
+            const int bq = row / p.L, j = row - bq * p.L;
+            // this row's q, weights and kept blocks first: the loads overlap the waits
+            float4 qf[QBF16 ? 1 : 2 * kQU];
+            uint4 qh[QBF16 ? kQU : 1];
+            if (QBF16) {
+                const uint4 *q16 = reinterpret_cast<const uint4 *>(
+                    reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)row * kH * kD);
+#pragma unroll
+                for (int m = 0; m < kQU; ++m) qh[m] = __ldg(q16 + bt + m * kGroup);
+            } else {
+                const float4 *q4 = reinterpret_cast<const float4 *>(
+                    reinterpret_cast<const float *>(p.q) + (int64_t)row * kH * kD);
+#pragma unroll
+                for (int m = 0; m < kQU; ++m) {
+                    qf[2 * m] = __ldg(q4 + 2 * (bt + m * kGroup));
+                    qf[2 * m + 1] = __ldg(q4 + 2 * (bt + m * kGroup) + 1);
+                }
+            }
+            const float wv = bt < kH ? __ldg(p.w + (int64_t)row * kH + bt) : 0.f;
+            int bv = 0;
+            if (MODE == kFine && bt < p.keep) bv = __ldg(p.top_blk + (int64_t)row * p.keep + bt);
+            // meta slot qb is free once query i - 2 is selected
+            const bool w1 = i < 2 || wait_bar(&bars[kBarSlotFree + qb], ((i >> 1) - 1) & 1, abort);
+            if (!group_all(kBarBld, kGroup, w1)) { fail(); break; }
+            QMeta &M = meta[qb];
+            if (MODE == kFine && bt < p.keep) M.blk[bt] = bv;
+            if (bt < kH) M.w[bt] = wv * p.head_scale;
+            named_sync(kBarBld, kGroup);
+            bool w2 = true;
+            if (bt == 0) {
+                int st = 0;
+                const int64_t k0 = p.key_off[bq];
+                const int64_t Np = p.key_off[bq + 1] - k0;
+                int64_t n = 0, base = k0;
+                if (!seq_ok(p.key_off, bq, p.Np_max, p.keys_rows)) {
+                    st = 1;
+                    flag(p.status, HISA_DEV_BAD_OFFSETS);
+                } else if (Np < (int64_t)p.b * p.keep) {
+                    st = 1;
+                    flag(p.status, HISA_DEV_GATE);
+                } else if (MODE == kCoarse) {
+                    n = Np / p.b;
+                    base = p.means_off[bq];
+                    if (p.means_off[bq + 1] - base < n || n > n_cap) {
+                        st = 1;
+                        flag(p.status, HISA_DEV_BAD_OFFSETS);
+                    }
+                } else {
+                    n = (int64_t)p.keep * 64;
+                    for (int s = 1; s < p.keep; ++s) {   // insertion sort: ascending pos
+                        const int v = M.blk[s];
+                        int u = s;
+                        while (u > 0 && M.blk[u - 1] > v) { M.blk[u] = M.blk[u - 1]; --u; }
+                        M.blk[u] = v;
+                    }
+                    for (int s = 0; s < p.keep; ++s)
+                        if (M.blk[s] < 0 || (int64_t)M.blk[s] >= Np / 64) st = 1;
+                    if (st) flag(p.status, HISA_DEV_BAD_BLOCK);
+                }
+                M.row = row;
+                M.state = st;
+                M.n = (int)n;
+                M.T = (int)((n + kM - 1) / kM);
+                M.base = base;
+                M.V = p.causal ? visible_len((int64_t)p.t0[bq] + j, p.r, Np) : Np;
+                mbar_arrive(&bars[kBarMetaFull + qb]);
+                // the q planes are free once the previous query's MMAs are done
+                w2 = i < 1 || wait_bar(&bars[kBarQEmpty], (i - 1) & 1, abort);
+            }
+            if (!group_all(kBarBld, kGroup, w2)) { fail(); break; }
+            if (QBF16) {
+#pragma unroll
+                for (int m = 0; m < kQU; ++m) {
+                    const int u = bt + m * kGroup;
+                    *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(0, u >> 4, u & 15, NQ)) = qh[m];
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < kQU; ++m) {
+                    const int u = bt + m * kGroup;
+                    const float x[8] = {qf[2 * m].x,     qf[2 * m].y,     qf[2 * m].z,     qf[2 * m].w,
+                                        qf[2 * m + 1].x, qf[2 * m + 1].y, qf[2 * m + 1].z, qf[2 * m + 1].w};
+                    uint4 pl[3];
+                    split3(x, pl);
+#pragma unroll
+                    for (int k = 0; k < 3; ++k)
+                        *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(k, u >> 4, u & 15, NQ)) = pl[k];
+                }
+            }
+            fence_async_smem();
+            mbar_arrive(&bars[kBarQFull]);
+        }
+    }
+    else if (MODE == kFine && warp == kWarpTma) {
+        // ---------------- TMA producer: kept blocks, two per 128-row tile ----------------
+        if (lane == 0) {
+            uint32_t g = 0;                                    // tiles issued
+            for (int i = 0; i < nql && ok; ++i) {
+                const int qb = i & 1;
+                if (!wait_bar(&bars[kBarMetaFull + qb], (i >> 1) & 1, abort)) { fail(); break; }
+                const QMeta &M = meta[qb];
+                if (M.state) continue;
+                for (int t = 0; t < M.T; ++t, ++g) {
+                    const uint32_t s = g % kFineSlots, use = g / kFineSlots;
+                    if (use >= 1 && !wait_bar(&bars[kBarEmpty + s], (use - 1) & 1, abort)) {
+                        fail();
+                        break;
+                    }
+                    const int nblk = p.keep - 2 * t < 2 ? p.keep - 2 * t : 2;
+                    const uint32_t slot = sbase + kOffReg + s * kTileBytes;
+                    mbar_arrive_expect_tx(&bars[kBarFull + s], (uint32_t)nblk * 16384u);
+                    for (int hb = 0; hb < nblk; ++hb) {
+                        const int32_t y = (int32_t)(M.base + (int64_t)M.blk[2 * t + hb] * 64);
+#pragma unroll
+                        for (int ch = 0; ch < 2; ++ch)
+                            tma_load_2d(slot + ch * (kM * 128) + hb * (64 * 128), &P.keys_map, ch * 64, y,
+                                        &bars[kBarFull + s]);
+                    }
+                }
+            }
+            if (!ok)   // let the copies in flight land before the CTA can exit
+                for (uint32_t h = g > kFineSlots ? g - kFineSlots : 0; h < g; ++h)
+                    mbar_wait(&bars[kBarFull + h % kFineSlots], (h / kFineSlots) & 1, 1u << 20);
+        }
+    } else if (warp == kWarpMma) {
+        // ---------------- MMA issue (warp-uniform loop, one elected lane issues) ----------
+        const uint32_t id_all = idesc_bf16_f32(kM, 64 * NQ, 0, 0);
+        const uint32_t id_two = idesc_bf16_f32(kM, 64 * (NQ > 1 ? NQ - 1 : 1), 0, 0);
+        const uint32_t id_one = idesc_bf16_f32(kM, 64, 0, 0);
+        const uint64_t qd = smem_desc_sw128(sbase + kOffQ, 16, 1024);
+        uint32_t g = 0, gs = 0, u = 0;                       // tiles, fine slots, coarse halves
+        for (int i = 0; i < nql && ok; ++i) {
+            const int qb = i & 1;
+            if (!wait_bar_warp(&bars[kBarMetaFull + qb], (i >> 1) & 1, abort) ||
+                !wait_bar_warp(&bars[kBarQFull], i & 1, abort)) {
+                fail();
+                break;
+            }
+            fence_after_sync();
+            const QMeta &M = meta[qb];
+            const int T = M.state ? 0 : M.T;
+            for (int t = 0; t < T; ++t, ++g) {
+                const uint32_t ab = g & 1;
+                if (g >= 2 && !wait_bar_warp(&bars[kBarAccEmpty + ab], ((g >> 1) - 1) & 1, abort)) {
+                    fail();
+                    break;
+                }
+                fence_after_sync();
+                const uint32_t d = tmem + ab * 256;
+                if (MODE == kFine) {
+                    const uint32_t s = gs % kFineSlots;
+                    if (!wait_bar_warp(&bars[kBarFull + s], (gs / kFineSlots) & 1, abort)) {
+                        fail();
+                        break;
+                    }
+                    fence_after_sync();
+                    const uint64_t rd = smem_desc_sw128(sbase + kOffReg + s * kTileBytes, 16, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < kD / 16; ++ks) {
+                        const uint32_t ko = ks >> 2, kb = (ks & 3) * 32;
+                        mma_bf16_warp(d, desc_add(rd, ko * (kM * 128) + kb),
+                                      desc_add(qd, ko * (NQ * kH * 128) + kb), id_all, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit_warp(&bars[kBarEmpty + s]);
+                    ++gs;
+                } else {
+                    bool good = true;
+                    for (int h = 0; h < 2; ++h, ++u) {
+                        const uint32_t pb = u & 1;
+                        if (!wait_bar_warp(&bars[kBarFull + pb], (u >> 1) & 1, abort)) { good = false; break; }
+                        fence_after_sync();
+                        const uint64_t pd =
+                            smem_desc_sw128(sbase + kOffReg + 2 * kRawBytes + pb * kPlaneSet, 16, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t kb = kk * 32;
+                            const uint64_t bq = desc_add(qd, h * (NQ * kH * 128) + kb);
+                            // rows plane ra against q planes 0 .. NQ-1-ra (all of them for bf16 q)
+                            mma_bf16_warp(d, desc_add(pd, kb), bq, id_all, (h | kk) ? 1u : 0u);
+                            mma_bf16_warp(d, desc_add(pd, kHalfPlane + kb), bq, id_two, 1u);
+                            mma_bf16_warp(d, desc_add(pd, 2 * kHalfPlane + kb), bq, id_one, 1u);
+                        }
+                        mma_commit_warp(&bars[kBarEmpty + pb]);
+                    }
+                    if (!good) { fail(); break; }
+                }
+                mma_commit_warp(&bars[kBarAccFull + ab]);
+            }
+            if (!ok) break;
+            mma_commit_warp(&bars[kBarQEmpty]);
+        }
+        mma_commit_warp(&bars[kBarDrain]);
+        mbar_wait(&bars[kBarDrain], 0, 1u << 24);
+    } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
+        // ---------------- epilogue: TMEM lane = tile row ----------------
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        uint32_t g = 0;
+        for (int i = 0; i < nql && ok; ++i) {
+            const int qb = i & 1;
+            const int row = (int)blockIdx.x + i * (int)gridDim.x;
+            if (!wait_bar(&bars[kBarMetaFull + qb], (i >> 1) & 1, abort) ||
+                (i >= 2 && !wait_bar(&bars[kBarSlotFree + qb], ((i >> 1) - 1) & 1, abort))) {
+                fail();
+                break;
+            }
+            const QMeta &M = meta[qb];
+            float *sc = scb + qb * n_cap;
+            const int T = M.state ? 0 : M.T;
+            for (int t = 0; t < T; ++t, ++g) {
+                const uint32_t ab = g & 1;
+                if (!wait_bar(&bars[kBarAccFull + ab], (g >> 1) & 1, abort)) { fail(); break; }
+                fence_after_sync();
+                const uint32_t ta = tmem + ab * 256 + ((uint32_t)(quad * 32) << 16);
+                float acc = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {               // 16 heads at a time
+                    float v[NQ][16];
+#pragma unroll
+                    for (int qa = 0; qa < NQ; ++qa) tmem_ld16(ta + qa * 64 + c * 16, v[qa]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < 16; ++h) {
+                        float dot = v[0][h];
+#pragma unroll
+                        for (int qa = 1; qa < NQ; ++qa) dot += v[qa][h];
+                        acc = fmaf(M.w[c * 16 + h], fmaxf(dot, 0.f), acc);
+                    }
+                }
+                fence_before_sync();
+                mbar_arrive(&bars[kBarAccEmpty + ab]);
+                const int cidx = t * kM + r;
+                if (cidx < M.n) {
+                    // coarse: a block is eligible iff its first row is visible
+                    const int64_t pos = MODE == kCoarse ? (int64_t)cidx * p.b
+                                                        : (int64_t)M.blk[cidx >> 6] * 64 + (cidx & 63);
+                    const float score = pos < M.V ? acc : kNeg;
+                    sc[cidx] = score;
+                    if (p.out) p.out[(int64_t)row * p.ld_out + cidx] = score;
+                }
+            }
+            if (!ok) break;
+            mbar_arrive(&bars[kBarScFull + qb]);
+        }
+    } else if (warp >= kWarpSel && warp < kWarpSel + 4) {
+        // ---------------- select: top-k of a finished query, beside the next one's stream ----
+        const int st = tid - kWarpSel * 32;
+        for (int i = 0; i < nql; ++i) {
+            const int qb = i & 1;
+            const int row = (int)blockIdx.x + i * (int)gridDim.x;
+            const bool w = wait_bar(&bars[kBarScFull + qb], (i >> 1) & 1, abort);
+            if (!group_all(kBarSel, kGroup, w)) { fail(); break; }
+            const QMeta &M = meta[qb];
+            const float *sc = scb + qb * n_cap;
+            int32_t *out = P.sel + (int64_t)row * P.k_sel;
+            const int64_t kout = M.state ? 0 : (M.n < P.k_sel ? M.n : P.k_sel);
+            if (kout > 0) {
+                if (MODE == kFine) {
+                    const int *blk = M.blk;
+                    small_topk<kGroup, kBarSel, kWarpSel * 32>(
+                        sc, M.n, (int)kout, out,
+                        [blk](int64_t c) { return (int32_t)(blk[(int)c >> 6] * 64 + ((int)c & 63)); },
+                        sel_sh, p.status);
+                } else {
+                    small_topk<kGroup, kBarSel, kWarpSel * 32>(
+                        sc, M.n, (int)kout, out, [](int64_t c) { return (int32_t)c; }, sel_sh, p.status);
+                }
+            }
+            for (int64_t e = kout + st; e < P.k_sel; e += kGroup) out[e] = -1;
+            named_sync(kBarSel, kGroup);
+            if (st == 0) mbar_arrive(&bars[kBarSlotFree + qb]);
+        }
+    }
+    else if (MODE == kCoarse && warp >= kWarpCvt && warp < kWarpCvt + 4) {
+        // ---------------- converters: f32 means -> three bf16 planes ----------------------
+        // Unit = one K half (64 dims) of one 128-row tile. Each thread copies its own
+        // 8 x 32 bytes of a unit with cp.async into a private, conflict-free spot of one of
+        // two raw buffers (two units in flight), then splits them into the plane set the
+        // MMA reads. Thread ct owns pairs p = m * 128 + ct: row p / 8, dims (p % 8) * 8.
+        const int ct = tid - kWarpCvt * 32;
+        const float *means = reinterpret_cast<const float *>(p.rows);
+        int ui = 0, ut = 0, uh = 0, uT = -2;               // next unit to hand out
+        // Next unit in MMA order (valid queries, tiles, halves): 1 = got one, 0 = none,
+        // 2 = its query's meta is not written yet (only when may_wait is false), -1 = timeout.
+        // A thread may block on a later query's meta only once every unit it has copied is
+        // converted: that meta waits for the select of an earlier query, which waits for
+        // those units.
+        auto next_unit = [&](int &oi, int &ot, int &oh, bool may_wait) -> int {
+            while (ui < nql) {
+                if (uT == -2) {
+                    uint64_t *mb = &bars[kBarMetaFull + (ui & 1)];
+                    const uint32_t ph = (ui >> 1) & 1;
+                    if (!may_wait) {
+                        if (!mbar_try_wait(mb, ph)) return 2;
+                    } else if (!wait_bar(mb, ph, abort)) {
+                        return -1;
+                    }
+                    const QMeta &M = meta[ui & 1];
+                    uT = M.state ? 0 : M.T;
+                    ut = 0;
+                    uh = 0;
+                }
+                if (ut < uT) {
+                    oi = ui; ot = ut; oh = uh;
+                    if (++uh == 2) { uh = 0; ++ut; }
+                    return 1;
+                }
+                ++ui;
+                uT = -2;
+            }
+            return 0;
+        };
+        auto issue = [&](int i, int t, int h, uint32_t buf) {
+            const QMeta &M = meta[i & 1];
+            const uint32_t dst0 = sbase + kOffReg + buf * kRawBytes;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int pp = m * kGroup + ct, r = pp >> 3, g8 = pp & 7;
+                const int c = t * kM + r;
+                const bool valid = c < M.n;
+                const float *src = means + (M.base + (valid ? c : 0)) * kD + h * 64 + g8 * 8;
+                cp_async16_zfill(dst0 + ((2 * m) * kGroup + ct) * 16u, src, valid);
+                cp_async16_zfill(dst0 + ((2 * m + 1) * kGroup + ct) * 16u, src + 4, valid);
+            }
+            cp_async_commit();
+        };
+        // unit u lives in raw buffer u & 1; have0 = unit u (copied), have1 = unit u + 1
+        // (1 copied, 0 none, 2 not known yet)
+        int i0 = 0, t0 = 0, h0 = 0, i1 = 0, t1 = 0, h1 = 0;
+        int have0 = next_unit(i0, t0, h0, true), have1 = 0;
+        if (have0 < 0) fail();
+        if (have0 == 1) {
+            issue(i0, t0, h0, 0);
+            have1 = next_unit(i1, t1, h1, false);
+            if (have1 == 1) issue(i1, t1, h1, 1);
+        }
+        for (uint32_t u = 0; have0 == 1 && ok; ++u) {
+            if (have1 == 1) cp_async_wait_group<1>(); else cp_async_wait_group<0>();
+            const uint32_t pb = u & 1;
+            if (u >= 2 && !wait_bar(&bars[kBarEmpty + pb], ((u >> 1) - 1) & 1, abort)) { fail(); break; }
+            const uint8_t *rawb = smem + kOffReg + (u & 1) * kRawBytes;
+            uint8_t *planes = smem + kOffReg + 2 * kRawBytes + pb * kPlaneSet;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int pp = m * kGroup + ct, r = pp >> 3, g8 = pp & 7;
+                const float4 a = *reinterpret_cast<const float4 *>(rawb + ((2 * m) * kGroup + ct) * 16);
+                const float4 b = *reinterpret_cast<const float4 *>(rawb + ((2 * m + 1) * kGroup + ct) * 16);
+                const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                uint4 pl[3];
+                split3(x, pl);
+                const uint32_t off = sw128_offset((uint32_t)r, (uint32_t)g8 * 8u);
+#pragma unroll
+                for (int k = 0; k < 3; ++k) *reinterpret_cast<uint4 *>(planes + k * kHalfPlane + off) = pl[k];
+            }
+            fence_async_smem();
+            mbar_arrive(&bars[kBarFull + pb]);
+            // every copied unit is converted now except unit u + 1
+            if (have1 == 2) {                      // unit u + 1 was not known: every unit
+                have1 = next_unit(i1, t1, h1, true);   // copied so far is converted, so wait
+                if (have1 < 0) { fail(); break; }
+                if (have1 == 1) issue(i1, t1, h1, (u + 1) & 1);
+            }
+            have0 = have1;
+            i0 = i1; t0 = t1; h0 = h1;
+            have1 = 0;
+            if (have0 == 1) {                      // refill buffer u & 1 with unit u + 2
+                have1 = next_unit(i1, t1, h1, false);
+                if (have1 == 1) issue(i1, t1, h1, u & 1);
+            }
+        }
+        cp_async_wait_all();
+    }
+
+    if (!ok) flag(p.status, HISA_DEV_TIMEOUT);
+    fence_before_sync();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+int score_pipe_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b, int keep) {
+    if (H_i != kH || D_i != kD || n_max < 1) return 0;
+    if (mode == kCoarse) return !rows_bf16 && n_max <= kPipeMaxCoarse;
+    if (mode == kFine) return rows_bf16 && b == 64 && keep >= 1 && keep <= 64 && n_max <= kPipeMaxFine;
+    return 0;
+}
+
+namespace {
+
+int sm_count() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (counts[dev] == 0) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = c;
+    }
+    return counts[dev];
+}
+
+template <int MODE, bool QBF16>
+cudaError_t launch_pipe_t(const ScoreTcParams &p, cudaStream_t s) {
+    constexpr int cap = MODE == kCoarse ? kPipeMaxCoarse : kPipeMaxFine;
+    static const cudaError_t attr =
+        cudaFuncSetAttribute(k_score_pipe<MODE, QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(Layout<MODE>::fixed + 2 * cap * 4));
+    if (attr != cudaSuccess) return attr;
+    const int rows = p.s.B * p.s.L;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int grid = rows < sms ? rows : sms;
+    const size_t smem = Layout<MODE>::fixed + 2 * (size_t)p.s.n_max * 4;
+    k_score_pipe<MODE, QBF16><<<grid, pipe_threads<MODE>(), smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_score_pipe(const ScoreTcParams &p_in, cudaStream_t s) {
+    ScoreTcParams p = p_in;
+    if (p.s.B * p.s.L == 0) return cudaSuccess;
+    if (p.s.mode == kFine &&
+        !encode_bf16_map(&p.keys_map, p.s.rows, (uint64_t)p.s.keys_rows, kD, 64, 64))
+        return cudaErrorInvalidValue;
+    const bool qb = p.s.q_bf16 != 0;
+    switch (p.s.mode) {
+        case kCoarse: return qb ? launch_pipe_t<kCoarse, true>(p, s) : launch_pipe_t<kCoarse, false>(p, s);
+        case kFine: return qb ? launch_pipe_t<kFine, true>(p, s) : launch_pipe_t<kFine, false>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace hisa

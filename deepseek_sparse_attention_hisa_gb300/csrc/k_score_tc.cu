@@ -404,17 +404,20 @@ __global__ void __launch_bounds__(kThreads, 2) k_score_tc(const __grid_constant_
         int32_t *out = P.sel + (int64_t)row * P.k_sel;
         const int aborted = misc->abort;
         const int64_t kout = aborted ? 0 : (n < P.k_sel ? n : (int64_t)P.k_sel);
+        // n <= kMaxSel <= kSmallMax scores in shared memory
+        static_assert(kMaxSel <= kSmallMax, "fused select capacity");
         if (MODE == kFine) {
             const uint32_t b = (uint32_t)p.b;
-            block_topk<kThreads>(sc, n, kout, out,
-                                 [&](int64_t i) {
-                                     const uint32_t q32 = (uint32_t)i / b;
-                                     return (int32_t)((uint32_t)blk[q32] * b + ((uint32_t)i - q32 * b));
-                                 },
-                                 sel_sh, p.status);
+            small_topk<kThreads, 0, 0>(
+                sc, (int)n, (int)kout, out,
+                [&](int64_t i) {
+                    const uint32_t q32 = (uint32_t)i / b;
+                    return (int32_t)((uint32_t)blk[q32] * b + ((uint32_t)i - q32 * b));
+                },
+                sel_sh, p.status);
         } else {
-            block_topk<kThreads>(sc, n, kout, out, [](int64_t i) { return (int32_t)i; }, sel_sh,
-                                 p.status);
+            small_topk<kThreads, 0, 0>(sc, (int)n, (int)kout, out, [](int64_t i) { return (int32_t)i; },
+                                       sel_sh, p.status);
         }
         for (int64_t e = kout + tid; e < P.k_sel; e += kThreads) out[e] = -1;
     }

@@ -22,6 +22,16 @@ namespace hisa {
 
 constexpr int kCand = 1024;
 
+// Barrier of the selecting threads: the whole CTA (BAR == 0) or the NT threads of named
+// barrier BAR (a group of whole warps that selects while the other warps keep working).
+template <int NT, int BAR>
+__device__ __forceinline__ void group_sync() {
+    if (BAR == 0)
+        __syncthreads();
+    else
+        asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NT) : "memory");
+}
+
 template <int NT>
 struct SelectShared {
     uint32_t hist[256];
@@ -81,37 +91,39 @@ constexpr float kMaskedBelow = -1e29f;
 
 // Block-wide radix select over the full keys: four 8-bit passes; resolves any input.
 // Leaves the k-th key in sh.prefix and the count of its equals to take in sh.kk.
-template <int NT>
+// The selecting threads are threadIdx.x in [TID0, TID0 + NT) (TID0 a multiple of 32).
+template <int NT, int BAR = 0, int TID0 = 0>
 __device__ void block_radix_threshold(const float *sc, int64_t n, uint32_t kout,
                                       SelectShared<NT> &sh) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = (int)threadIdx.x - TID0, lane = tid & 31, warp = tid >> 5;
     uint32_t prefix = 0u, mask = 0u, kk = kout;
     for (int shift = 24; shift >= 0; shift -= 8) {
         for (int e = tid; e < 256; e += NT) sh.hist[e] = 0u;
-        __syncthreads();
+        group_sync<NT, BAR>();
         for (int64_t base = (int64_t)warp * 32; base < n; base += NT) {
             const int64_t i = base + lane;
             const uint32_t key = i < n ? order_key(sc[i]) : 0u;
             warp_hist_add(sh.hist, i < n && (key & mask) == prefix, (key >> shift) & 255u);
         }
-        __syncthreads();
+        group_sync<NT, BAR>();
         if (warp == 0) warp_find_digit(sh.hist, prefix, kk, shift, &sh.prefix, &sh.kk);
-        __syncthreads();
+        group_sync<NT, BAR>();
         prefix = sh.prefix;
         kk = sh.kk;
         mask |= 255u << shift;
-        __syncthreads();
+        group_sync<NT, BAR>();
     }
 }
 
 // Writes the kout selected columns, mapped through map(i), to out[0..kout) in ascending
-// column order. Caller guarantees 0 <= kout <= n. Contains __syncthreads(): every thread
-// of the CTA must call it with the same arguments.
-template <int NT, typename Map>
+// column order. Caller guarantees 0 <= kout <= n. Contains barriers (group_sync<NT, BAR>):
+// every selecting thread (threadIdx.x in [TID0, TID0 + NT)) must call it with the same
+// arguments.
+template <int NT, int BAR = 0, int TID0 = 0, typename Map>
 __device__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *out, Map map,
                            SelectShared<NT> &sh, uint32_t *status) {
     constexpr int NW = NT / 32;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = (int)threadIdx.x - TID0, lane = tid & 31, warp = tid >> 5;
     if (kout <= 0) return;
 
     // ---- range of the unmasked finite scores (as keys: integer min / max) ----
@@ -135,7 +147,7 @@ __device__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *ou
     if (lane == 0) { sh.wg[warp] = kmin; sh.we[warp] = kmax; sh.cand[warp] = (int32_t)nfree; }
     if (tid == 0) { sh.nonfinite = 0; sh.ncand = 0u; }
     for (int e = tid; e < 256; e += NT) sh.hist[e] = 0u;
-    __syncthreads();
+    group_sync<NT, BAR>();
     if (lane == 0 && nonfinite) sh.nonfinite = 1;
     kmin = 0xffffffffu;
     kmax = 0u;
@@ -145,12 +157,12 @@ __device__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *ou
         kmax = sh.we[w] > kmax ? sh.we[w] : kmax;
         nfree += (uint32_t)sh.cand[w];
     }
-    __syncthreads();
+    group_sync<NT, BAR>();
     const float smin = key_to_float(kmin), smax = key_to_float(kmax);
     const float scale = 255.0f / (smax - smin);
     if (nfree < (uint64_t)kout || !(smax > smin) || !isfinite(scale)) {
         // the k-th score is masked, or the unmasked scores are (nearly) all equal
-        block_radix_threshold<NT>(sc, n, (uint32_t)kout, sh);
+        block_radix_threshold<NT, BAR, TID0>(sc, n, (uint32_t)kout, sh);
     } else {
         // value bins: bin(s) is non-decreasing in s, so a higher bin holds strictly
         // larger scores and equal scores share a bin
@@ -165,10 +177,10 @@ __device__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *ou
             const float v = i < n ? sc[i] : 0.f;
             warp_hist_add(sh.hist, i < n, bin_of(v));
         }
-        __syncthreads();
+        group_sync<NT, BAR>();
         // the bin of the k-th largest score; sh.kk = its rank inside that bin
         if (warp == 0) warp_find_digit(sh.hist, 0u, (uint32_t)kout, 0, &sh.prefix, &sh.kk);
-        __syncthreads();
+        group_sync<NT, BAR>();
         const uint32_t dbin = sh.prefix;
         uint32_t kk = sh.kk;
         for (int64_t base = (int64_t)warp * 32; base < n; base += NT) {
@@ -180,7 +192,7 @@ __device__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *ou
             at = __shfl_sync(0xffffffffu, at, 0) + __popc(bal & ((1u << lane) - 1u));
             if (c && at < (uint32_t)kCand) sh.cand[at] = (int32_t)i;
         }
-        __syncthreads();
+        group_sync<NT, BAR>();
         const uint32_t m = sh.ncand;
         if (m <= 32u) {
             if (warp == 0) {                   // few candidates: rank them directly
@@ -219,10 +231,10 @@ __device__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *ou
                 }
             }
         } else {
-            block_radix_threshold<NT>(sc, n, (uint32_t)kout, sh);
+            block_radix_threshold<NT, BAR, TID0>(sc, n, (uint32_t)kout, sh);
         }
     }
-    __syncthreads();
+    group_sync<NT, BAR>();
     if (tid == 0 && sh.nonfinite) flag(status, HISA_DEV_NONFINITE);
     const uint32_t T = sh.prefix;
     const uint32_t kk = sh.kk;
@@ -239,7 +251,7 @@ __device__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *ou
         ce += __popc(__ballot_sync(0xffffffffu, i < hi && key == T));
     }
     if (lane == 0) { sh.wg[warp] = cg; sh.we[warp] = ce; }
-    __syncthreads();
+    group_sync<NT, BAR>();
     if (warp == 0) {
         const uint32_t vg = lane < NW ? sh.wg[lane] : 0u;
         const uint32_t ve = lane < NW ? sh.we[lane] : 0u;
@@ -252,7 +264,7 @@ __device__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *ou
         }
         if (lane < NW) { sh.wg[lane] = ig - vg; sh.we[lane] = ie - ve; }
     }
-    __syncthreads();
+    group_sync<NT, BAR>();
     uint32_t base_g = sh.wg[warp], base_e = sh.we[warp];
     for (int64_t start = lo; start < hi; start += 32) {
         const int64_t i = start + lane;
@@ -269,7 +281,175 @@ __device__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *ou
         base_g += __popc(bg);
         base_e += __popc(be);
     }
-    __syncthreads();
+    group_sync<NT, BAR>();
+}
+
+}  // namespace hisa
+
+namespace hisa {
+
+// Capacity of the threshold bin that small_topk resolves itself.
+constexpr int kSmallCand = 128;
+
+// Top kout of n <= kSmallMax scores held in shared memory, for the common case: finite
+// scores, at least kout unmasked, a non-degenerate range and at most kSmallCand scores in
+// the k-th score's bin; anything else goes to block_topk. Warp w owns columns
+// [w * seg, (w + 1) * seg). Four passes over the scores: range; value-bin histogram (the
+// bins of block_topk); threshold-bin candidates plus per-warp counts above the bin; and
+// the emission. The candidates are ranked once, exactly, by (key desc, column asc) into a
+// bitmap of selected columns. The selection is written in ascending column order and
+// equals block_topk's. Each lane handles four columns per step, so that their shared-
+// memory loads overlap (a selecting warp may be the only warp of its SM sub-partition).
+// Caller guarantees 0 <= kout <= n <= kSmallMax. Contains group_sync<NT, BAR>().
+constexpr int kSmallMax = (kCand - 2 * kSmallCand) * 32;
+template <int NT, int BAR, int TID0, typename Map>
+__device__ void small_topk(const float *sc, int n, int kout, int32_t *out, Map map,
+                           SelectShared<NT> &sh, uint32_t *status) {
+    constexpr int NW = NT / 32, U = 4;
+    const int tid = (int)threadIdx.x - TID0, lane = tid & 31, warp = tid >> 5;
+    if (kout <= 0) return;
+    const int seg = ((n + NW * 32 * U - 1) / (NW * 32 * U)) * (32 * U);
+    const int lo = warp * seg, hi = lo + seg < n ? lo + seg : n;
+    uint32_t *bits = reinterpret_cast<uint32_t *>(sh.cand + 2 * kSmallCand);   // selected columns
+    uint32_t kmin = 0xffffffffu, kmax = 0u, nfree = 0u;
+    int nonfinite = 0;
+    for (int base = lo + lane; base < hi; base += 32 * U) {
+        float x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) x[u] = base + 32 * u < hi ? sc[base + 32 * u] : kNeg;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const bool fin = isfinite(x[u]);
+            nonfinite |= !fin;
+            if (fin && x[u] > kMaskedBelow) {
+                const uint32_t key = order_key(x[u]);
+                kmin = key < kmin ? key : kmin;
+                kmax = key > kmax ? key : kmax;
+                ++nfree;
+            }
+        }
+    }
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    nfree = __reduce_add_sync(0xffffffffu, nfree);
+    nonfinite = __reduce_or_sync(0xffffffffu, nonfinite);
+    if (lane == 0) {
+        sh.wg[warp] = kmin;
+        sh.we[warp] = kmax;
+        sh.cand[warp] = (int32_t)nfree;
+        sh.cand[NW + warp] = nonfinite;
+    }
+    for (int e = tid; e < 256; e += NT) sh.hist[e] = 0u;
+    for (int e = tid; e < (n + 31) / 32; e += NT) bits[e] = 0u;
+    if (tid == 0) sh.ncand = 0u;
+    group_sync<NT, BAR>();
+    kmin = 0xffffffffu;
+    kmax = 0u;
+    nfree = 0u;
+    nonfinite = 0;
+    for (int w = 0; w < NW; ++w) {
+        kmin = sh.wg[w] < kmin ? sh.wg[w] : kmin;
+        kmax = sh.we[w] > kmax ? sh.we[w] : kmax;
+        nfree += (uint32_t)sh.cand[w];
+        nonfinite |= sh.cand[NW + w];
+    }
+    const float smin = key_to_float(kmin), smax = key_to_float(kmax);
+    const float scale = 255.0f / (smax - smin);
+    if (nonfinite || nfree < (uint32_t)kout || !(smax > smin) || !isfinite(scale)) {
+        group_sync<NT, BAR>();                       // everyone has read sh before it is reused
+        block_topk<NT, BAR, TID0>(sc, n, kout, out, map, sh, status);
+        return;
+    }
+    auto bin_of = [&](float x) -> int {
+        if (!(x >= smin)) return 0;
+        if (!(x < smax)) return 255;
+        const int b = (int)((x - smin) * scale);
+        return b < 0 ? 0 : (b > 254 ? 254 : b);
+    };
+    for (int base = lo + lane; base < hi; base += 32 * U) {
+        float x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) x[u] = base + 32 * u < hi ? sc[base + 32 * u] : 0.f;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + 32 * u < hi) atomicAdd(&sh.hist[bin_of(x[u])], 1u);
+    }
+    group_sync<NT, BAR>();
+    if (warp == 0) warp_find_digit(sh.hist, 0u, (uint32_t)kout, 0, &sh.prefix, &sh.kk);
+    if (tid < NW) sh.wg[tid] = 0u;                   // threshold-bin selections per warp
+    group_sync<NT, BAR>();
+    const int tb = (int)sh.prefix;
+    const uint32_t kk = sh.kk;                       // taken from the threshold bin
+    uint32_t above = 0u;
+    for (int base = lo + lane; base < hi; base += 32 * U) {
+        float x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) x[u] = base + 32 * u < hi ? sc[base + 32 * u] : 0.f;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + 32 * u;
+            if (i < hi) {
+                const int b = bin_of(x[u]);
+                above += b > tb ? 1u : 0u;
+                if (b == tb) {
+                    const uint32_t slot = atomicAdd(&sh.ncand, 1u);
+                    if (slot < (uint32_t)kSmallCand) {
+                        sh.cand[2 * slot] = i;
+                        sh.cand[2 * slot + 1] = (int32_t)order_key(x[u]);
+                    }
+                }
+            }
+        }
+    }
+    above = __reduce_add_sync(0xffffffffu, above);
+    if (lane == 0) sh.we[warp] = above;
+    group_sync<NT, BAR>();
+    const uint32_t m = sh.ncand;
+    if (m > (uint32_t)kSmallCand) {
+        group_sync<NT, BAR>();
+        block_topk<NT, BAR, TID0>(sc, n, kout, out, map, sh, status);
+        return;
+    }
+    // rank every candidate once; the kk first in (key desc, column asc) are selected
+    for (uint32_t c = tid; c < m; c += NT) {
+        const int ic = sh.cand[2 * c];
+        const uint32_t kc = (uint32_t)sh.cand[2 * c + 1];
+        uint32_t r = 0u;
+        for (uint32_t d = 0; d < m; ++d) {
+            const uint32_t kd = (uint32_t)sh.cand[2 * d + 1];
+            r += (kd > kc || (kd == kc && sh.cand[2 * d] < ic)) ? 1u : 0u;
+        }
+        if (r < kk) {
+            atomicOr(&bits[ic >> 5], 1u << (ic & 31));
+            atomicAdd(&sh.wg[ic / seg], 1u);
+        }
+    }
+    group_sync<NT, BAR>();
+    uint32_t pos = 0u;
+    for (int w = 0; w < warp; ++w) pos += sh.we[w] + sh.wg[w];
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int base = lo; base < hi; base += 32 * U) {
+        float x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + 32 * u + lane;
+            x[u] = i < hi ? sc[i] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + 32 * u + lane;
+            bool s = false;
+            if (i < hi) {
+                const int b = bin_of(x[u]);
+                s = b > tb || (b == tb && ((bits[i >> 5] >> (i & 31)) & 1u));
+            }
+            const uint32_t bal = __ballot_sync(0xffffffffu, s);
+            const uint32_t at = pos + __popc(bal & lt);
+            if (s && at < (uint32_t)kout) out[at] = map(i);
+            pos += __popc(bal);
+        }
+    }
+    group_sync<NT, BAR>();
 }
 
 }  // namespace hisa

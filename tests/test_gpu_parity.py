@@ -342,3 +342,53 @@ def test_offsets_past_the_allocation_are_skipped():
     torch.cuda.synchronize()
     assert prob.status() & hb.DEV_BAD_OFFSETS
     P.check_attend(data, 0, 0, np_(out)[0], None)
+
+
+def test_many_queries_per_sm_with_invalid_rows_between():
+    """More query rows than SMs, so each persistent scoring CTA walks several; rows that
+    fail the gate or carry a bad kept block sit between valid ones and must not disturb
+    the rows after them."""
+    B = 330
+    rng = np.random.default_rng(21)
+    Np = rng.integers(1024, 3000, size=B)
+    Np[[5, 157, 158, 310]] = 700                  # below index_block * index_keep = 1024
+    wl = inputs.small_workload(name="many_rows", seed=21, B=B, H_i=64, D_i=128, index_block=64,
+                               index_keep=16, index_topk=512, q_idx_dtype="f32", key_dtype="bf16",
+                               Np=tuple(int(x) for x in Np), with_attention=False)
+    data = inputs.generate(wl)
+    prob = Problem(data)
+    rows_cs = torch.full((B, int(prob.nb.max())), 7.0, device="cuda")
+    rows_fs = torch.full((B, 1024), 7.0, device="cuda")
+    prob.block_means()
+    prob.block_filter(cscores=rows_cs)
+    torch.cuda.synchronize()
+    assert prob.status() == hb.DEV_GATE
+    tb = np_(prob.top_blk)
+    bad = [5, 157, 158, 310]
+    assert np.all(tb[bad] == -1)
+    tb_bad = tb.copy()
+    tb_bad[200, 3] = 10 ** 6                      # one row with an out-of-range kept block
+    hb.workspace_init(prob.ws)
+    prob.select_topk(top_blk=torch.as_tensor(tb_bad, device="cuda"), fscores=rows_fs)
+    torch.cuda.synchronize()
+    assert prob.status() == (hb.DEV_GATE | hb.DEV_BAD_BLOCK)
+    I = np_(prob.I)
+    assert np.all(I[bad] == -1) and np.all(I[200] == -1)
+    cs, fs = np_(rows_cs), np_(rows_fs)
+    for b in (0, 1, 4, 6, 151, 152, 153, 156, 159, 199, 201, 303, 304, 309, 311, 329):
+        P.check_coarse(data, b, 0, tb[b], cs[b], wl.index_block, wl.index_keep)
+        P.check_fine(data, b, 0, tb[b], I[b], fs[b], wl.index_block, wl.index_topk)
+
+
+@pytest.mark.parametrize("t0,qd", [(2000, "f32"), (7000, "bf16")])
+def test_v4_shape_batched_rows_with_few_visible(t0, qd):
+    """The tensor-core pipeline with L > 1 at the V4 indexer shape: at t0 = 2000 every row
+    sees fewer than keep eligible blocks and fewer than k visible candidates (masked ids
+    fill the selection); at t0 = 7000 the visibility edge falls inside the kept blocks."""
+    wl = inputs.small_workload(name="v4_few_visible", seed=31, L=48, H_i=64, D_i=128,
+                               index_block=64, index_keep=16, index_topk=512, q_idx_dtype=qd,
+                               key_dtype="bf16", Np=(2048,), t0=t0, with_attention=False)
+    data = inputs.generate(wl)
+    prob = Problem(data)
+    res = run_hisa(prob)
+    check_rows(data, prob, res, [(0, j) for j in range(0, 48, 3)] + [(0, 47)])
