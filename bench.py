@@ -33,6 +33,16 @@ UNIT = "queries/s"
 L2_FLUSH_BYTES = 256 << 20
 
 
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -368,9 +378,15 @@ def run_gpu(args, wl, R):
         with torch.cuda.graph(g, stream=stream):
             calls[name](stream)
         graphs[name] = g
+    # the whole step as one graph (the headline), and one graph per stage (stage times)
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
+        for name in stages:
+            calls[name](stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def step(evs=None):
+        """One step from the per-stage graphs, with an event after every stage."""
         if evs is not None:
             evs[0].record(stream)
         for i, name in enumerate(stages):
@@ -381,11 +397,15 @@ def run_gpu(args, wl, R):
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             flush.zero_()
+            g_step.replay()
+            flush.zero_()
             step()
     stream.synchronize()
     assert prob.status(stream) == 0, "device status flags set during warm-up"
 
     K = args.steps
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
     if world > 1:
         dist.barrier()
@@ -394,14 +414,19 @@ def run_gpu(args, wl, R):
         clk.mark_start()
         t_wall = time.perf_counter()
         with torch.cuda.stream(stream):
-            for i in range(K):
+            for i in range(K):                      # headline: whole-step graph
                 flush.zero_()                       # L2 flush outside the step's events
+                step_ev[i][0].record(stream)
+                g_step.replay()
+                step_ev[i][1].record(stream)
+            for i in range(K):                      # stage times: per-stage graphs
+                flush.zero_()
                 step(evs[i])
         stream.synchronize()
         t_wall = time.perf_counter() - t_wall
         clk.mark_stop()
     torch.cuda.synchronize()
-    step_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(K)]
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
     stage_ms = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]
                 for j, name in enumerate(stages)}
     total_ms = max_over_ranks(sum(step_ms), dev)
@@ -424,7 +449,7 @@ def run_gpu(args, wl, R):
             prob.q_idx.copy_(host_in["q_idx"], non_blocking=True)
             prob.w.copy_(host_in["w"], non_blocking=True)
             prob.q_attn.copy_(host_in["q_attn"], non_blocking=True)
-            step()
+            g_step.replay()
             host_out["out"].copy_(prob.out, non_blocking=True)
             host_out["I"].copy_(prob.I, non_blocking=True)
             e2e_ev[i][1].record(stream)
@@ -456,7 +481,7 @@ def run_gpu(args, wl, R):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic},
-        "gpu_launches": K * launches_per_step(prob),
+        "gpu_launches": 2 * K * launches_per_step(prob),   # whole-step pass + per-stage pass
         "e2e": {"value": job_value(world, R, 1, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "wall_s": t_wall,
@@ -469,11 +494,52 @@ def run_gpu(args, wl, R):
         line["cpu_baseline"] = {"value": n / el, "unit": UNIT, "cores": cores_used(),
                                 "kind": "oracle",
                                 "sample": f"{n} queries of sequence 0 of the batch, {el:.1f} s"}
+    if not args.no_prefill:
+        line["prefill_scoring"] = run_prefill_scoring(args, dev, stream)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def prefill_flops(wl):
+    """Unmasked flops of the dense prefill scoring: sum over rows j of V(t0 + j) keys x
+    H_i heads x D_i dims x 2 (multiply and add)."""
+    Np = int(wl.Np[0])
+    V = np.minimum(Np, (wl.t0 + np.arange(wl.L) + 1) // wl.r)
+    return int(V.sum()) * wl.H_i * wl.D_i * 2
+
+
+def run_prefill_scoring(args, dev, stream):
+    """hisa_index_scores on the batched-prefill workload (L = 4096 rows, Np = 16384 bf16
+    keys, bf16 q): the dense L x Np x (H_i * D_i) contraction, timed with CUDA events."""
+    import torch
+
+    from deepseek_sparse_attention_hisa_gb300.problem import Problem
+    wl = inputs.WORKLOADS["prefill"].replace(with_attention=False)
+    data = inputs.generate_device(wl, device=dev, seed=3000)
+    prob = Problem(data, device=dev)
+    scores = torch.empty((wl.L, int(wl.Np[0])), dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            prob.index_scores(scores, stream=stream)
+    stream.synchronize()
+    n = 10
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            a.record(stream)
+            prob.index_scores(scores, stream=stream)
+            b.record(stream)
+    stream.synchronize()
+    assert prob.status(stream) == 0
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    flops = prefill_flops(wl)
+    peak = bf16_peak()
+    return {"workload": "prefill L=4096 x Np=16384 x (64 x 128), bf16 q and keys, causal",
+            "ms": ms, "flops": flops, "tflops": flops / ms / 1e9, "peak_tflops": peak[0],
+            "peak_source": peak[1], "frac": flops / ms / 1e9 / peak[0]}
 
 
 def launches_per_step(prob):
@@ -497,6 +563,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-queries", type=int, default=4, help="oracle queries per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill scoring leg")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
