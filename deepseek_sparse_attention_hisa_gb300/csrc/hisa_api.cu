@@ -137,6 +137,9 @@ cudaError_t run_scores(const ScoreParams &p, int32_t *sel, int k_sel, bool *fuse
         *fused = true;
         return launch_score_pipe(t, s);
     }
+    if (p.mode == kFlat && p.out && p.keys_rows > 0 &&
+        score_gemm_supported(p.H_i, p.D_i, p.q_bf16, p.rows_bf16, p.B, p.L))
+        return launch_score_gemm(p, s);
     if (score_tc_supported(p.mode, p.H_i, p.D_i, p.rows_bf16, p.n_max, p.b) &&
         (p.mode == kCoarse || p.keys_rows > 0)) {
         ScoreTcParams t{};

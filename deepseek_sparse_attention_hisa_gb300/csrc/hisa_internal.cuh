@@ -157,5 +157,8 @@ int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max,
 // Persistent coarse / fine scoring + select pipeline (one CTA per SM over all query rows).
 cudaError_t launch_score_pipe(const ScoreTcParams &p, cudaStream_t s);
 int score_pipe_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b, int keep);
+// Dense scoring of many query rows per sequence (batched prefill): flat scores to p.out.
+cudaError_t launch_score_gemm(const ScoreParams &p, cudaStream_t s);
+int score_gemm_supported(int H_i, int D_i, int q_bf16, int rows_bf16, int B, int L);
 
 }  // namespace hisa

@@ -138,6 +138,13 @@ def test_prefill_sampled_rows():
         q, w = data["q_idx"][0, j], data["w"][0, j]
         o = O.flat_scores(q[None], w[None], data["keys"], int(data["t0"][0]) + j, 4, causal=True)[0]
         P.check_scores(sc[j], o, O.error_scale(q, w, data["keys"]), what=f"prefill score row {j}")
+    # the flat selection over those scores
+    I = torch.full((L, prob.k), -7, dtype=torch.int32, device="cuda")
+    prob.flat_topk(I)
+    torch.cuda.synchronize()
+    I = np_(I)
+    for j in rows[:4]:
+        P.check_flat(data, 0, j, I[j], prob.k)
 
 
 @pytest.mark.parametrize("keep", [16, 64])
@@ -392,3 +399,31 @@ def test_v4_shape_batched_rows_with_few_visible(t0, qd):
     prob = Problem(data)
     res = run_hisa(prob)
     check_rows(data, prob, res, [(0, j) for j in range(0, 48, 3)] + [(0, 47)])
+
+
+def test_dense_scoring_partial_units_and_ragged_sequences():
+    """The dense scoring of many bf16 query rows per sequence (four rows per tensor-core
+    unit): L = 6 leaves a partial unit, three sequences of different Np, and the causal
+    edge V(t0 + j) falls inside the key tiles of the first two."""
+    wl = inputs.small_workload(name="dense_rows", seed=41, B=3, L=6, H_i=64, D_i=128,
+                               index_block=64, index_keep=16, index_topk=512, q_idx_dtype="bf16",
+                               key_dtype="bf16", Np=(700, 1500, 300), t0=2200, with_attention=False)
+    data = inputs.generate(wl)
+    prob = Problem(data)
+    sc = torch.full((wl.B * wl.L, prob.Np_max), 7.0, device="cuda")
+    prob.index_scores(sc)
+    I = torch.full((wl.B * wl.L, wl.index_topk), -7, dtype=torch.int32, device="cuda")
+    prob.flat_topk(I)
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    sc, I = np_(sc), np_(I)
+    for b in range(wl.B):
+        s = P.seq(data, b)
+        for j in range(wl.L):
+            r = b * wl.L + j
+            q, w = data["q_idx"][b, j], data["w"][b, j]
+            o = O.flat_scores(q[None], w[None], s["keys"], s["t0"] + j, wl.r, causal=True)[0]
+            P.check_scores(sc[r, : s["Np"]], o, O.error_scale(q, w, s["keys"]),
+                           what=f"dense score row {b},{j}")
+            assert np.all(sc[r, s["Np"]:] == 7.0)        # columns past Np are not written
+            P.check_flat(data, b, j, I[r], wl.index_topk)
