@@ -35,6 +35,7 @@ class IndexDesc(ctypes.Structure):
                 ("D_i", ctypes.c_int32), ("r", ctypes.c_int32), ("index_topk", ctypes.c_int32),
                 ("index_block", ctypes.c_int32), ("index_keep", ctypes.c_int32),
                 ("Np_max", ctypes.c_int64), ("keys_rows", ctypes.c_int64),
+                ("means_rows", ctypes.c_int64),
                 ("q_dtype", ctypes.c_int32), ("k_dtype", ctypes.c_int32)]
 
 

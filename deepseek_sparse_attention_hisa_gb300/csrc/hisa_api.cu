@@ -26,6 +26,7 @@ hisa_status check_index_desc(const hisa_index_desc *d) {
     if (d->index_block < 0 || d->index_keep < 0 || d->index_keep > 64) return HISA_EINVAL;
     if (d->Np_max < 0 || d->Np_max > (int64_t)65535 * 256) return HISA_EINVAL;
     if (d->keys_rows < 0 || d->keys_rows > 0x7fffffffLL) return HISA_EINVAL;
+    if (d->means_rows < 0 || d->means_rows > 0x7fffffffLL) return HISA_EINVAL;
     if ((int64_t)d->B * d->L > 0x7fffffffLL) return HISA_EINVAL;
     if (!dtype_ok(d->q_dtype) || !dtype_ok(d->k_dtype)) return HISA_EDTYPE;
     if (d->D_i != 32 && d->D_i != 64 && d->D_i != 128) return HISA_EDTYPE;
@@ -117,6 +118,7 @@ ScoreParams score_params(const hisa_index_desc *d, int mode, const void *q, cons
     p.out = out; p.ld_out = ld;
     p.Np_max = d->Np_max;
     p.keys_rows = d->keys_rows;
+    p.means_rows = d->means_rows;
     p.status = status_of(ws);
     return p;
 }
@@ -129,7 +131,7 @@ cudaError_t run_scores(const ScoreParams &p, int32_t *sel, int k_sel, bool *fuse
     *fused = false;
     if (sel && p.mode != kFlat &&
         score_pipe_supported(p.mode, p.H_i, p.D_i, p.rows_bf16, p.n_max, p.b, p.keep) &&
-        (p.mode == kCoarse || p.keys_rows > 0)) {
+        (p.mode == kCoarse ? p.means_rows > 0 : p.keys_rows > 0)) {
         ScoreTcParams t{};
         t.s = p;
         t.sel = sel;
@@ -249,7 +251,8 @@ hisa_status hisa_block_means(const hisa_index_desc *d, const void *keys, const i
     p.B = d->B; p.D_i = d->D_i; p.b = d->index_block;
     p.keys = keys; p.keys_bf16 = d->k_dtype == HISA_BF16;
     p.key_off = key_off; p.means_off = means_off; p.first_block = first_block;
-    p.means = means; p.Np_max = d->Np_max; p.keys_rows = d->keys_rows; p.status = status_of(ws);
+    p.means = means; p.Np_max = d->Np_max; p.keys_rows = d->keys_rows;
+    p.means_rows = d->means_rows; p.status = status_of(ws);
     return from_cuda(launch_block_means(p, d->Np_max / d->index_block,
                                         reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -42,6 +42,13 @@ __device__ __forceinline__ bool seq_ok(const int64_t *off, int b, int64_t Np_max
     return a >= 0 && e >= a && e - a <= Np_max && e <= rows;
 }
 
+// Sequence b's nb block-mean rows [moff[b], moff[b] + nb) fit its offsets and lie inside
+// the rows allocated in the block-mean array.
+__device__ __forceinline__ bool means_ok(const int64_t *moff, int b, int64_t nb, int64_t rows) {
+    const int64_t a = moff[b], e = moff[b + 1];
+    return a >= 0 && e - a >= nb && a + nb <= rows;
+}
+
 // Orderable key of an f32 score: larger float -> larger key; -0.0 == +0.0.
 __device__ __forceinline__ uint32_t order_key(float s) {
     uint32_t u = __float_as_uint(s);
@@ -71,6 +78,7 @@ struct ScoreParams {
     int64_t n_max;            // max scored rows per query row (grid.x extent)
     int64_t Np_max;
     int64_t keys_rows;        // rows allocated in the key array
+    int64_t means_rows;       // rows allocated in the block-mean array (coarse)
     uint32_t *status;
 };
 
@@ -97,6 +105,7 @@ struct MeansParams {
     float *means;
     int64_t Np_max;
     int64_t keys_rows;
+    int64_t means_rows;
     uint32_t *status;
 };
 
@@ -128,6 +137,7 @@ struct AttnParams {
 // is optional for them (the scores of every row) and required for the flat mode.
 struct ScoreTcParams {
     CUtensorMap keys_map;     // bf16 keys [keys_rows, 128], box 64 dims x 64 rows, 128B swizzle
+    CUtensorMap means_map;    // f32 block means [means_rows, 128], box 32 dims x 128 rows, 128B swizzle
     ScoreParams s;
     int32_t *sel;
     int k_sel;
@@ -137,6 +147,8 @@ struct ScoreTcParams {
 // Encodes a 2-D bf16 tensor map over [rows, cols] (row-major) with a box of box_cols x
 // box_rows and the 128-byte swizzle. Returns false if the driver has no encoder or
 // rejects the map.
+bool encode_f32_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                    uint32_t box_cols, uint32_t box_rows);
 bool encode_bf16_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                      uint32_t box_cols, uint32_t box_rows);
 

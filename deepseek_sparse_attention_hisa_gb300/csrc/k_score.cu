@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256) k_scores_simt(ScoreParams p) {
             return;
         }
         n = (p.mode == kCoarse) ? Np / p.b : (int64_t)p.keep * p.b;
-        if (p.mode == kCoarse && p.means_off[bq + 1] - p.means_off[bq] < n) {
+        if (p.mode == kCoarse && !means_ok(p.means_off, bq, n, p.means_rows)) {
             if (threadIdx.x == 0 && blockIdx.y == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
             return;
         }
@@ -176,7 +176,7 @@ __global__ void k_block_means(MeansParams p) {
     }
     const int64_t nb = Np / p.b;
     const int64_t m0 = p.means_off[bq];
-    if (p.means_off[bq + 1] - m0 < nb) {
+    if (!means_ok(p.means_off, bq, nb, p.means_rows)) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
         return;
     }

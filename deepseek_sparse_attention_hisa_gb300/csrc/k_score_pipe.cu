@@ -10,11 +10,12 @@
 // form a pipeline, so that one query's set-up and top-k overlap the next query's
 // streaming and only the first set-up and the last top-k are exposed:
 //   warp 0      MMA issue (one elected lane) and TMEM owner
-//   warp 1      fine: TMA producer of the kept blocks' bf16 key tiles
+//   warp 1      fine: TMA producer of the kept blocks' bf16 key tiles; coarse: bulk
+//               copies of the block means (256-byte row halves) into three raw slots
 //   warps 2-5   epilogue: TMEM -> relu, head weights, head sum -> scores in shared memory
 //   warps 6-9   builders: per-query checks, kept blocks, head weights, q planes
 //   warps 10-13 select: block top-k over the finished query's scores (named barrier 1)
-//   warps 14-17 coarse: converters, f32 block means -> three bf16 planes
+//   warps 14-21 coarse: converters, f32 block means -> three bf16 planes
 //
 // A tile is 128 scored rows, D[128 rows x 64 * planes] = rows . q^T (M = 128, K = 128) in
 // one of two TMEM accumulators. Scoring is f32 on the page; f32 operands are split
@@ -36,10 +37,11 @@ using namespace tc;
 constexpr int kH = 64, kD = 128, kM = 128;
 constexpr int kWarpMma = 0, kWarpTma = 1, kWarpEpi = 2, kWarpBld = 6, kWarpSel = 10, kWarpCvt = 14;
 constexpr int kGroup = 128;                               // threads of each 4-warp role
+constexpr int kCvtWarps = 8, kCvtThreads = kCvtWarps * 32;  // coarse converters
 constexpr int kBarSel = 1, kBarBld = 2;                   // named barriers (0 = __syncthreads)
 
 template <int MODE>
-constexpr int pipe_threads() { return MODE == kCoarse ? 18 * 32 : 14 * 32; }
+constexpr int pipe_threads() { return MODE == kCoarse ? (kWarpCvt + kCvtWarps) * 32 : 14 * 32; }
 
 // ---- shared memory (offsets from the 1024-aligned base) ----
 constexpr uint32_t kQPlane = kH * kD * 2;                 // [64 heads x 128 dims] bf16, 16 KiB
@@ -50,10 +52,13 @@ constexpr uint32_t kTileBytes = kM * kD * 2;              // fine: one [128 x 12
 constexpr uint32_t kRawBytes = kM * 64 * 4;               // coarse: f32 means, 128 rows x 64 dims
 constexpr uint32_t kHalfPlane = kM * 128;                 // [128 rows x 64 dims] bf16, 16 KiB
 constexpr uint32_t kPlaneSet = 3 * kHalfPlane;            // its three planes
+constexpr int kRawSlots = 3;                              // coarse units in flight
+// coarse: kRawSlots raw f32 units, then one plane set; fine: the key tile ring
 template <int MODE>
 constexpr uint32_t region_bytes() {
-    return MODE == kCoarse ? 2 * kRawBytes + 2 * kPlaneSet : kFineSlots * kTileBytes;
+    return MODE == kCoarse ? kRawSlots * kRawBytes + kPlaneSet : kFineSlots * kTileBytes;
 }
+constexpr uint32_t kOffPlanes = kOffReg + kRawSlots * kRawBytes;
 
 struct QMeta {            // one query row, double-buffered
     int row;              // b * L + j
@@ -184,7 +189,9 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             if (b == kBarQFull || b == kBarAccEmpty || b == kBarAccEmpty + 1 || b == kBarScFull ||
                 b == kBarScFull + 1)
                 cnt = kGroup;
-            if (MODE == kCoarse && (b == kBarFull || b == kBarFull + 1)) cnt = kGroup;
+            // coarse: Full / Empty + 0 guard the plane set, + 1 .. 3 the raw slots
+            if (MODE == kCoarse && b == kBarFull) cnt = kCvtThreads;
+            if (MODE == kCoarse && b > kBarEmpty && b <= kBarEmpty + kRawSlots) cnt = kCvtThreads;
             mbar_init(&bars[b], cnt);
         }
         mbar_fence_init();
@@ -212,22 +219,29 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             const int qb = i & 1;
             const int row = (int)blockIdx.x + i * (int)gridDim.x;
             const int bq = row / p.L, j = row - bq * p.L;
-            // this row's q, weights and kept blocks first: the loads overlap the waits
-            float4 qf[QBF16 ? 1 : 2 * kQU];
+            // this row's q, weights and kept blocks first: the loads overlap the waits. With
+            // 22 warps (coarse, f32 q) only half of q is held in registers; the other half is
+            // prefetched into L2 and read once the previous query's planes are free.
+            constexpr bool kHalves = MODE == kCoarse && !QBF16;
+            constexpr int kQHeld = kHalves ? kQU / 2 : kQU;
+            float4 qf[QBF16 ? 1 : 2 * kQHeld];
             uint4 qh[QBF16 ? kQU : 1];
+            const float4 *q4 = reinterpret_cast<const float4 *>(
+                reinterpret_cast<const float *>(p.q) + (int64_t)row * kH * kD);
             if (QBF16) {
                 const uint4 *q16 = reinterpret_cast<const uint4 *>(
                     reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)row * kH * kD);
 #pragma unroll
                 for (int m = 0; m < kQU; ++m) qh[m] = __ldg(q16 + bt + m * kGroup);
             } else {
-                const float4 *q4 = reinterpret_cast<const float4 *>(
-                    reinterpret_cast<const float *>(p.q) + (int64_t)row * kH * kD);
 #pragma unroll
-                for (int m = 0; m < kQU; ++m) {
+                for (int m = 0; m < kQHeld; ++m) {
                     qf[2 * m] = __ldg(q4 + 2 * (bt + m * kGroup));
                     qf[2 * m + 1] = __ldg(q4 + 2 * (bt + m * kGroup) + 1);
                 }
+#pragma unroll
+                for (int m = kQHeld; m < kQU; ++m)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(q4 + 2 * (bt + m * kGroup)));
             }
             const float wv = bt < kH ? __ldg(p.w + (int64_t)row * kH + bt) : 0.f;
             int bv = 0;
@@ -254,7 +268,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 } else if (MODE == kCoarse) {
                     n = Np / p.b;
                     base = p.means_off[bq];
-                    if (p.means_off[bq + 1] - base < n || n > n_cap) {
+                    if (!means_ok(p.means_off, bq, n, p.means_rows) || n > n_cap) {
                         st = 1;
                         flag(p.status, HISA_DEV_BAD_OFFSETS);
                     }
@@ -288,16 +302,25 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                     *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(0, u >> 4, u & 15, NQ)) = qh[m];
                 }
             } else {
-#pragma unroll
-                for (int m = 0; m < kQU; ++m) {
+                auto put = [&](int m, const float4 &a, const float4 &b) {
                     const int u = bt + m * kGroup;
-                    const float x[8] = {qf[2 * m].x,     qf[2 * m].y,     qf[2 * m].z,     qf[2 * m].w,
-                                        qf[2 * m + 1].x, qf[2 * m + 1].y, qf[2 * m + 1].z, qf[2 * m + 1].w};
+                    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
                     uint4 pl[3];
                     split3(x, pl);
 #pragma unroll
                     for (int k = 0; k < 3; ++k)
                         *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(k, u >> 4, u & 15, NQ)) = pl[k];
+                };
+#pragma unroll
+                for (int m = 0; m < kQHeld; ++m) put(m, qf[2 * m], qf[2 * m + 1]);
+                if (kHalves) {
+#pragma unroll
+                    for (int m = kQHeld; m < kQU; ++m) {
+                        qf[2 * (m - kQHeld)] = __ldg(q4 + 2 * (bt + m * kGroup));
+                        qf[2 * (m - kQHeld) + 1] = __ldg(q4 + 2 * (bt + m * kGroup) + 1);
+                    }
+#pragma unroll
+                    for (int m = kQHeld; m < kQU; ++m) put(m, qf[2 * (m - kQHeld)], qf[2 * (m - kQHeld) + 1]);
                 }
             }
             fence_async_smem();
@@ -334,6 +357,38 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             if (!ok)   // let the copies in flight land before the CTA can exit
                 for (uint32_t h = g > kFineSlots ? g - kFineSlots : 0; h < g; ++h)
                     mbar_wait(&bars[kBarFull + h % kFineSlots], (h / kFineSlots) & 1, 1u << 20);
+        }
+    } else if (MODE == kCoarse && warp == kWarpTma) {
+        // ---------------- coarse loader: block means by TMA ----------------
+        // Unit = one K half (64 dims) of one 128-row tile, into raw slot u % kRawSlots as two
+        // 128B-swizzled [128 rows x 32 dims] f32 boxes. Rows past the allocation read as 0;
+        // rows past the query's blocks are other data and never scored.
+        if (lane == 0) {
+            uint32_t u = 0;                                    // units issued
+            for (int i = 0; i < nql && ok; ++i) {
+                const int qb = i & 1;
+                if (!wait_bar(&bars[kBarMetaFull + qb], (i >> 1) & 1, abort)) { fail(); break; }
+                const QMeta &M = meta[qb];
+                const int T = M.state ? 0 : M.T;
+                for (int t = 0; t < T && ok; ++t) {
+                    for (int h = 0; h < 2; ++h, ++u) {
+                        const uint32_t slot = u % kRawSlots, use = u / kRawSlots;
+                        if (use >= 1 && !wait_bar(&bars[kBarEmpty + 1 + slot], (use - 1) & 1, abort)) {
+                            fail();
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bars[kBarFull + 1 + slot], kRawBytes);
+                        const int32_t y = (int32_t)(M.base + (int64_t)t * kM);
+#pragma unroll
+                        for (int c2 = 0; c2 < 2; ++c2)
+                            tma_load_2d(sbase + kOffReg + slot * kRawBytes + c2 * (kM * 128), &P.means_map,
+                                        h * 64 + c2 * 32, y, &bars[kBarFull + 1 + slot]);
+                    }
+                }
+            }
+            if (!ok)   // let the copies in flight land before the CTA can exit
+                for (uint32_t v = u > kRawSlots ? u - kRawSlots : 0; v < u; ++v)
+                    mbar_wait(&bars[kBarFull + 1 + v % kRawSlots], (v / kRawSlots) & 1, 1u << 20);
         }
     } else if (warp == kWarpMma) {
         // ---------------- MMA issue (warp-uniform loop, one elected lane issues) ----------
@@ -379,11 +434,10 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 } else {
                     bool good = true;
                     for (int h = 0; h < 2; ++h, ++u) {
-                        const uint32_t pb = u & 1;
-                        if (!wait_bar_warp(&bars[kBarFull + pb], (u >> 1) & 1, abort)) { good = false; break; }
+                        // one plane set: unit u is the (u + 1)-th phase of its barriers
+                        if (!wait_bar_warp(&bars[kBarFull], u & 1, abort)) { good = false; break; }
                         fence_after_sync();
-                        const uint64_t pd =
-                            smem_desc_sw128(sbase + kOffReg + 2 * kRawBytes + pb * kPlaneSet, 16, 1024);
+                        const uint64_t pd = smem_desc_sw128(sbase + kOffPlanes, 16, 1024);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t kb = kk * 32;
@@ -393,7 +447,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                             mma_bf16_warp(d, desc_add(pd, kHalfPlane + kb), bq, id_two, 1u);
                             mma_bf16_warp(d, desc_add(pd, 2 * kHalfPlane + kb), bq, id_one, 1u);
                         }
-                        mma_commit_warp(&bars[kBarEmpty + pb]);
+                        mma_commit_warp(&bars[kBarEmpty]);
                     }
                     if (!good) { fail(); break; }
                 }
@@ -484,104 +538,56 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             if (st == 0) mbar_arrive(&bars[kBarSlotFree + qb]);
         }
     }
-    else if (MODE == kCoarse && warp >= kWarpCvt && warp < kWarpCvt + 4) {
+    else if (MODE == kCoarse && warp >= kWarpCvt && warp < kWarpCvt + kCvtWarps) {
         // ---------------- converters: f32 means -> three bf16 planes ----------------------
-        // Unit = one K half (64 dims) of one 128-row tile. Each thread copies its own
-        // 8 x 32 bytes of a unit with cp.async into a private, conflict-free spot of one of
-        // two raw buffers (two units in flight), then splits them into the plane set the
-        // MMA reads. Thread ct owns pairs p = m * 128 + ct: row p / 8, dims (p % 8) * 8.
+        // Thread ct converts the 16-byte pieces c = m * kCvtThreads + ct (m < 8) of a raw
+        // unit: box c / 1024, row (c % 1024) / 8, dims 32 (c / 1024) + 4 (c % 8) .. + 3; a warp
+        // reads four whole swizzled rows (no bank conflict).
+        constexpr int kChunks = kM * 16 / kCvtThreads;          // 8
         const int ct = tid - kWarpCvt * 32;
-        const float *means = reinterpret_cast<const float *>(p.rows);
-        int ui = 0, ut = 0, uh = 0, uT = -2;               // next unit to hand out
-        // Next unit in MMA order (valid queries, tiles, halves): 1 = got one, 0 = none,
-        // 2 = its query's meta is not written yet (only when may_wait is false), -1 = timeout.
-        // A thread may block on a later query's meta only once every unit it has copied is
-        // converted: that meta waits for the select of an earlier query, which waits for
-        // those units.
-        auto next_unit = [&](int &oi, int &ot, int &oh, bool may_wait) -> int {
-            while (ui < nql) {
-                if (uT == -2) {
-                    uint64_t *mb = &bars[kBarMetaFull + (ui & 1)];
-                    const uint32_t ph = (ui >> 1) & 1;
-                    if (!may_wait) {
-                        if (!mbar_try_wait(mb, ph)) return 2;
-                    } else if (!wait_bar(mb, ph, abort)) {
-                        return -1;
+        uint32_t u = 0;                                        // units converted
+        for (int i = 0; i < nql && ok; ++i) {
+            const int qb = i & 1;
+            if (!wait_bar(&bars[kBarMetaFull + qb], (i >> 1) & 1, abort)) { fail(); break; }
+            const QMeta &M = meta[qb];
+            const int nunits = M.state ? 0 : 2 * M.T;
+            for (int e = 0; e < nunits; ++e, ++u) {
+                const uint32_t slot = u % kRawSlots;
+                if (!wait_bar(&bars[kBarFull + 1 + slot], (u / kRawSlots) & 1, abort) ||
+                    (u >= 1 && !wait_bar(&bars[kBarEmpty], (u - 1) & 1, abort))) {
+                    fail();
+                    break;
+                }
+                const uint8_t *rawb = smem + kOffReg + slot * kRawBytes;
+                uint8_t *planes = smem + kOffPlanes;
+#pragma unroll
+                for (int m = 0; m < kChunks; ++m) {
+                    const int c = m * kCvtThreads + ct, bx = c >> 10, r = (c >> 3) & 127, v = c & 7;
+                    const float4 a = *reinterpret_cast<const float4 *>(
+                        rawb + bx * (kM * 128) + r * 128 + ((v ^ (r & 7)) << 4));
+                    uint32_t w[3][2];
+                    float x0 = a.x, x1 = a.y, x2 = a.z, x3 = a.w;
+#pragma unroll
+                    for (int k = 0; k < 3; ++k) {
+                        const __nv_bfloat162 b0 = __floats2bfloat162_rn(x0, x1);
+                        const __nv_bfloat162 b1 = __floats2bfloat162_rn(x2, x3);
+                        w[k][0] = *reinterpret_cast<const uint32_t *>(&b0);
+                        w[k][1] = *reinterpret_cast<const uint32_t *>(&b1);
+                        if (k < 2) {
+                            const float2 f0 = __bfloat1622float2(b0), f1 = __bfloat1622float2(b1);
+                            x0 -= f0.x; x1 -= f0.y; x2 -= f1.x; x3 -= f1.y;
+                        }
                     }
-                    const QMeta &M = meta[ui & 1];
-                    uT = M.state ? 0 : M.T;
-                    ut = 0;
-                    uh = 0;
+                    const uint32_t off = sw128_offset((uint32_t)r, (uint32_t)(bx * 32 + v * 4));
+#pragma unroll
+                    for (int k = 0; k < 3; ++k)
+                        *reinterpret_cast<uint2 *>(planes + k * kHalfPlane + off) = make_uint2(w[k][0], w[k][1]);
                 }
-                if (ut < uT) {
-                    oi = ui; ot = ut; oh = uh;
-                    if (++uh == 2) { uh = 0; ++ut; }
-                    return 1;
-                }
-                ++ui;
-                uT = -2;
-            }
-            return 0;
-        };
-        auto issue = [&](int i, int t, int h, uint32_t buf) {
-            const QMeta &M = meta[i & 1];
-            const uint32_t dst0 = sbase + kOffReg + buf * kRawBytes;
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int pp = m * kGroup + ct, r = pp >> 3, g8 = pp & 7;
-                const int c = t * kM + r;
-                const bool valid = c < M.n;
-                const float *src = means + (M.base + (valid ? c : 0)) * kD + h * 64 + g8 * 8;
-                cp_async16_zfill(dst0 + ((2 * m) * kGroup + ct) * 16u, src, valid);
-                cp_async16_zfill(dst0 + ((2 * m + 1) * kGroup + ct) * 16u, src + 4, valid);
-            }
-            cp_async_commit();
-        };
-        // unit u lives in raw buffer u & 1; have0 = unit u (copied), have1 = unit u + 1
-        // (1 copied, 0 none, 2 not known yet)
-        int i0 = 0, t0 = 0, h0 = 0, i1 = 0, t1 = 0, h1 = 0;
-        int have0 = next_unit(i0, t0, h0, true), have1 = 0;
-        if (have0 < 0) fail();
-        if (have0 == 1) {
-            issue(i0, t0, h0, 0);
-            have1 = next_unit(i1, t1, h1, false);
-            if (have1 == 1) issue(i1, t1, h1, 1);
-        }
-        for (uint32_t u = 0; have0 == 1 && ok; ++u) {
-            if (have1 == 1) cp_async_wait_group<1>(); else cp_async_wait_group<0>();
-            const uint32_t pb = u & 1;
-            if (u >= 2 && !wait_bar(&bars[kBarEmpty + pb], ((u >> 1) - 1) & 1, abort)) { fail(); break; }
-            const uint8_t *rawb = smem + kOffReg + (u & 1) * kRawBytes;
-            uint8_t *planes = smem + kOffReg + 2 * kRawBytes + pb * kPlaneSet;
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int pp = m * kGroup + ct, r = pp >> 3, g8 = pp & 7;
-                const float4 a = *reinterpret_cast<const float4 *>(rawb + ((2 * m) * kGroup + ct) * 16);
-                const float4 b = *reinterpret_cast<const float4 *>(rawb + ((2 * m + 1) * kGroup + ct) * 16);
-                const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                uint4 pl[3];
-                split3(x, pl);
-                const uint32_t off = sw128_offset((uint32_t)r, (uint32_t)g8 * 8u);
-#pragma unroll
-                for (int k = 0; k < 3; ++k) *reinterpret_cast<uint4 *>(planes + k * kHalfPlane + off) = pl[k];
-            }
-            fence_async_smem();
-            mbar_arrive(&bars[kBarFull + pb]);
-            // every copied unit is converted now except unit u + 1
-            if (have1 == 2) {                      // unit u + 1 was not known: every unit
-                have1 = next_unit(i1, t1, h1, true);   // copied so far is converted, so wait
-                if (have1 < 0) { fail(); break; }
-                if (have1 == 1) issue(i1, t1, h1, (u + 1) & 1);
-            }
-            have0 = have1;
-            i0 = i1; t0 = t1; h0 = h1;
-            have1 = 0;
-            if (have0 == 1) {                      // refill buffer u & 1 with unit u + 2
-                have1 = next_unit(i1, t1, h1, false);
-                if (have1 == 1) issue(i1, t1, h1, u & 1);
+                fence_async_smem();
+                mbar_arrive(&bars[kBarFull]);
+                mbar_arrive(&bars[kBarEmpty + 1 + slot]);
             }
         }
-        cp_async_wait_all();
     }
 
     if (!ok) flag(p.status, HISA_DEV_TIMEOUT);
@@ -639,6 +645,9 @@ cudaError_t launch_score_pipe(const ScoreTcParams &p_in, cudaStream_t s) {
     if (p.s.B * p.s.L == 0) return cudaSuccess;
     if (p.s.mode == kFine &&
         !encode_bf16_map(&p.keys_map, p.s.rows, (uint64_t)p.s.keys_rows, kD, 64, 64))
+        return cudaErrorInvalidValue;
+    if (p.s.mode == kCoarse &&
+        !encode_f32_map(&p.means_map, p.s.rows, (uint64_t)p.s.means_rows, kD, 32, kM))
         return cudaErrorInvalidValue;
     const bool qb = p.s.q_bf16 != 0;
     switch (p.s.mode) {

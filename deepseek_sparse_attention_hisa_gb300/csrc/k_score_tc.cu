@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_score_tc(const __grid_constant_
             st = 1;
             flag(p.status, HISA_DEV_GATE);
         } else if (MODE == kCoarse &&
-                   (p.means_off[bq + 1] - p.means_off[bq] < Np / p.b || Np / p.b > kMaxSel)) {
+                   (!means_ok(p.means_off, bq, Np / p.b, p.means_rows) || Np / p.b > kMaxSel)) {
             st = 1;
             flag(p.status, HISA_DEV_BAD_OFFSETS);
         } else if (MODE == kFine) {

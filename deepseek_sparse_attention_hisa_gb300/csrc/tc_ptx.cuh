@@ -203,6 +203,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// One thread: copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// to shared memory, counted in bytes on mbar.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(mbar))
+        : "memory");
+}
+
 // ---- cp.async (16-byte global -> shared copies) ---------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void *g) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(saddr), "l"(g) : "memory");

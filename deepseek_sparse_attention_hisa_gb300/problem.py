@@ -49,7 +49,7 @@ class Problem:
         self.idesc = hb.IndexDesc(
             B=wl.B, L=wl.L, H_i=wl.H_i, D_i=wl.D_i, r=wl.r, index_topk=wl.index_topk,
             index_block=self.b, index_keep=self.keep, Np_max=self.Np_max,
-            keys_rows=int(self.keys.shape[0]),
+            keys_rows=int(self.keys.shape[0]), means_rows=0,
             q_dtype=hb.dtype_code(self.q_idx), k_dtype=hb.dtype_code(self.keys))
         nb = Np // self.b if self.b > 0 else np.zeros_like(Np)
         self.nb = nb
@@ -58,6 +58,7 @@ class Problem:
         self.means_off = _i64(means_off, dev)
         self.means = torch.zeros((max(int(means_off[-1]), 1), wl.D_i), dtype=torch.float32,
                                  device=dev)
+        self.idesc.means_rows = int(self.means.shape[0])
         rows = wl.B * wl.L
         self.top_blk = torch.full((rows, max(self.keep, 1)), -7, dtype=torch.int32, device=dev)
         self.I = torch.full((rows, self.k), -7, dtype=torch.int32, device=dev)

@@ -69,7 +69,7 @@ typedef enum {
 typedef enum { HISA_F32 = 0, HISA_BF16 = 1 } hisa_dtype;
 
 /* Bits of the device status word. */
-#define HISA_DEV_BAD_OFFSETS 0x1u /* offsets not monotone, past keys_rows / kv_rows, Np_b > Np_max,
+#define HISA_DEV_BAD_OFFSETS 0x1u /* offsets not monotone, past keys_rows / means_rows / kv_rows, Np_b > Np_max,
                                     or a capacity too small; the sequence is skipped */
 #define HISA_DEV_GATE        0x2u /* a sequence failed Np_b >= index_block*index_keep; rows are -1 */
 #define HISA_DEV_BAD_ID      0x4u /* a selected id outside [-1, Np_b) reached the combine; skipped */
@@ -97,6 +97,8 @@ typedef struct {
     int32_t index_keep;   /* keep: blocks kept by the coarse stage */
     int64_t Np_max;       /* an upper bound of Np_b over the batch (sizes grids and workspace) */
     int64_t keys_rows;    /* rows allocated in keys (>= key_off[B]); no key read goes past it */
+    int64_t means_rows;   /* rows allocated in the block-mean array; no block-mean read or
+                             write goes past it (0 for calls that take no means) */
     int32_t q_dtype;      /* hisa_dtype of q: HISA_F32 or HISA_BF16 */
     int32_t k_dtype;      /* hisa_dtype of the pooled indexer keys */
 } hisa_index_desc;

@@ -80,9 +80,9 @@ def test_struct_layout_matches_c():
 #include <stddef.h>
 #include "hisa.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu\n", sizeof(hisa_index_desc), offsetof(hisa_index_desc, Np_max),
-         offsetof(hisa_index_desc, keys_rows), offsetof(hisa_index_desc, q_dtype),
-         offsetof(hisa_index_desc, k_dtype));
+  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(hisa_index_desc), offsetof(hisa_index_desc, Np_max),
+         offsetof(hisa_index_desc, keys_rows), offsetof(hisa_index_desc, means_rows),
+         offsetof(hisa_index_desc, q_dtype), offsetof(hisa_index_desc, k_dtype));
   printf("%zu %zu %zu %zu %zu %zu\n", sizeof(hisa_attn_desc), offsetof(hisa_attn_desc, Np_max),
          offsetof(hisa_attn_desc, kv_rows), offsetof(hisa_attn_desc, scale),
          offsetof(hisa_attn_desc, q_dtype), offsetof(hisa_attn_desc, kv_dtype));
@@ -98,15 +98,16 @@ int main(void) {
     i = [int(x) for x in lines[0].split()]
     a = [int(x) for x in lines[1].split()]
     assert i == [ctypes.sizeof(hb.IndexDesc), hb.IndexDesc.Np_max.offset,
-                 hb.IndexDesc.keys_rows.offset, hb.IndexDesc.q_dtype.offset,
-                 hb.IndexDesc.k_dtype.offset]
+                 hb.IndexDesc.keys_rows.offset, hb.IndexDesc.means_rows.offset,
+                 hb.IndexDesc.q_dtype.offset, hb.IndexDesc.k_dtype.offset]
     assert a == [ctypes.sizeof(hb.AttnDesc), hb.AttnDesc.Np_max.offset, hb.AttnDesc.kv_rows.offset,
                  hb.AttnDesc.scale.offset, hb.AttnDesc.q_dtype.offset, hb.AttnDesc.kv_dtype.offset]
 
 
 def v4_index_desc(**kw):
     d = dict(B=1, L=1, H_i=64, D_i=128, r=4, index_topk=512, index_block=64, index_keep=16,
-             Np_max=32768, keys_rows=32768, q_dtype=hb.HISA_F32, k_dtype=hb.HISA_BF16)
+             Np_max=32768, keys_rows=32768, means_rows=512, q_dtype=hb.HISA_F32,
+             k_dtype=hb.HISA_BF16)
     d.update(kw)
     return hb.IndexDesc(**d)
 
