@@ -11,7 +11,9 @@
 // K = V, so the same staged tile is the B operand of the first product (K-major) and the
 // A operand of the second (MN-major). The running max m is lazy: O^T and l are rescaled
 // only when a tile's max exceeds m by more than 8 (log2 units), so p <= 256.
-// Warp roles: 0-3 softmax + epilogue (warp w reads TMEM lanes 32w..32w+31), 4 MMA issue
+// Warp roles: 0-3 softmax + epilogue (warp w reads TMEM lanes 32w..32w+31; in the softmax
+// the two halves of a warp split each head's tile rows), 4 S = Q.K^T issue, 7 O += V^T.P^T
+// issue (two issuing warps, so that neither product waits behind the other), 4 MMA issue
 // and TMEM owner, 5-6 producers (cp.async gather, 128-byte swizzle, zero-fill of rows
 // that are invisible or past the list). Every mbarrier wait is bounded; a timeout sets
 // HISA_DEV_TIMEOUT, raises a shared abort flag and the CTA drains and exits.
@@ -25,8 +27,8 @@ using namespace tc;
 
 constexpr int kH = 64, kDH = 512, kTR = 32, kSlots = 4;
 constexpr int kRPL = kTR / 32;                        // tile rows per producer lane
-constexpr int kSoftWarps = 4, kMmaWarp = 4, kProdWarp0 = 5, kProdWarps = 2;
-constexpr int kThreads = 32 * (kSoftWarps + 1 + kProdWarps);
+constexpr int kSoftWarps = 4, kMmaWarp = 4, kProdWarp0 = 5, kProdWarps = 2, kPvWarp = 7;
+constexpr int kThreads = 32 * (kSoftWarps + 1 + kProdWarps + 1);
 constexpr uint32_t kQBytes = kH * kDH * 2;            // 64 KiB, K-major, 8 chunks of 64 dims
 constexpr uint32_t kSlotBytes = kTR * kDH * 2;        // 32 KiB per staged tile
 constexpr uint32_t kPBytes = kH * 128;                // P^T: 64 heads x 64 rows bf16
@@ -54,11 +56,7 @@ struct Misc {
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    for (uint32_t i = 0; i < (1u << 22); ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && *abort) return false;
-    }
-    return false;
+    return mbar_wait_abortable(bar, parity, abort);
 }
 
 // A wait taken by a whole warp; the result is made warp-uniform.
@@ -130,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             if (b == kBarSFree || b == kBarSFree + 1 || b == kBarPFull || b == kBarPFull + 1)
                 cnt = kSoftWarps * 32;
             if (b == kBarQ) cnt = kProdWarps * 32;
+            if (b == kBarDrain) cnt = 2;                  // one commit from each issuing warp
             mbar_init(&bars[b], cnt);
         }
         mbar_fence_init();
@@ -145,42 +144,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
     fence_after_sync();
     const uint32_t tmem = misc->tmem;
 
-    if (warp >= kProdWarp0) {
+    if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
         // ---------------- producers ----------------
         const int pt = tid - kProdWarp0 * 32;                 // 0..63: one 16-byte unit per row
+        int32_t *ids = reinterpret_cast<int32_t *>(smem + kOffIds);
+        const int64_t kk0 = e0 > nloc ? e0 - nloc : 0;
+        const int64_t kk1 = e1 > nloc ? e1 - nloc : 0;
+        // the first 512 selected ids of this CTA's range, fetched now, staged after the
+        // local-window tiles are on their way
+        int32_t pre[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int64_t kk = kk0 + pt + 64 * m;
+            pre[m] = (Irow && kk < kk1) ? Irow[kk] : -1;
+        }
         const uint32_t qb = sbase + kOffQ;
         const __nv_bfloat16 *qrow = reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)row * kH * kDH;
         for (int h = 0; h < kH; ++h)
             cp_async16(qb + (pt >> 3) * (kH * 128) + sw128_offset(h, (pt & 7) * 8),
                        qrow + h * kDH + pt * 8);
         cp_async_arrive(&bars[kBarQ]);
-        // the selected ids of this CTA's range, staged once (8 loads in flight per thread)
-        int32_t *ids = reinterpret_cast<int32_t *>(smem + kOffIds);
-        const int64_t kk0 = e0 > nloc ? e0 - nloc : 0;
-        const int64_t kk1 = e1 > nloc ? e1 - nloc : 0;
-        if (Irow) {
-            for (int64_t base = kk0; base < kk1; base += 8 * 64) {
-                int32_t v[8];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int64_t kk = base + pt + 64 * m;
-                    v[m] = kk < kk1 ? Irow[kk] : -1;
-                }
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int64_t kk = base + pt + 64 * m;
-                    if (kk < kk1) ids[kk - kk0] = v[m];
-                }
-            }
-        }
-        asm volatile("bar.sync 2, 64;" ::: "memory");    // the two producer warps
-        bool ok = true;
-        for (int i = 0; i < T && ok; ++i) {
+        // gathers tile i into slot i % kSlots (the slot must be free)
+        auto issue_tile = [&](int i) {
             const int s = i % kSlots;
-            if (i >= kSlots && !wait_bar(&bars[kBarEmpty + s], ((i / kSlots) - 1) & 1, abort)) {
-                ok = false;
-                break;
-            }
             // lane r resolves rows r, r + 32, ... of the tile
             const __nv_bfloat16 *src[kRPL];
             uint32_t valid[kRPL];
@@ -221,14 +207,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             }
             cp_async_arrive(&bars[kBarFull + s]);
             if (pt == 0) mbar_arrive(&bars[kBarFull + s]);
+        };
+        // leading tiles with local rows only go out before the ids are staged
+        int n_pre = 0;
+        while (n_pre < T && n_pre < kSlots) {
+            const int64_t end = e0 + (int64_t)(n_pre + 1) * kTR;
+            if ((end < e1 ? end : e1) > nloc) break;
+            issue_tile(n_pre++);
+        }
+        if (Irow) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int64_t kk = kk0 + pt + 64 * m;
+                if (kk < kk1) ids[kk - kk0] = pre[m];
+            }
+            for (int64_t base = kk0 + 8 * 64; base < kk1; base += 8 * 64) {
+                int32_t v[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int64_t kk = base + pt + 64 * m;
+                    v[m] = kk < kk1 ? Irow[kk] : -1;
+                }
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int64_t kk = base + pt + 64 * m;
+                    if (kk < kk1) ids[kk - kk0] = v[m];
+                }
+            }
+        }
+        asm volatile("bar.sync 2, 64;" ::: "memory");    // the two producer warps
+        bool ok = true;
+        for (int i = n_pre; i < T; ++i) {
+            const int s = i % kSlots;
+            if (i >= kSlots && !wait_bar(&bars[kBarEmpty + s], ((i / kSlots) - 1) & 1, abort)) {
+                ok = false;
+                break;
+            }
+            issue_tile(i);
         }
         cp_async_wait_all();
         if (!ok) {
             *abort = 1;
             flag(p.status, HISA_DEV_TIMEOUT);
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issue (warp-uniform loop, one elected lane issues) -------
+    } else if (warp == kMmaWarp || warp == kPvWarp) {
+        // ---------------- MMA issue (warp-uniform loops, one elected lane issues) ------
         if (T > 0) {
             const uint32_t id_s = idesc_bf16_f32(64, kTR, 0, 0);   // N = kTR rows
             const uint32_t id_o = idesc_bf16_f32(128, 64, 1, 0);
@@ -267,26 +290,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 mma_commit_warp(&bars[kBarPFree + pb]);
                 return true;
             };
-            if (ok) ok = issue_s(0);
-            for (int i = 1; i < T && ok; ++i) {
-                ok = issue_s(i);
-                if (ok) ok = issue_pv(i - 1);
-            }
-            if (ok) ok = issue_pv(T - 1);
+            if (warp == kMmaWarp)
+                for (int i = 0; i < T && ok; ++i) ok = issue_s(i);
+            else
+                for (int i = 0; i < T && ok; ++i) ok = issue_pv(i);
             if (!ok) {
                 *abort = 1;
                 flag(p.status, HISA_DEV_TIMEOUT);
             }
-            // drain: every MMA issued by this thread has completed before TMEM is freed
+            // drain: every MMA issued by either warp has completed before TMEM is freed
+            // (a bounded wait that an abort does not cut short)
             mma_commit_warp(&bars[kBarDrain]);
-            wait_bar_warp(&bars[kBarDrain], 0, abort);
+            __syncwarp();
+            mbar_wait(&bars[kBarDrain], 0, 1u << 24);
+            __syncwarp();
         }
     } else {
         // ---------------- softmax + epilogue (warps 0-3) ----------------
-        const bool active = lane < 16;
-        const int h = warp * 16 + lane;                 // head owned by this lane (M = 64 layout)
+        // S rows (heads) live in TMEM lanes 0-15 of each quadrant (M = 64). Lane l of warp w
+        // owns head 16 w + (l % 16) and the tile rows 16 (l / 16) .. + 15: the two lanes of a
+        // head combine their max and sum with one shuffle.
+        const bool lead = lane < 16;                    // writes the head's shared values
+        const int h = warp * 16 + (lane & 15);
+        const int half = lane >> 4;
         const float c2 = p.scale * kLog2e;
-        const float sink2 = active ? p.sinks[h] * kLog2e : 0.f;
+        const float sink2 = p.sinks[h] * kLog2e;
         float m2 = -INFINITY, l = 0.f;
         uint32_t pfree_seen[2] = {0u, 0u};
         bool ok = true;
@@ -297,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             }
             return true;
         };
+        constexpr int kHR = kTR / 2;                    // rows per lane
         for (int i = 0; i < T && ok; ++i) {
             const int s = i % kSlots, sb = i & 1;
             if (!wait_bar(&bars[kBarFull + s], (i / kSlots) & 1, abort) ||
@@ -305,34 +334,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 break;
             }
             fence_after_sync();
-            const uint64_t mask = misc->mask[s];
-            float v[kTR];
-            {
-                float a[4][16];
-                const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + sb * kTR;
-#pragma unroll
-                for (int c = 0; c < kTR / 16; ++c) tmem_ld16(ta + c * 16, a[c]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < kTR / 16; ++c)
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) v[c * 16 + r] = a[c][r];
-            }
+            const uint32_t mask = (uint32_t)(misc->mask[s] >> (kHR * half));
+            float v[kHR];
+            tmem_ld16_x2(tmem + ((uint32_t)(32 * warp) << 16) + sb * kTR, v);
+            tmem_ld_wait();
             fence_before_sync();
             mbar_arrive(&bars[kBarSFree + sb]);
 #pragma unroll
-            for (int r = 0; r < kTR; ++r) v[r] = ((mask >> r) & 1ull) ? v[r] * c2 : -INFINITY;
-            float mx[kTR / 2];                              // pairwise tree: short dependency chains
+            for (int r = 0; r < kHR; ++r) v[r] = ((mask >> r) & 1u) ? v[r] * c2 : -INFINITY;
+            float mx[kHR / 2];                              // pairwise tree: short dependency chains
 #pragma unroll
-            for (int r = 0; r < kTR / 2; ++r) mx[r] = fmaxf(v[2 * r], v[2 * r + 1]);
+            for (int r = 0; r < kHR / 2; ++r) mx[r] = fmaxf(v[2 * r], v[2 * r + 1]);
 #pragma unroll
-            for (int w = kTR / 4; w >= 1; w >>= 1)
+            for (int w = kHR / 4; w >= 1; w >>= 1)
 #pragma unroll
                 for (int r = 0; r < w; ++r) mx[r] = fmaxf(mx[r], mx[r + w]);
-            const float tmax = mx[0];
+            const float tmax = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], 16));
             float alpha = 1.f;
             uint32_t resc = 0;
-            if (active && tmax > m2 + kLazy) {
+            if (tmax > m2 + kLazy) {
                 if (m2 != -INFINITY) {
                     alpha = ex2_approx(m2 - tmax);
                     resc = 1;
@@ -342,33 +362,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             // exp2(-inf - m) = +0 in the hardware approximation; m2 is finite once any row
             // of this head was visible, and rows are only ever -inf when masked
             const float msub = m2 == -INFINITY ? 0.f : m2;
-            float pr[kTR];
+            float pr[kHR];
 #pragma unroll
-            for (int r = 0; r < kTR; ++r) pr[r] = ex2_approx(v[r] - msub);
-            uint32_t packed[kTR / 2];
+            for (int r = 0; r < kHR; ++r) pr[r] = ex2_approx(v[r] - msub);
+            uint32_t packed[kHR / 2];
 #pragma unroll
-            for (int r = 0; r < kTR; r += 2) {
+            for (int r = 0; r < kHR; r += 2) {
                 __nv_bfloat162 b2 = __floats2bfloat162_rn(pr[r], pr[r + 1]);
                 packed[r / 2] = *reinterpret_cast<uint32_t *>(&b2);
             }
 #pragma unroll
-            for (int w = kTR / 2; w >= 1; w >>= 1)
+            for (int w = kHR / 2; w >= 1; w >>= 1)
 #pragma unroll
                 for (int r = 0; r < w; ++r) pr[r] += pr[r + w];
-            const float sum = pr[0];
+            const float sum = pr[0] + __shfl_xor_sync(0xffffffffu, pr[0], 16);
             // P buffer (i & 1) is free once PV(i - 2) has completed
             if (i >= 2 && !wait_pfree(i & 1, (uint32_t)((i >> 1) - 1))) { ok = false; break; }
             l = l * alpha + sum;
-            if (active) {
+            {
                 uint8_t *pb = smem + kOffP + (i & 1) * kPBytes;
 #pragma unroll
-                for (int u = 0; u < kTR / 8; ++u)
-                    *reinterpret_cast<uint4 *>(pb + sw128_offset(h, u * 8)) =
+                for (int u = 0; u < kHR / 8; ++u)
+                    *reinterpret_cast<uint4 *>(pb + sw128_offset(h, (half * (kHR / 8) + u) * 8)) =
                         make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
             }
             if (named_or_soft(resc)) {
                 // rescale O^T columns of the heads whose reference max moved up
-                if (active) misc->alpha[h] = alpha;
+                if (lead) misc->alpha[h] = alpha;
                 named_sync_soft();
                 if (!wait_pfree((i - 1) & 1, (uint32_t)((i - 1) >> 1))) { ok = false; break; }
                 fence_after_sync();
@@ -399,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
         fence_after_sync();
         const bool have_o = ok && T > 0;
         if (p.nsplit == 1) {
-            if (active) {
+            if (lead) {
                 const float M = fmaxf(m2, sink2);
                 const float wm = (m2 == -INFINITY) ? 0.f : exp2f(m2 - M);
                 misc->factor[h] = wm / (l * wm + exp2f(sink2 - M));
@@ -423,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             }
         } else {
             float *base = p.part + ((int64_t)row * p.nsplit + split) * kH * (kDH + 2);
-            if (active) {
+            if (lead) {
                 base[h * (kDH + 2)] = (m2 == -INFINITY) ? -INFINITY : m2 / kLog2e;
                 base[h * (kDH + 2) + 1] = l;
             }

@@ -133,6 +133,21 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 16 lanes x 2 halves: threads 0-15 read columns [c, c + 16) of TMEM lanes base + 0..15,
+// threads 16-31 columns [c + 16, c + 32) of the same lanes (for M = 64 accumulators,
+// whose rows live in lanes 0-15 of each 32-lane quadrant).
+__device__ __forceinline__ void tmem_ld16_x2(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], 16;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -175,12 +190,40 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t *mbar, uint32_t parit
         : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
     return ok;
 }
-// Bounded wait: returns false (and leaves the phase unconsumed) after `limit` polls,
-// so a kernel can record an error and exit instead of hanging.
+// Non-blocking test of the same condition (try_wait may hold the thread for a while).
+__device__ __forceinline__ uint32_t mbar_test_wait(uint64_t *mbar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
+    return ok;
+}
+// A waiter gives up after about kWaitCycles SM cycles (a quarter second at 2 GHz), far
+// beyond any legitimate wait of these kernels, so a stuck pipeline ends promptly.
+constexpr long long kWaitCycles = 1ll << 29;
+
+// Bounded wait: returns false (and leaves the phase unconsumed) after `limit` polls or
+// kWaitCycles cycles, so a kernel can record an error and exit instead of hanging.
 __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity,
                                           uint32_t limit = (1u << 26)) {
-    for (uint32_t i = 0; i < limit; ++i)
+    const long long t0 = clock64();
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(mbar, parity)) return true;
+        if ((i & 255u) == 255u && clock64() - t0 > kWaitCycles) return false;
+    }
+    return false;
+}
+
+// The same, also giving up (every 256 polls) as soon as *abort is set.
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t *mbar, uint32_t parity,
+                                                    volatile int *abort) {
+    const long long t0 = clock64();
+    for (uint32_t i = 0; i < (1u << 26); ++i) {
+        if (mbar_try_wait(mbar, parity)) return true;
+        if ((i & 255u) == 255u && (*abort || clock64() - t0 > kWaitCycles)) return false;
+    }
     return false;
 }
 
