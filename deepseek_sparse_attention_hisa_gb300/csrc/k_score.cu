@@ -203,6 +203,62 @@ __global__ void k_block_means(MeansParams p) {
     }
 }
 
+// The same means, one block per pass with all of its b * D_i keys in flight at once: the
+// block is one contiguous run of keys, copied with 16-byte loads into shared memory as
+// f32, then each thread sums one dimension over the rows in row order (the same f32
+// additions, in the same order, as k_block_means).
+constexpr int kMeansThreads = 256;
+constexpr int kMeansStage = 8192;                      // f32 elements staged per block
+
+template <typename KT>
+__global__ void __launch_bounds__(kMeansThreads) k_block_means_staged(MeansParams p) {
+    __shared__ float stage[kMeansStage];
+    const int bq = blockIdx.y;
+    const int64_t k0 = p.key_off[bq];
+    const int64_t Np = p.key_off[bq + 1] - k0;
+    if (!seq_ok(p.key_off, bq, p.Np_max, p.keys_rows)) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
+        return;
+    }
+    const int64_t nb = Np / p.b;
+    const int64_t m0 = p.means_off[bq];
+    if (!means_ok(p.means_off, bq, nb, p.means_rows)) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
+        return;
+    }
+    int64_t fb = p.first_block ? (int64_t)p.first_block[bq] : 0;
+    if (fb < 0) fb = 0;
+    constexpr int kPer = 16 / (int)sizeof(KT);          // keys per 16-byte load
+    const int n = p.b * p.D_i;                          // keys of one block
+    const KT *keys = reinterpret_cast<const KT *>(p.keys);
+    const float inv_div = (float)p.b;
+    for (int64_t beta = fb + blockIdx.x; beta < nb; beta += gridDim.x) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(keys + (k0 + beta * p.b) * p.D_i);
+        for (int v = threadIdx.x; v < n / kPer; v += 4 * kMeansThreads) {
+            uint4 u[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                if (v + m * kMeansThreads < n / kPer) u[m] = __ldg(src + v + m * kMeansThreads);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int vv = v + m * kMeansThreads;
+                if (vv < n / kPer) {
+                    const KT *x = reinterpret_cast<const KT *>(&u[m]);
+#pragma unroll
+                    for (int e = 0; e < kPer; ++e) stage[vv * kPer + e] = to_f32(x[e]);
+                }
+            }
+        }
+        __syncthreads();
+        for (int d = threadIdx.x; d < p.D_i; d += kMeansThreads) {
+            float s = 0.f;
+            for (int i = 0; i < p.b; ++i) s += stage[i * p.D_i + d];
+            p.means[(m0 + beta) * p.D_i + d] = s / inv_div;
+        }
+        __syncthreads();
+    }
+}
+
 cudaError_t launch_block_means(const MeansParams &p, int64_t nb_max, cudaStream_t s) {
     if (nb_max <= 0) return cudaSuccess;
     // Blocks [first_block, nb) are walked grid-stride; size the grid from the batch so
@@ -211,6 +267,13 @@ cudaError_t launch_block_means(const MeansParams &p, int64_t nb_max, cudaStream_
     if (per_seq > nb_max) per_seq = nb_max;
     const unsigned gx = (unsigned)(per_seq < 1 ? 1 : per_seq);
     dim3 grid(gx, (unsigned)p.B);
+    if ((int64_t)p.b * p.D_i <= kMeansStage) {
+        if (p.keys_bf16)
+            k_block_means_staged<__nv_bfloat16><<<grid, kMeansThreads, 0, s>>>(p);
+        else
+            k_block_means_staged<float><<<grid, kMeansThreads, 0, s>>>(p);
+        return cudaGetLastError();
+    }
     const int threads = p.D_i;
     if (p.keys_bf16)
         k_block_means<__nv_bfloat16><<<grid, threads, 0, s>>>(p);
