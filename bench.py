@@ -350,7 +350,7 @@ def run_gpu(args, wl, R):
     build.build_library()
     hb.lib()
 
-    bwl = wl.replace(B=R)
+    bwl = wl.replace(B=R, Np=(int(args.Np),))
     data = inputs.generate_device(bwl, device=dev, seed=1000 + rank)
     prob = Problem(data, device=dev)
     nb = int(prob.nb[0])
@@ -471,9 +471,9 @@ def run_gpu(args, wl, R):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"v4flash_decode x R={R} independent sequences per GPU "
-                               f"(Np=32768 each, H_i=64x128, b=64, keep=16, k=512, "
+                               f"(Np={args.Np} each, H_i=64x128, b=64, keep=16, k=512, "
                                f"H=64x512 bf16, W=128)",
-                   "R": R, "Np": 32768, "l2": "256 MiB L2 flush between steps; "
+                   "R": R, "Np": int(args.Np), "l2": "256 MiB L2 flush between steps; "
                                                f"{step_bytes * R / 1e6:.0f} MB touched per step"},
         "step_hbm_gbs": step_bytes * R / (ms_per_step / 1e3) / 1e9,
         "step_bytes_per_query": step_bytes,
@@ -564,6 +564,8 @@ def main():
     ap.add_argument("--ref-queries", type=int, default=4, help="oracle queries per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill scoring leg")
+    ap.add_argument("--Np", type=int, default=32768,
+                    help="pooled rows per sequence (32768 = the V4-Flash 131072-token prefix)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

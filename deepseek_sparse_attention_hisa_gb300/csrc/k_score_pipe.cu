@@ -164,7 +164,14 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     using Lay = Layout<MODE>;
     const ScoreParams &p = P.s;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ SelectShared<kGroup> sel_sh;
+    constexpr int kAll = pipe_threads<MODE>();
+    // the select warps' state, and the whole CTA's for the last query (never both at once)
+    __shared__ union {
+        SelectShared<kGroup> group;
+        SelectShared<kAll> all;
+    } sel_u;
+    SelectShared<kGroup> &sel_sh = sel_u.group;
+    __shared__ int s_blk_raw[64];                       // kept blocks as read (fine)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t sbase = smem_u32(smem);
@@ -242,18 +249,32 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             const float wv = bt < kH ? __ldg(p.w + (int64_t)row * kH + bt) : 0.f;
             int bv = 0;
             if (MODE == kFine && bt < p.keep) bv = __ldg(p.top_blk + (int64_t)row * p.keep + bt);
+            // the offsets and position this row's checks need, fetched with q
+            const int64_t k0 = p.key_off[bq], k1 = p.key_off[bq + 1];
+            const int64_t t_row = p.causal ? (int64_t)p.t0[bq] + j : 0;
             // meta slot qb is free once query i - 2 is selected
             const bool w1 = i < 2 || wait_bar(&bars[kBarSlotFree + qb], ((i >> 1) - 1) & 1, abort);
             if (!group_all(kBarBld, kGroup, w1)) { fail(); break; }
             QMeta &M = meta[qb];
-            if (MODE == kFine && bt < p.keep) M.blk[bt] = bv;
+            const int64_t Np = k1 - k0;
+            if (MODE == kFine && bt < p.keep) s_blk_raw[bt] = bv;
             if (bt < kH) M.w[bt] = wv * p.head_scale;
             named_sync(kBarBld, kGroup);
+            bool bad_blk = false;
+            if (MODE == kFine && bt < p.keep) {
+                // kept blocks in ascending order: each thread places its own by rank
+                int rank = 0;
+                for (int u = 0; u < p.keep; ++u) {
+                    const int o = s_blk_raw[u];
+                    rank += (o < bv || (o == bv && u < bt)) ? 1 : 0;
+                }
+                M.blk[rank] = bv;
+                bad_blk = bv < 0 || (int64_t)bv >= Np / 64;
+            }
+            bad_blk = MODE == kFine && !group_all(kBarBld, kGroup, !bad_blk);
             bool w2 = true;
             if (bt == 0) {
                 int st = 0;
-                const int64_t k0 = p.key_off[bq];
-                const int64_t Np = p.key_off[bq + 1] - k0;
                 int64_t n = 0, base = k0;
                 if (!seq_ok(p.key_off, bq, p.Np_max, p.keys_rows)) {
                     st = 1;
@@ -270,22 +291,17 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                     }
                 } else {
                     n = (int64_t)p.keep * 64;
-                    for (int s = 1; s < p.keep; ++s) {   // insertion sort: ascending pos
-                        const int v = M.blk[s];
-                        int u = s;
-                        while (u > 0 && M.blk[u - 1] > v) { M.blk[u] = M.blk[u - 1]; --u; }
-                        M.blk[u] = v;
+                    if (bad_blk) {
+                        st = 1;
+                        flag(p.status, HISA_DEV_BAD_BLOCK);
                     }
-                    for (int s = 0; s < p.keep; ++s)
-                        if (M.blk[s] < 0 || (int64_t)M.blk[s] >= Np / 64) st = 1;
-                    if (st) flag(p.status, HISA_DEV_BAD_BLOCK);
                 }
                 M.row = row;
                 M.state = st;
                 M.n = (int)n;
                 M.T = (int)((n + kM - 1) / kM);
                 M.base = base;
-                M.V = p.causal ? visible_len((int64_t)p.t0[bq] + j, p.r, Np) : Np;
+                M.V = p.causal ? visible_len(t_row, p.r, Np) : Np;
                 mbar_arrive(&bars[kBarMetaFull + qb]);
                 // the q planes are free once the previous query's MMAs are done
                 w2 = i < 1 || wait_bar(&bars[kBarQEmpty], (i - 1) & 1, abort);
@@ -507,8 +523,9 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
         }
     } else if (warp >= kWarpSel && warp < kWarpSel + 4) {
         // ---------------- select: top-k of a finished query, beside the next one's stream ----
+        // (fine: the last query is selected by the whole CTA below, once every role is done)
         const int st = tid - kWarpSel * 32;
-        for (int i = 0; i < nql; ++i) {
+        for (int i = 0; i < nql - (MODE == kFine ? 1 : 0); ++i) {
             const int qb = i & 1;
             const int row = (int)blockIdx.x + i * (int)gridDim.x;
             const bool w = wait_bar(&bars[kBarScFull + qb], (i >> 1) & 1, abort);
@@ -592,6 +609,32 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     if (warp == kWarpMma) {
         fence_after_sync();
         tmem_dealloc(tmem, 512);
+    }
+    // ---------------- fine: the last query's top-k on every warp of the CTA ----------------
+    // Every role has left its loop, so the last query's scores are complete (or a wait
+    // gave up, and the row is written as -1). The coarse top-Kb is short and stays with
+    // the select warps, where it overlaps the other roles' tail.
+    if (MODE == kFine && nql > 0) {
+        const int i = nql - 1, qb = i & 1;
+        const int row = (int)blockIdx.x + i * (int)gridDim.x;
+        const QMeta &M = meta[qb];
+        const float *sc = scb + qb * n_cap;
+        int32_t *out = P.sel + (int64_t)row * P.k_sel;
+        const bool done = *abort == 0;
+        const int64_t kout = (M.state || !done) ? 0 : (M.n < P.k_sel ? M.n : P.k_sel);
+        if (kout > 0) {
+            if (MODE == kFine) {
+                const int *blk = M.blk;
+                small_topk<kAll, 0, 0>(
+                    sc, M.n, (int)kout, out,
+                    [blk](int64_t c) { return (int32_t)(blk[(int)c >> 6] * 64 + ((int)c & 63)); },
+                    sel_u.all, p.status);
+            } else {
+                small_topk<kAll, 0, 0>(sc, M.n, (int)kout, out, [](int64_t c) { return (int32_t)c; },
+                                       sel_u.all, p.status);
+            }
+        }
+        for (int64_t e = kout + tid; e < P.k_sel; e += kAll) out[e] = -1;
     }
 }
 
