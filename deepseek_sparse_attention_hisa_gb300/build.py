@@ -43,7 +43,7 @@ def _stamp() -> str:
                                 if f.endswith((".cuh", ".h")))
     files.append(os.path.join(INCLUDE, "hisa.h"))
     for f in files:
-        h.update(f.encode())
+        h.update(os.path.basename(f).encode())          # independent of where the tree lives
         with open(f, "rb") as fh:
             h.update(fh.read())
     h.update(" ".join(NVCC_FLAGS).encode())
