@@ -462,8 +462,8 @@ def run_gpu(args, wl, R):
     stage_avg = {n: statistics.mean(v) for n, v in stage_ms.items()}
     dom = max(stage_avg, key=stage_avg.get)
     achieved = per_stage_bytes[dom] * R / (stage_avg[dom] / 1e3) / 1e9
-    kernel_of = {"block_means": "k_block_means", "block_filter": "k_score_tc (coarse)",
-                 "select_topk": "k_score_tc (fine)", "sparse_attend": "k_attend_tc"}
+    kernel_of = {"block_means": "k_block_means_staged", "block_filter": "k_score_pipe (coarse)",
+                 "select_topk": "k_score_pipe (fine)", "sparse_attend": "k_attend_tc"}
     traffic = traffic_from_profile(kernel_of[dom])
 
     line = {
