@@ -27,18 +27,22 @@ using namespace tc;
 
 constexpr int kH = 64, kDH = 512, kTR = 32, kSlots = 4;
 constexpr int kRPL = kTR / 32;                        // tile rows per producer lane
-constexpr int kSoftWarps = 4, kMmaWarp = 4, kProdWarp0 = 5, kProdWarps = 2, kPvWarp = 7;
+constexpr int kSoftWarps = 4, kMmaWarp = 4, kProdWarp0 = 5, kProdWarps = 4;
+constexpr int kPvWarp = kProdWarp0 + kProdWarps;
+constexpr int kProdThreads = 32 * kProdWarps;
 constexpr int kThreads = 32 * (kSoftWarps + 1 + kProdWarps + 1);
 constexpr uint32_t kQBytes = kH * kDH * 2;            // 64 KiB, K-major, 8 chunks of 64 dims
 constexpr uint32_t kSlotBytes = kTR * kDH * 2;        // 32 KiB per staged tile
 constexpr uint32_t kPBytes = kH * 128;                // P^T: 64 heads x 64 rows bf16
+constexpr int kPBufs = 3;                              // P tiles in flight (softmax ahead of PV)
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kQBytes;
 constexpr uint32_t kOffP = kOffKV + kSlots * kSlotBytes;
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffBar = kOffP + kPBufs * kPBytes;
 // barriers: full[4] empty[4] s_full[2] s_free[2] p_full[2] p_free[2] q_full drain
 constexpr int kBarFull = 0, kBarEmpty = 4, kBarSFull = 8, kBarSFree = 10, kBarPFull = 12,
-              kBarPFree = 14, kBarQ = 16, kBarDrain = 17, kNumBars = 18;
+              kBarPFree = kBarPFull + kPBufs, kBarQ = kBarPFree + kPBufs, kBarDrain = kBarQ + 1,
+              kNumBars = kBarDrain + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffIds = kOffMisc + 1024;          // this CTA's slice of I (<= kMaxTopk)
 constexpr uint32_t kSmemBytes = kOffIds + kMaxTopk * 4 + 1024;  // + 1 KiB alignment slack
@@ -124,10 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) {
             uint32_t cnt = 1;
-            if (b >= kBarFull && b < kBarFull + kSlots) cnt = kProdWarps * 32 + 1;
-            if (b == kBarSFree || b == kBarSFree + 1 || b == kBarPFull || b == kBarPFull + 1)
+            if (b >= kBarFull && b < kBarFull + kSlots) cnt = kProdThreads + 1;
+            if (b == kBarSFree || b == kBarSFree + 1 || (b >= kBarPFull && b < kBarPFull + kPBufs))
                 cnt = kSoftWarps * 32;
-            if (b == kBarQ) cnt = kProdWarps * 32;
+            if (b == kBarQ) cnt = kProdThreads;
             if (b == kBarDrain) cnt = 2;                  // one commit from each issuing warp
             mbar_init(&bars[b], cnt);
         }
@@ -146,23 +150,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
 
     if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
         // ---------------- producers ----------------
-        const int pt = tid - kProdWarp0 * 32;                 // 0..63: one 16-byte unit per row
+        const int pt = tid - kProdWarp0 * 32;
+        const int pu = pt & 63;                               // the 16-byte unit of a row it copies
+        const int pr0 = pt >> 6;                              // first row; rows pr0, pr0 + kRowStep, ...
+        constexpr int kRowStep = kProdThreads / 64;
+        constexpr int kPre = 512 / kProdThreads;
         int32_t *ids = reinterpret_cast<int32_t *>(smem + kOffIds);
         const int64_t kk0 = e0 > nloc ? e0 - nloc : 0;
         const int64_t kk1 = e1 > nloc ? e1 - nloc : 0;
         // the first 512 selected ids of this CTA's range, fetched now, staged after the
         // local-window tiles are on their way
-        int32_t pre[8];
+        int32_t pre[kPre];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const int64_t kk = kk0 + pt + 64 * m;
+        for (int m = 0; m < kPre; ++m) {
+            const int64_t kk = kk0 + pt + kProdThreads * m;
             pre[m] = (Irow && kk < kk1) ? Irow[kk] : -1;
         }
         const uint32_t qb = sbase + kOffQ;
         const __nv_bfloat16 *qrow = reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)row * kH * kDH;
-        for (int h = 0; h < kH; ++h)
-            cp_async16(qb + (pt >> 3) * (kH * 128) + sw128_offset(h, (pt & 7) * 8),
-                       qrow + h * kDH + pt * 8);
+        for (int h = pr0; h < kH; h += kRowStep)
+            cp_async16(qb + (pu >> 3) * (kH * 128) + sw128_offset(h, (pu & 7) * 8),
+                       qrow + h * kDH + pu * 8);
         cp_async_arrive(&bars[kBarQ]);
         // gathers tile i into slot i % kSlots (the slot must be free)
         auto issue_tile = [&](int i) {
@@ -190,14 +198,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 valid[hlf] = __ballot_sync(0xffffffffu, src[hlf] != nullptr);
             }
             const uint32_t slot = sbase + kOffKV + s * kSlotBytes;
-            const uint32_t dst0 = slot + (pt >> 3) * (kTR * 128);
+            const uint32_t dst0 = slot + (pu >> 3) * (kTR * 128);
 #pragma unroll 4
-            for (int r = 0; r < kTR; ++r) {
+            for (int r = pr0; r < kTR; r += kRowStep) {
                 const __nv_bfloat16 *rs = reinterpret_cast<const __nv_bfloat16 *>(__shfl_sync(
                     0xffffffffu, reinterpret_cast<uintptr_t>(src[r >> 5]), r & 31));
                 const bool v = (valid[r >> 5] >> (r & 31)) & 1u;
-                cp_async16_zfill(dst0 + sw128_offset(r, (pt & 7) * 8),
-                                 v ? static_cast<const void *>(rs + pt * 8) : p.q, v);
+                cp_async16_zfill(dst0 + sw128_offset(r, (pu & 7) * 8),
+                                 v ? static_cast<const void *>(rs + pu * 8) : p.q, v);
             }
             if (pt == 0) {
                 uint64_t m = 0;
@@ -217,25 +225,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
         }
         if (Irow) {
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int64_t kk = kk0 + pt + 64 * m;
+            for (int m = 0; m < kPre; ++m) {
+                const int64_t kk = kk0 + pt + kProdThreads * m;
                 if (kk < kk1) ids[kk - kk0] = pre[m];
             }
-            for (int64_t base = kk0 + 8 * 64; base < kk1; base += 8 * 64) {
-                int32_t v[8];
+            for (int64_t base = kk0 + 512; base < kk1; base += 512) {
+                int32_t v[kPre];
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int64_t kk = base + pt + 64 * m;
+                for (int m = 0; m < kPre; ++m) {
+                    const int64_t kk = base + pt + kProdThreads * m;
                     v[m] = kk < kk1 ? Irow[kk] : -1;
                 }
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int64_t kk = base + pt + 64 * m;
+                for (int m = 0; m < kPre; ++m) {
+                    const int64_t kk = base + pt + kProdThreads * m;
                     if (kk < kk1) ids[kk - kk0] = v[m];
                 }
             }
         }
-        asm volatile("bar.sync 2, 64;" ::: "memory");    // the two producer warps
+        asm volatile("bar.sync 2, %0;" ::"n"(kProdThreads) : "memory");   // the producer warps
         bool ok = true;
         for (int i = n_pre; i < T; ++i) {
             const int s = i % kSlots;
@@ -274,8 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 return true;
             };
             auto issue_pv = [&](int i) -> bool {
-                const int s = i % kSlots, pb = i & 1;
-                if (!wait_bar_warp(&bars[kBarPFull + pb], (i >> 1) & 1, abort)) return false;
+                const int s = i % kSlots, pb = i % kPBufs;
+                if (!wait_bar_warp(&bars[kBarPFull + pb], (i / kPBufs) & 1, abort)) return false;
                 fence_after_sync();
                 const uint64_t ad = smem_desc_sw128(sbase + kOffKV + s * kSlotBytes, kTR * 128, 1024);
                 const uint64_t bd = smem_desc_sw128(sbase + kOffP + pb * kPBytes, 16, 1024);
@@ -316,9 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
         const float c2 = p.scale * kLog2e;
         const float sink2 = p.sinks[h] * kLog2e;
         float m2 = -INFINITY, l = 0.f;
-        uint32_t pfree_seen[2] = {0u, 0u};
+        uint32_t pfree_seen[kPBufs] = {};
         bool ok = true;
-        auto wait_pfree = [&](int buf, uint32_t phase) -> bool {   // PV of tile (2*phase + buf) done
+        auto wait_pfree = [&](int buf, uint32_t phase) -> bool {   // PV of tile (kPBufs*phase + buf) done
             while (pfree_seen[buf] <= phase) {
                 if (!wait_bar(&bars[kBarPFree + buf], pfree_seen[buf] & 1, abort)) return false;
                 ++pfree_seen[buf];
@@ -376,11 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
 #pragma unroll
                 for (int r = 0; r < w; ++r) pr[r] += pr[r + w];
             const float sum = pr[0] + __shfl_xor_sync(0xffffffffu, pr[0], 16);
-            // P buffer (i & 1) is free once PV(i - 2) has completed
-            if (i >= 2 && !wait_pfree(i & 1, (uint32_t)((i >> 1) - 1))) { ok = false; break; }
+            // P buffer i % kPBufs is free once PV(i - kPBufs) has completed
+            if (i >= kPBufs && !wait_pfree(i % kPBufs, (uint32_t)(i / kPBufs - 1))) { ok = false; break; }
             l = l * alpha + sum;
             {
-                uint8_t *pb = smem + kOffP + (i & 1) * kPBytes;
+                uint8_t *pb = smem + kOffP + (i % kPBufs) * kPBytes;
 #pragma unroll
                 for (int u = 0; u < kHR / 8; ++u)
                     *reinterpret_cast<uint4 *>(pb + sw128_offset(h, (half * (kHR / 8) + u) * 8)) =
@@ -390,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 // rescale O^T columns of the heads whose reference max moved up
                 if (lead) misc->alpha[h] = alpha;
                 named_sync_soft();
-                if (!wait_pfree((i - 1) & 1, (uint32_t)((i - 1) >> 1))) { ok = false; break; }
+                if (!wait_pfree((i - 1) % kPBufs, (uint32_t)((i - 1) / kPBufs))) { ok = false; break; }
                 fence_after_sync();
 #pragma unroll 1
                 for (int mt = 0; mt < 4; ++mt)
@@ -408,10 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             }
             fence_async_smem();
             fence_before_sync();
-            mbar_arrive(&bars[kBarPFull + (i & 1)]);
+            mbar_arrive(&bars[kBarPFull + (i % kPBufs)]);
         }
         // ---------------- epilogue ----------------
-        if (ok && T > 0) ok = wait_pfree((T - 1) & 1, (uint32_t)((T - 1) >> 1));
+        if (ok && T > 0) ok = wait_pfree((T - 1) % kPBufs, (uint32_t)((T - 1) / kPBufs));
         if (!ok) {
             *abort = 1;
             flag(p.status, HISA_DEV_TIMEOUT);
