@@ -19,12 +19,13 @@
 //
 // A tile is 128 scored rows, D[128 rows x 64 * planes] = rows . q^T (M = 128, K = 128) in
 // one of two TMEM accumulators. Scoring is f32 on the page; f32 operands are split
-// exactly into bf16 planes x = x1 + x2 + x3 (each the bf16 rounding of the remainder), so
-// every bf16 product is exact in the f32 accumulator. The q planes are stacked along N.
-// bf16 keys take one MMA per K step over all q planes. f32 block means take six of the
-// nine plane products (x1 y1, x1 y2, x1 y3, x2 y1, x2 y2, x3 y1): since |x2| <= 2^-8 |x|
-// and |x3| <= 2^-16 |x|, the three left out (x2 y3, x3 y2, x3 y3) add up to at most about
-// 2^-23 of |x y|, the size of one f32 rounding of the product.
+// exactly into bf16 planes x = x1 + x2 + x3 (q: each plane the bf16 rounding of the
+// remainder; block means: the remainder truncated to its top 8 significant bits, which is
+// cheaper to form), so every bf16 product is exact in the f32 accumulator. The q planes
+// are stacked along N. bf16 keys take one MMA per K step over all q planes. f32 block
+// means take six of the nine plane products (x1 y1, x1 y2, x1 y3, x2 y1, x2 y2, x3 y1):
+// with |x2| < 2^-7 |x|, |x3| < 2^-14 |x|, |y2| <= 2^-8 |y| and |y3| <= 2^-16 |y|, the three
+// left out (x2 y3, x3 y2, x3 y3) add up to less than 2^-21 of |x y|.
 // Every wait is bounded; a timeout raises HISA_DEV_TIMEOUT, and the CTA drains and exits.
 #include "select_core.cuh"
 #include "tc_ptx.cuh"
@@ -52,11 +53,12 @@ constexpr uint32_t kTileBytes = kM * kD * 2;              // fine: one [128 x 12
 constexpr uint32_t kRawBytes = kM * 64 * 4;               // coarse: f32 means, 128 rows x 64 dims
 constexpr uint32_t kHalfPlane = kM * 128;                 // [128 rows x 64 dims] bf16, 16 KiB
 constexpr uint32_t kPlaneSet = 3 * kHalfPlane;            // its three planes
-constexpr int kRawSlots = 3;                              // coarse units in flight
-// coarse: kRawSlots raw f32 units, then one plane set; fine: the key tile ring
+constexpr int kRawSlots = 2;                              // coarse raw units in flight
+constexpr int kPlaneSets = 2;                             // coarse converted units
+// coarse: kRawSlots raw f32 units, then kPlaneSets plane sets; fine: the key tile ring
 template <int MODE>
 constexpr uint32_t region_bytes() {
-    return MODE == kCoarse ? kRawSlots * kRawBytes + kPlaneSet : kFineSlots * kTileBytes;
+    return MODE == kCoarse ? kRawSlots * kRawBytes + kPlaneSets * kPlaneSet : kFineSlots * kTileBytes;
 }
 constexpr uint32_t kOffPlanes = kOffReg + kRawSlots * kRawBytes;
 
@@ -192,9 +194,9 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             if (b == kBarQFull || b == kBarAccEmpty || b == kBarAccEmpty + 1 || b == kBarScFull ||
                 b == kBarScFull + 1)
                 cnt = kGroup;
-            // coarse: Full / Empty + 0 guard the plane set, + 1 .. 3 the raw slots
-            if (MODE == kCoarse && b == kBarFull) cnt = kCvtThreads;
-            if (MODE == kCoarse && b > kBarEmpty && b <= kBarEmpty + kRawSlots) cnt = kCvtThreads;
+            // coarse: Full / Empty + 0, 1 guard the plane sets, + 2, 3 the raw slots
+            if (MODE == kCoarse && (b == kBarFull || b == kBarFull + 1)) cnt = kCvtThreads;
+            if (MODE == kCoarse && (b == kBarEmpty + 2 || b == kBarEmpty + 3)) cnt = kCvtThreads;
             mbar_init(&bars[b], cnt);
         }
         mbar_fence_init();
@@ -385,22 +387,22 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 for (int t = 0; t < T && ok; ++t) {
                     for (int h = 0; h < 2; ++h, ++u) {
                         const uint32_t slot = u % kRawSlots, use = u / kRawSlots;
-                        if (use >= 1 && !wait_bar(&bars[kBarEmpty + 1 + slot], (use - 1) & 1, abort)) {
+                        if (use >= 1 && !wait_bar(&bars[kBarEmpty + 2 + slot], (use - 1) & 1, abort)) {
                             fail();
                             break;
                         }
-                        mbar_arrive_expect_tx(&bars[kBarFull + 1 + slot], kRawBytes);
+                        mbar_arrive_expect_tx(&bars[kBarFull + 2 + slot], kRawBytes);
                         const int32_t y = (int32_t)(M.base + (int64_t)t * kM);
 #pragma unroll
                         for (int c2 = 0; c2 < 2; ++c2)
                             tma_load_2d(sbase + kOffReg + slot * kRawBytes + c2 * (kM * 128), &P.means_map,
-                                        h * 64 + c2 * 32, y, &bars[kBarFull + 1 + slot]);
+                                        h * 64 + c2 * 32, y, &bars[kBarFull + 2 + slot]);
                     }
                 }
             }
             if (!ok)   // let the copies in flight land before the CTA can exit
                 for (uint32_t v = u > kRawSlots ? u - kRawSlots : 0; v < u; ++v)
-                    mbar_wait(&bars[kBarFull + 1 + v % kRawSlots], (v / kRawSlots) & 1, 1u << 20);
+                    mbar_wait(&bars[kBarFull + 2 + v % kRawSlots], (v / kRawSlots) & 1, 1u << 20);
         }
     } else if (warp == kWarpMma) {
         // ---------------- MMA issue (warp-uniform loop, one elected lane issues) ----------
@@ -446,10 +448,10 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 } else {
                     bool good = true;
                     for (int h = 0; h < 2; ++h, ++u) {
-                        // one plane set: unit u is the (u + 1)-th phase of its barriers
-                        if (!wait_bar_warp(&bars[kBarFull], u & 1, abort)) { good = false; break; }
+                        const uint32_t pb = u & 1;               // plane set of unit u
+                        if (!wait_bar_warp(&bars[kBarFull + pb], (u >> 1) & 1, abort)) { good = false; break; }
                         fence_after_sync();
-                        const uint64_t pd = smem_desc_sw128(sbase + kOffPlanes, 16, 1024);
+                        const uint64_t pd = smem_desc_sw128(sbase + kOffPlanes + pb * kPlaneSet, 16, 1024);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint32_t kb = kk * 32;
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                             mma_bf16_warp(d, desc_add(pd, kHalfPlane + kb), bq, id_two, 1u);
                             mma_bf16_warp(d, desc_add(pd, 2 * kHalfPlane + kb), bq, id_one, 1u);
                         }
-                        mma_commit_warp(&bars[kBarEmpty]);
+                        mma_commit_warp(&bars[kBarEmpty + pb]);
                     }
                     if (!good) { fail(); break; }
                 }
@@ -566,30 +568,38 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             const int nunits = M.state ? 0 : 2 * M.T;
             for (int e = 0; e < nunits; ++e, ++u) {
                 const uint32_t slot = u % kRawSlots;
-                if (!wait_bar(&bars[kBarFull + 1 + slot], (u / kRawSlots) & 1, abort) ||
-                    (u >= 1 && !wait_bar(&bars[kBarEmpty], (u - 1) & 1, abort))) {
+                const uint32_t pb = u & 1;
+                if (!wait_bar(&bars[kBarFull + 2 + slot], (u / kRawSlots) & 1, abort) ||
+                    (u >= 2 && !wait_bar(&bars[kBarEmpty + pb], ((u >> 1) - 1) & 1, abort))) {
                     fail();
                     break;
                 }
                 const uint8_t *rawb = smem + kOffReg + slot * kRawBytes;
-                uint8_t *planes = smem + kOffPlanes;
+                uint8_t *planes = smem + kOffPlanes + pb * kPlaneSet;
 #pragma unroll
                 for (int m = 0; m < kChunks; ++m) {
                     const int c = m * kCvtThreads + ct, bx = c >> 10, r = (c >> 3) & 127, v = c & 7;
                     const float4 a = *reinterpret_cast<const float4 *>(
                         rawb + bx * (kM * 128) + r * 128 + ((v ^ (r & 7)) << 4));
+                    // exact split by truncation: hi = top 8 significant bits, then the same
+                    // of the (exact) remainder; the last remainder has at most 8 bits left
                     uint32_t w[3][2];
-                    float x0 = a.x, x1 = a.y, x2 = a.z, x3 = a.w;
+                    const float xs[4] = {a.x, a.y, a.z, a.w};
+                    uint32_t pk[3][4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t b0 = __float_as_uint(xs[e]) & 0xffff0000u;
+                        const float r1 = xs[e] - __uint_as_float(b0);
+                        const uint32_t b1 = __float_as_uint(r1) & 0xffff0000u;
+                        const float r2 = r1 - __uint_as_float(b1);
+                        pk[0][e] = b0;
+                        pk[1][e] = b1;
+                        pk[2][e] = __float_as_uint(r2);
+                    }
 #pragma unroll
                     for (int k = 0; k < 3; ++k) {
-                        const __nv_bfloat162 b0 = __floats2bfloat162_rn(x0, x1);
-                        const __nv_bfloat162 b1 = __floats2bfloat162_rn(x2, x3);
-                        w[k][0] = *reinterpret_cast<const uint32_t *>(&b0);
-                        w[k][1] = *reinterpret_cast<const uint32_t *>(&b1);
-                        if (k < 2) {
-                            const float2 f0 = __bfloat1622float2(b0), f1 = __bfloat1622float2(b1);
-                            x0 -= f0.x; x1 -= f0.y; x2 -= f1.x; x3 -= f1.y;
-                        }
+                        w[k][0] = __byte_perm(pk[k][0], pk[k][1], 0x7632);   // {hi(e0), hi(e1)}
+                        w[k][1] = __byte_perm(pk[k][2], pk[k][3], 0x7632);
                     }
                     const uint32_t off = sw128_offset((uint32_t)r, (uint32_t)(bx * 32 + v * 4));
 #pragma unroll
@@ -597,8 +607,8 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                         *reinterpret_cast<uint2 *>(planes + k * kHalfPlane + off) = make_uint2(w[k][0], w[k][1]);
                 }
                 fence_async_smem();
-                mbar_arrive(&bars[kBarFull]);
-                mbar_arrive(&bars[kBarEmpty + 1 + slot]);
+                mbar_arrive(&bars[kBarFull + pb]);
+                mbar_arrive(&bars[kBarEmpty + 2 + slot]);
             }
         }
     }
