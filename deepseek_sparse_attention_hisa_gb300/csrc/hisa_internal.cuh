@@ -11,6 +11,32 @@
 
 namespace hisa {
 
+// ---- programmatic dependent launch ------------------------------------------------
+// Kernels of a step are launched with programmatic stream serialization: the launch of a
+// kernel is prepared while the previous kernel on the stream runs and is released when it
+// completes (none of these kernels triggers its dependents early: measured, an early or a
+// late trigger made the step slower). Every such kernel executes grid_dep_wait() before
+// its first global-memory access, which waits until the previous grid has completed and
+// its writes are visible, so results never depend on the overlap.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+
 constexpr float kNeg = -1e30f;            // selection mask value ([HiSA issue] "Flat selection")
 constexpr size_t kStatusBytes = 256;      // status word region at the head of the workspace
 constexpr int kTargetCtas = 304;          // 2 CTAs per SM on a 152-SM GB300

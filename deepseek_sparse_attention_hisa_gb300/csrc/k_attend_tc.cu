@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
     Misc *misc = reinterpret_cast<Misc *>(smem + kOffMisc);
     volatile int *abort = &misc->abort;
 
+    grid_dep_wait();                                    // before the first global access
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row = blockIdx.x, split = blockIdx.y;
     const int bq = row / p.L, j = row - bq * p.L;
@@ -489,8 +490,7 @@ cudaError_t launch_attend_tc(const AttnParams &p, cudaStream_t s) {
         k_attend_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (attr != cudaSuccess) return attr;
     dim3 grid((unsigned)(p.B * p.L), (unsigned)p.nsplit);
-    k_attend_tc<<<grid, kThreads, kSmemBytes, s>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_attend_tc, grid, dim3(kThreads), kSmemBytes, s, p);
     if (e != cudaSuccess || p.nsplit == 1) return e;
     return launch_attend_combine(p, s);
 }

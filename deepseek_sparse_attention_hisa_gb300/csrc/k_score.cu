@@ -213,6 +213,7 @@ constexpr int kMeansStage = 8192;                      // f32 elements staged pe
 template <typename KT>
 __global__ void __launch_bounds__(kMeansThreads) k_block_means_staged(MeansParams p) {
     __shared__ float stage[kMeansStage];
+    grid_dep_wait();
     const int bq = blockIdx.y;
     const int64_t k0 = p.key_off[bq];
     const int64_t Np = p.key_off[bq + 1] - k0;
@@ -269,10 +270,8 @@ cudaError_t launch_block_means(const MeansParams &p, int64_t nb_max, cudaStream_
     dim3 grid(gx, (unsigned)p.B);
     if ((int64_t)p.b * p.D_i <= kMeansStage) {
         if (p.keys_bf16)
-            k_block_means_staged<__nv_bfloat16><<<grid, kMeansThreads, 0, s>>>(p);
-        else
-            k_block_means_staged<float><<<grid, kMeansThreads, 0, s>>>(p);
-        return cudaGetLastError();
+            return launch_pdl(k_block_means_staged<__nv_bfloat16>, grid, dim3(kMeansThreads), 0, s, p);
+        return launch_pdl(k_block_means_staged<float>, grid, dim3(kMeansThreads), 0, s, p);
     }
     const int threads = p.D_i;
     if (p.keys_bf16)

@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_gemm(const __grid_constan
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = misc->tmem;
+    grid_dep_wait();                                    // before the first global access
     bool ok = true;
     auto fail = [&]() {
         ok = false;
@@ -319,8 +320,7 @@ cudaError_t launch_score_gemm(const ScoreParams &s, cudaStream_t stream) {
     const int sms = sm_count_gemm();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = units < sms ? (int)units : sms;
-    k_score_gemm<<<grid, kThreads, kSmem, stream>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(k_score_gemm, dim3(grid), dim3(kThreads), kSmem, stream, P);
 }
 
 }  // namespace hisa

@@ -210,6 +210,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = misc->tmem;
+    grid_dep_wait();                                    // before the first global access
     bool ok = true;
     auto fail = [&]() {
         ok = false;
@@ -683,8 +684,7 @@ cudaError_t launch_pipe_t(const ScoreTcParams &p, cudaStream_t s) {
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = rows < sms ? rows : sms;
     const size_t smem = Layout<MODE>::fixed + 2 * (size_t)p.s.n_max * 4;
-    k_score_pipe<MODE, QBF16><<<grid, pipe_threads<MODE>(), smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k_score_pipe<MODE, QBF16>, dim3(grid), dim3(pipe_threads<MODE>()), smem, s, p);
 }
 
 }  // namespace
