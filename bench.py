@@ -3,9 +3,10 @@
 Workload: R independent V4-Flash-shaped decode queries per step (each: Np = 32768
 pooled rows of a 131072-token prefix, H_i = 64 x D_i = 128 indexer, index_block = 64,
 keep = 16, index_topk = 512, 64 query heads x Dh = 512, window 128, bf16 keys / KV,
-f32 indexer q). One step = the newest block mean of every sequence, the coarse block
-filter, the fine top-k and the sparse combine: four C-ABI calls, each replayed from its
-own CUDA graph, with CUDA events between them on the launching stream.
+f32 indexer q). One step = the newest block mean of every sequence appended to the
+block-mean cache, the coarse block filter, the fine top-k and the sparse combine: three
+C-ABI calls (hisa_block_filter_append, hisa_select_topk, hisa_sparse_attend), replayed as
+one CUDA graph for the headline and from one graph per call for the stage times.
 
 Prints one JSON line (rank 0). `--impl reference` times the CPU oracle instead.
 """
@@ -68,7 +69,7 @@ def stage_bytes(wl, nb):
     # unique bytes of the whole step: q/w and I/top_blk counted once
     step = means + q_idx + w + nb * D_i * 4 + keep * b * D_i * 2 + H * Dh * 2 + W * Dh * 2 + \
         k * Dh * 2 + H * 4 + H * Dh * 4 + k * 4 + keep * 4
-    return dict(block_means=means, block_filter=filt, select_topk=sel, sparse_attend=att), step
+    return dict(block_filter_append=means + filt, select_topk=sel, sparse_attend=att), step
 
 
 # ----------------------------------------------------------------------------
@@ -359,11 +360,11 @@ def run_gpu(args, wl, R):
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
-    stages = ["block_means", "block_filter", "select_topk", "sparse_attend"]
+    # the newest block's mean is appended every step (a new block completes every
+    # r * index_block = 256 tokens in a real decode loop: this recomputes it each step)
+    stages = ["block_filter_append", "select_topk", "sparse_attend"]
     calls = {
-        "block_means": lambda s: hb.block_means(prob.idesc, prob.keys, prob.key_off,
-                                                prob.means_off, newest, prob.means, prob.ws, s),
-        "block_filter": lambda s: prob.block_filter(stream=s),
+        "block_filter_append": lambda s: prob.block_filter_append(first_block=newest, stream=s),
         "select_topk": lambda s: prob.select_topk(stream=s),
         "sparse_attend": lambda s: prob.attend(stream=s),
     }
@@ -462,7 +463,7 @@ def run_gpu(args, wl, R):
     stage_avg = {n: statistics.mean(v) for n, v in stage_ms.items()}
     dom = max(stage_avg, key=stage_avg.get)
     achieved = per_stage_bytes[dom] * R / (stage_avg[dom] / 1e3) / 1e9
-    kernel_of = {"block_means": "k_block_means_staged", "block_filter": "k_score_pipe (coarse)",
+    kernel_of = {"block_filter_append": "k_score_pipe (coarse, appending the newest block means)",
                  "select_topk": "k_score_pipe (fine)", "sparse_attend": "k_attend_tc"}
     traffic = traffic_from_profile(kernel_of[dom])
 
@@ -543,13 +544,13 @@ def run_prefill_scoring(args, dev, stream):
 
 
 def launches_per_step(prob):
-    """Kernels this library launches per step for the V4 decode shape: block means 1, the
-    coarse filter 1 and the fine top-k 1 (each scores and selects in one tcgen05 kernel),
-    the combine 1, plus the split-K merge when the combine is split."""
+    """Kernels this library launches per step for the V4 decode shape: the coarse filter
+    with the newest block means appended 1 and the fine top-k 1 (each scores and selects
+    in one tcgen05 kernel), the combine 1, plus the split-K merge when it is split."""
     from deepseek_sparse_attention_hisa_gb300 import binding as hb
     ws_need = hb.workspace_bytes(hb.OP_SPARSE_ATTEND, prob.adesc)
     attend = 2 if ws_need > 256 else 1
-    return 1 + 1 + 1 + attend
+    return 1 + 1 + attend
 
 
 def main():

@@ -60,6 +60,7 @@ _SIG = {
     "hisa_block_filter": (ctypes.c_int32, [_P] * 9 + [ctypes.c_int64, _P, ctypes.c_size_t, _P]),
     "hisa_select_topk": (ctypes.c_int32, [_P] * 10 + [ctypes.c_size_t, _P]),
     "hisa_flat_topk": (ctypes.c_int32, [_P] * 8 + [ctypes.c_size_t, _P]),
+    "hisa_block_filter_append": (ctypes.c_int32, [_P] * 11 + [ctypes.c_int64, _P, ctypes.c_size_t, _P]),
     "hisa_flat_topk_noalloc": (ctypes.c_int32, [_P] * 9),
     "hisa_sparse_attend": (ctypes.c_int32, [_P] * 12 + [ctypes.c_size_t, _P]),
 }
@@ -177,6 +178,15 @@ def flat_topk(desc, q, w, keys, key_off, t0, I, ws, stream=None):
     _check(lib().hisa_flat_topk(ctypes.byref(desc), _ptr(q), _ptr(w), _ptr(keys), _ptr(key_off),
                                 _ptr(t0), _ptr(I), _ptr(ws), ws.numel(), _stream(stream)),
            "hisa_flat_topk")
+
+
+def block_filter_append(desc, q, w, keys, key_off, means, means_off, first_block, t0, top_blk, ws,
+                        cscores=None, ld_cscores=0, stream=None):
+    _check(lib().hisa_block_filter_append(ctypes.byref(desc), _ptr(q), _ptr(w), _ptr(keys),
+                                          _ptr(key_off), _ptr(means), _ptr(means_off),
+                                          _ptr(first_block), _ptr(t0), _ptr(top_blk), _ptr(cscores),
+                                          ld_cscores, _ptr(ws), ws.numel(), _stream(stream)),
+           "hisa_block_filter_append")
 
 
 def flat_topk_noalloc(desc, q, w, keys, key_off, t0, I, dev_status=None, stream=None):

@@ -290,6 +290,45 @@ hisa_status hisa_block_filter(const hisa_index_desc *d, const void *q, const flo
     return from_cuda(launch_select(sp, nb_max, s));
 }
 
+hisa_status hisa_block_filter_append(const hisa_index_desc *d, const void *q, const float *w,
+                                     const void *keys, const int64_t *key_off, float *means,
+                                     const int64_t *means_off, const int32_t *first_block,
+                                     const int32_t *t0, int32_t *top_blk, float *cscores,
+                                     int64_t ld_cscores, void *ws, size_t ws_bytes,
+                                     hisa_stream_t stream) {
+    hisa_status st = check_index_desc(d);
+    if (st != HISA_OK) return st;
+    if ((st = check_hisa_gate(d)) != HISA_OK) return st;
+    if (!q || !w || !keys || !means || !means_off || !key_off || !t0 || !top_blk) return HISA_EINVAL;
+    if (!aligned(q, 16) || !aligned(keys, 16) || !aligned(means, 16) || !aligned(w, 4))
+        return HISA_EINVAL;
+    const int64_t nb_max = d->Np_max / d->index_block;
+    if (cscores && ld_cscores < nb_max) return HISA_EINVAL;
+    if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_BLOCK_FILTER, d))) != HISA_OK)
+        return st;
+    const bool fused = d->L == 1 && d->k_dtype == HISA_BF16 && d->index_block == 64 && d->D_i == 128 &&
+                       d->means_rows > 0 && d->keys_rows > 0 &&
+                       score_pipe_supported(kCoarse, d->H_i, d->D_i, 0, nb_max, d->index_block,
+                                            d->index_keep);
+    if (!fused) {
+        st = hisa_block_means(d, keys, key_off, means_off, first_block, means, ws, ws_bytes, stream);
+        if (st != HISA_OK) return st;
+        return hisa_block_filter(d, q, w, means, means_off, key_off, t0, top_blk, cscores,
+                                 ld_cscores, ws, ws_bytes, stream);
+    }
+    ScoreParams p = score_params(d, kCoarse, q, w, means, 0, key_off, t0, cscores,
+                                 cscores ? ld_cscores : 0, ws);
+    p.means_off = means_off;
+    p.n_max = nb_max;
+    ScoreTcParams t{};
+    t.s = p;
+    t.sel = top_blk;
+    t.k_sel = d->index_keep;
+    t.append_keys = keys;
+    t.first_block = first_block;
+    return from_cuda(launch_score_pipe(t, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 hisa_status hisa_select_topk(const hisa_index_desc *d, const void *q, const float *w,
                              const void *keys, const int64_t *key_off, const int32_t *t0,
                              const int32_t *top_blk, int32_t *I, float *fscores, void *ws,

@@ -165,6 +165,10 @@ struct ScoreTcParams {
     CUtensorMap keys_map;     // bf16 keys [keys_rows, 128], box 64 dims x 64 rows, 128B swizzle
     CUtensorMap means_map;    // f32 block means [means_rows, 128], box 32 dims x 128 rows, 128B swizzle
     ScoreParams s;
+    // coarse only: when append_keys is set, the kernel first writes the block means of blocks
+    // [first_block[b], nb_b) from these bf16 keys (decode rows, index_block 64, D_i 128)
+    const void *append_keys;
+    const int32_t *first_block;
     int32_t *sel;
     int k_sel;
     int tiles_per_cta;        // flat: 128-row tiles per CTA (grid.y covers the row)

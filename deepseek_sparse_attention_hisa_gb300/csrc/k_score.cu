@@ -205,8 +205,9 @@ __global__ void k_block_means(MeansParams p) {
 
 // The same means, one block per pass with all of its b * D_i keys in flight at once: the
 // block is one contiguous run of keys, copied with 16-byte loads into shared memory as
-// f32, then each thread sums one dimension over the rows in row order (the same f32
-// additions, in the same order, as k_block_means).
+// f32, then each thread sums one dimension: eight partial sums over the rows i = k (mod 8)
+// in row order, combined by a fixed pairwise tree (the order the coarse kernel's append
+// path uses too, so a block mean has the same bits whichever kernel wrote it).
 constexpr int kMeansThreads = 256;
 constexpr int kMeansStage = 8192;                      // f32 elements staged per block
 
@@ -252,8 +253,16 @@ __global__ void __launch_bounds__(kMeansThreads) k_block_means_staged(MeansParam
         }
         __syncthreads();
         for (int d = threadIdx.x; d < p.D_i; d += kMeansThreads) {
-            float s = 0.f;
-            for (int i = 0; i < p.b; ++i) s += stage[i * p.D_i + d];
+            // partial sums over the rows i = k (mod 8), each in row order, then the fixed
+            // pairwise tree ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7))
+            float ps[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float a = 0.f;
+                for (int i = k; i < p.b; i += 8) a += stage[i * p.D_i + d];
+                ps[k] = a;
+            }
+            const float s = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             p.means[(m0 + beta) * p.D_i + d] = s / inv_div;
         }
         __syncthreads();

@@ -77,7 +77,8 @@ struct QMeta {            // one query row, double-buffered
 constexpr int kBarMetaFull = 0, kBarSlotFree = 2, kBarQFull = 4, kBarQEmpty = 5,
               kBarAccFull = 6, kBarAccEmpty = 8, kBarScFull = 10, kBarDrain = 12,
               kBarFull = 13,                                // fine: kFineSlots; coarse: 2 planes
-              kBarEmpty = kBarFull + kFineSlots, kNumBars = kBarEmpty + kFineSlots;
+              kBarEmpty = kBarFull + kFineSlots, kBarMeansReady = kBarEmpty + kFineSlots,
+              kNumBars = kBarMeansReady + 2;
 
 template <int MODE>
 struct Layout {
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
         for (int b = 0; b < kNumBars; ++b) {
             uint32_t cnt = 1;
             if (b == kBarQFull || b == kBarAccEmpty || b == kBarAccEmpty + 1 || b == kBarScFull ||
-                b == kBarScFull + 1)
+                b == kBarScFull + 1 || b == kBarMeansReady || b == kBarMeansReady + 1)
                 cnt = kGroup;
             // coarse: Full / Empty + 0, 1 guard the plane sets, + 2, 3 the raw slots
             if (MODE == kCoarse && (b == kBarFull || b == kBarFull + 1)) cnt = kCvtThreads;
@@ -340,6 +341,49 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             }
             fence_async_smem();
             mbar_arrive(&bars[kBarQFull]);
+            if (MODE == kCoarse && P.append_keys) {
+                // block means of the newly completed blocks [first_block, nb): thread bt owns
+                // dims 8 (bt / 8) .. + 7 of rows bt % 8 + 8 m; eight partial sums in row order,
+                // then the pairwise tree over the eight lanes of a dimension group
+                const QMeta &M = meta[qb];
+                if (!M.state) {
+                    int64_t fb = P.first_block ? (int64_t)P.first_block[bq] : 0;
+                    fb = fb < 0 ? 0 : fb;
+                    const int k = bt & 7, gq = bt >> 3;
+                    const uint4 *kv = reinterpret_cast<const uint4 *>(P.append_keys);
+                    float *means_w = const_cast<float *>(reinterpret_cast<const float *>(p.rows));
+                    for (int64_t beta = fb; beta < M.n; ++beta) {
+                        const uint4 *src = kv + (k0 + beta * 64) * (kD / 8);
+                        uint4 u[8];
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) u[m] = __ldg(src + (8 * m + k) * (kD / 8) + gq);
+                        float ps[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ps[e] = 0.f;
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) {
+                            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&u[m]);
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2) {
+                                const float2 f = __bfloat1622float2(h2[e2]);
+                                ps[2 * e2] += f.x;
+                                ps[2 * e2 + 1] += f.y;
+                            }
+                        }
+#pragma unroll
+                        for (int off = 1; off < 8; off <<= 1)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) ps[e] += __shfl_xor_sync(0xffffffffu, ps[e], off);
+                        if (k == 0) {
+                            float4 *dst = reinterpret_cast<float4 *>(means_w + (M.base + beta) * kD + gq * 8);
+                            dst[0] = make_float4(ps[0] / 64.f, ps[1] / 64.f, ps[2] / 64.f, ps[3] / 64.f);
+                            dst[1] = make_float4(ps[4] / 64.f, ps[5] / 64.f, ps[6] / 64.f, ps[7] / 64.f);
+                        }
+                    }
+                    fence_async_global();               // the loader reads them by TMA
+                }
+                mbar_arrive(&bars[kBarMeansReady + qb]);
+            }
         }
     }
     else if (MODE == kFine && warp == kWarpTma) {
@@ -385,7 +429,19 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 if (!wait_bar(&bars[kBarMetaFull + qb], (i >> 1) & 1, abort)) { fail(); break; }
                 const QMeta &M = meta[qb];
                 const int T = M.state ? 0 : M.T;
+                // appended means: tiles from the one holding the first new block on wait for them
+                int t_new = T;
+                if (P.append_keys && T > 0) {
+                    const int row = (int)blockIdx.x + i * (int)gridDim.x;
+                    int64_t fb = P.first_block ? (int64_t)P.first_block[row / p.L] : 0;
+                    fb = fb < 0 ? 0 : fb;
+                    if (fb < M.n) t_new = (int)(fb / kM);
+                }
                 for (int t = 0; t < T && ok; ++t) {
+                    if (t == t_new && !wait_bar(&bars[kBarMeansReady + qb], (i >> 1) & 1, abort)) {
+                        fail();
+                        break;
+                    }
                     for (int h = 0; h < 2; ++h, ++u) {
                         const uint32_t slot = u % kRawSlots, use = u / kRawSlots;
                         if (use >= 1 && !wait_bar(&bars[kBarEmpty + 2 + slot], (use - 1) & 1, abort)) {

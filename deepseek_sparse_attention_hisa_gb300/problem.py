@@ -96,6 +96,13 @@ class Problem:
         hb.block_filter(self.idesc, self.q_idx, self.w, self.means, self.means_off, self.key_off,
                         self.t0, self.top_blk, self.ws, cscores, ld, stream)
 
+    def block_filter_append(self, first_block=None, cscores=None, stream=None):
+        """Append the means of blocks [first_block[b], nb_b), then the coarse filter."""
+        ld = 0 if cscores is None else cscores.shape[1]
+        hb.block_filter_append(self.idesc, self.q_idx, self.w, self.keys, self.key_off, self.means,
+                               self.means_off, first_block, self.t0, self.top_blk, self.ws,
+                               cscores, ld, stream)
+
     def select_topk(self, fscores=None, top_blk=None, stream=None):
         tb = self.top_blk if top_blk is None else top_blk
         hb.select_topk(self.idesc, self.q_idx, self.w, self.keys, self.key_off, self.t0, tb,

@@ -153,7 +153,9 @@ HISA_API hisa_status hisa_index_scores(const hisa_index_desc *desc, const void *
  *             leave room for nb_b rows (else HISA_DEV_BAD_OFFSETS and nothing is written).
  *   first_block [B] int32 or NULL: blocks [first_block[b], nb_b) are (re)computed, so
  *             a decode loop appends the newly completed blocks only. NULL = from 0.
- * f32 sum in row order, divided by b. */
+ * f32 sums: for each dimension, eight partial sums over the rows i = k (mod 8) in row
+ * order, combined as ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)), divided by b
+ * (blocks of more than 8192 keys: one sum in row order). */
 HISA_API hisa_status hisa_block_means(const hisa_index_desc *desc, const void *keys,
                              const int64_t *key_off, const int64_t *means_off,
                              const int32_t *first_block, float *means, void *ws, size_t ws_bytes,
@@ -173,6 +175,20 @@ HISA_API hisa_status hisa_block_filter(const hisa_index_desc *desc, const void *
                               const int64_t *key_off, const int32_t *t0, int32_t *top_blk,
                               float *cscores, int64_t ld_cscores, void *ws, size_t ws_bytes,
                               hisa_stream_t stream);
+
+/* hisa_block_means, then hisa_block_filter, as one call: the block means of blocks
+ * [first_block[b], nb_b) are appended to `means` (same values as hisa_block_means), then
+ * the coarse stage runs over all nb_b means. Arguments as in those two calls. For decode
+ * (L = 1) with the DeepSeek-V4 indexer shape (H_i = 64, D_i = 128, index_block = 64, bf16
+ * keys) it is one kernel, in which the new means are computed while the older means
+ * stream into the coarse scoring; otherwise it makes the two calls in turn. ws must hold
+ * hisa_workspace_bytes(HISA_OP_BLOCK_FILTER, desc) bytes. */
+HISA_API hisa_status hisa_block_filter_append(const hisa_index_desc *desc, const void *q,
+                                     const float *w, const void *keys, const int64_t *key_off,
+                                     float *means, const int64_t *means_off,
+                                     const int32_t *first_block, const int32_t *t0,
+                                     int32_t *top_blk, float *cscores, int64_t ld_cscores,
+                                     void *ws, size_t ws_bytes, hisa_stream_t stream);
 
 /* Fine stage ([HiSA issue] "HiSA decode path" / "HiSA batched path": candidates
  * pos = top_blk[c / b]*b + c % b, exact rescoring, NEG where pos >= V(t0+j) when

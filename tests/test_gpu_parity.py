@@ -427,3 +427,54 @@ def test_dense_scoring_partial_units_and_ragged_sequences():
                            what=f"dense score row {b},{j}")
             assert np.all(sc[r, s["Np"]:] == 7.0)        # columns past Np are not written
             P.check_flat(data, b, j, I[r], wl.index_topk)
+
+
+def test_block_filter_append_matches_means_then_filter():
+    """hisa_block_filter_append (means of the new blocks computed inside the coarse kernel
+    for decode) gives the bits of hisa_block_means followed by hisa_block_filter: zero,
+    one, three and all blocks new, across ragged sequences."""
+    B = 6
+    wl = inputs.small_workload(name="append", seed=51, B=B, H_i=64, D_i=128, index_block=64,
+                               index_keep=16, index_topk=512, q_idx_dtype="f32", key_dtype="bf16",
+                               Np=(2048, 4100, 8192, 1024, 3000, 6400), with_attention=False)
+    data = inputs.generate(wl)
+    ref, fus = Problem(data), Problem(data)
+    nb = np.asarray(data["Np"]) // 64
+    fb = np.array([nb[0] - 1, nb[1], nb[2] - 3, 0, nb[4] - 1, nb[5] - 2], dtype=np.int32)
+    fb_t = torch.as_tensor(fb, device="cuda")
+    # both start from a cache whose new blocks hold garbage
+    ref.block_means()
+    fus.means.copy_(ref.means)
+    for b in range(B):
+        m0 = int(np_(ref.means_off)[b])
+        ref.means[m0 + int(fb[b]):m0 + int(nb[b])] = 123.0
+        fus.means[m0 + int(fb[b]):m0 + int(nb[b])] = -77.0
+    cs_ref = torch.full((B, int(nb.max())), 7.0, device="cuda")
+    cs_fus = torch.full((B, int(nb.max())), 7.0, device="cuda")
+    hb.block_means(ref.idesc, ref.keys, ref.key_off, ref.means_off, fb_t, ref.means, ref.ws)
+    ref.block_filter(cscores=cs_ref)
+    fus.block_filter_append(first_block=fb_t, cscores=cs_fus)
+    torch.cuda.synchronize()
+    assert ref.status() == 0 and fus.status() == 0
+    assert torch.equal(ref.means, fus.means)
+    assert torch.equal(cs_ref, cs_fus)
+    assert np.array_equal(np.sort(np_(ref.top_blk), axis=1), np.sort(np_(fus.top_blk), axis=1))
+    P.check_block_means(data, np_(fus.means), np_(fus.means_off), 64)
+    for b in range(B):
+        P.check_coarse(data, b, 0, np_(fus.top_blk)[b], np_(cs_fus)[b], 64, 16)
+
+
+def test_block_filter_append_two_call_path():
+    """Shapes the fused kernel does not take (f32 keys, or L > 1) run the two calls."""
+    for kw in (dict(seed=52, B=2, Np=(700, 1000)), dict(seed=53, L=6, Np=(512,), t0=1900)):
+        data = small(**kw)
+        prob = Problem(data)
+        fb = torch.zeros(data["wl"].B, dtype=torch.int32, device="cuda")
+        prob.block_filter_append(first_block=fb)
+        torch.cuda.synchronize()
+        assert prob.status() == 0
+        P.check_block_means(data, np_(prob.means), np_(prob.means_off), data["wl"].index_block)
+        for b in range(data["wl"].B):
+            for j in range(data["wl"].L):
+                P.check_coarse(data, b, j, np_(prob.top_blk)[b * data["wl"].L + j], None,
+                               data["wl"].index_block, data["wl"].index_keep)
