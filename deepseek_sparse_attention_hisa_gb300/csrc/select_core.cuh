@@ -33,12 +33,12 @@ __device__ __forceinline__ void group_sync() {
 }
 
 template <int NT>
-struct SelectShared {
+struct alignas(16) SelectShared {
     uint32_t hist[256];
     uint32_t wg[NT / 32], we[NT / 32];
     uint32_t prefix, kk, ncand;
     int nonfinite;
-    int32_t cand[kCand];
+    alignas(16) int32_t cand[kCand];
 };
 
 // One warp: find the digit (at `shift`) of the kk-th largest key among the keys counted
@@ -291,6 +291,201 @@ namespace hisa {
 // Capacity of the threshold bin that small_topk resolves itself.
 constexpr int kSmallCand = 128;
 
+// Top kout of n <= E * NT scores in shared memory, short form. Thread t holds the E
+// contiguous columns [t E, t E + E) in registers for the whole call. The selecting warps
+// share the SM's shared-memory and shuffle pipes, so every step keeps those instructions
+// few (one warp scans the histogram; no warp repeats another's reads):
+//   1. per-warp range (integer min / max of the unmasked keys) and counts;
+//   2. a 512-bin histogram of the unmasked scores over their value range; warp 0 finds
+//      the bin tb of the kout-th largest score and the rank kk that the selection takes
+//      inside tb;
+//   3. the threshold-bin candidates (column, key) appended to a list; each owner ranks its
+//      own candidates against the list by (key desc, column asc) and keeps those below kk;
+//   4. a block scan of the per-thread selected counts gives each thread its output slots,
+//      so the selection is written in ascending column order.
+// Returns false, before writing anything and after a barrier that ends every use of sh,
+// when the input needs the general select: a non-finite score, fewer than kout unmasked
+// scores, (nearly) equal unmasked scores, or more than kSmallCand scores in the threshold
+// bin. The result is block_topk's.
+template <int NT, int BAR, int TID0, int E, typename Map>
+__device__ bool fast_topk(const float *sc, int n, int kout, int32_t *out, Map map,
+                          SelectShared<NT> &sh) {
+    constexpr int NW = NT / 32, kBins = 512;
+    static_assert(E == 4 || E == 8, "columns per thread");
+    static_assert(kBins + 2 * kSmallCand <= kCand && NW <= 32 && 4 * NW <= 256 && E * 32 < 0x10000, "scratch");
+    const int tid = (int)threadIdx.x - TID0, lane = tid & 31, warp = tid >> 5;
+    uint32_t *hist = reinterpret_cast<uint32_t *>(sh.cand);             // kBins counts
+    uint2 *cand = reinterpret_cast<uint2 *>(sh.cand + kBins);             // (column, key)
+    uint2 *part = reinterpret_cast<uint2 *>(sh.hist);                     // per warp (min, max)
+    uint32_t *pcnt = sh.hist + 2 * NW, *wtot = sh.hist + 3 * NW;          // per warp
+    const int c0 = tid * E;
+    const int dwarps = (n + 32 * E - 1) / (32 * E);                       // warps with columns
+    const bool dw = warp < dwarps;
+    float x[E];
+    uint32_t key[E];
+    uint32_t fr = 0u;                                  // bit e: column c0 + e is unmasked
+    if (dw) {
+        if (c0 + E <= n && (reinterpret_cast<uintptr_t>(sc) & 15u) == 0u) {
+#pragma unroll
+            for (int v = 0; v < E / 4; ++v) {
+                const float4 f = reinterpret_cast<const float4 *>(sc + c0)[v];
+                x[4 * v] = f.x; x[4 * v + 1] = f.y; x[4 * v + 2] = f.z; x[4 * v + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) x[e] = c0 + e < n ? sc[c0 + e] : kNeg;
+        }
+        uint32_t kmin = 0xffffffffu, kmax = 0u;
+        bool bad = false;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            key[e] = order_key(x[e]);
+            const bool fin = isfinite(x[e]);
+            bad |= c0 + e < n && !fin;
+            if (c0 + e < n && fin && x[e] > kMaskedBelow) {
+                fr |= 1u << e;
+                kmin = key[e] < kmin ? key[e] : kmin;
+                kmax = key[e] > kmax ? key[e] : kmax;
+            }
+        }
+        // count of unmasked columns (< 2^16 per warp) and a non-finite flag in one word
+        const uint32_t cw = (uint32_t)__popc(fr) + (bad ? 0x10000u : 0u);
+        kmin = __reduce_min_sync(0xffffffffu, kmin);
+        kmax = __reduce_max_sync(0xffffffffu, kmax);
+        const uint32_t cs = __reduce_add_sync(0xffffffffu, cw);
+        if (lane == 0) part[warp] = make_uint2(kmin, kmax), pcnt[warp] = cs;
+    }
+    for (int e = tid; e < kBins / 4; e += NT) reinterpret_cast<uint4 *>(hist)[e] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) sh.ncand = 0u;
+    group_sync<NT, BAR>();                                                  // 1
+    float smin, scale;
+    uint32_t nfree, anybad;
+    {
+        const uint2 pw = lane < dwarps ? part[lane] : make_uint2(0xffffffffu, 0u);
+        const uint32_t pc = lane < dwarps ? pcnt[lane] : 0u;
+        const uint32_t kmin = __reduce_min_sync(0xffffffffu, pw.x);
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, pw.y);
+        const uint32_t csum = __reduce_add_sync(0xffffffffu, pc);  // nfree <= n < 2^16
+        nfree = csum & 0xffffu;
+        anybad = csum >> 16;
+        smin = key_to_float(kmin);
+        const float smax = key_to_float(kmax);
+        scale = (float)(kBins - 1) / (smax - smin);
+        anybad |= !(smax > smin) || !isfinite(scale);   // (nearly) all equal: general select
+    }
+    if (anybad || nfree < (uint32_t)kout) {
+        group_sync<NT, BAR>();
+        return false;
+    }
+    // value bins: non-decreasing in the score, equal scores share a bin
+    uint32_t bin[E];
+    if (dw) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int bi = (int)((x[e] - smin) * scale);
+            bin[e] = (uint32_t)(bi < 0 ? 0 : (bi > kBins - 1 ? kBins - 1 : bi));
+            if ((fr >> e) & 1u) atomicAdd(&hist[bin[e]], 1u);
+        }
+    }
+    group_sync<NT, BAR>();                                                  // 2
+    if (warp == 0) {
+        // lane l scans bins 511 - 16 l down to 496 - 16 l
+        uint32_t pre[16];                              // inclusive prefix, descending bins
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint4 h = reinterpret_cast<const uint4 *>(hist + kBins - 16 * (lane + 1))[v];
+            pre[15 - 4 * v] = h.x; pre[14 - 4 * v] = h.y; pre[13 - 4 * v] = h.z; pre[12 - 4 * v] = h.w;
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1)
+#pragma unroll
+            for (int t = 15; t >= o; --t) pre[t] += pre[t - o];
+        const uint32_t tot = pre[15];
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const uint32_t excl = incl - tot;
+        if (excl < (uint32_t)kout && (uint32_t)kout <= incl) {
+            // the first t whose inclusive count reaches kout: the count of those below it
+            const uint32_t need = (uint32_t)kout - excl;
+            uint32_t t0 = 0u, before = 0u;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) t0 += pre[t] < need ? 1u : 0u;
+#pragma unroll
+            for (int t = 1; t < 16; ++t) before = (uint32_t)t == t0 ? pre[t - 1] : before;
+            sh.prefix = (uint32_t)(kBins - 1 - 16 * lane) - t0;
+            sh.kk = need - before;
+        }
+    }
+    group_sync<NT, BAR>();                                                  // 3
+    const uint32_t tb = sh.prefix, kk = sh.kk;
+    uint32_t sel = 0u, mine = 0u;                      // bit e: selected / a tb candidate
+    if (dw) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const bool f = (fr >> e) & 1u;
+            if (f && bin[e] > tb) sel |= 1u << e;
+            if (f && bin[e] == tb) mine |= 1u << e;
+        }
+        if (mine) {
+            uint32_t at = atomicAdd(&sh.ncand, (uint32_t)__popc(mine));
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                if ((mine >> e) & 1u) {
+                    if (at < (uint32_t)kSmallCand) cand[at] = make_uint2((uint32_t)(c0 + e), key[e]);
+                    ++at;
+                }
+        }
+    }
+    group_sync<NT, BAR>();                                                  // 4
+    const uint32_t m = sh.ncand;
+    if (m > (uint32_t)kSmallCand) {
+        group_sync<NT, BAR>();
+        return false;
+    }
+    if (mine) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            if ((mine >> e) & 1u) {
+                const uint32_t k0 = key[e], col = (uint32_t)(c0 + e);
+                uint32_t r = 0u;
+#pragma unroll 4
+                for (uint32_t d = 0; d < m; ++d) {
+                    const uint2 o = cand[d];
+                    r += (o.y > k0 || (o.y == k0 && o.x < col)) ? 1u : 0u;
+                }
+                if (r < kk) sel |= 1u << e;
+            }
+        }
+    }
+    const uint32_t cnt_t = (uint32_t)__popc(sel);
+    uint32_t excl = 0u;                                // selected columns of lower lanes
+    if (dw) {
+        const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int bit = 0; (1 << bit) <= E; ++bit)
+            excl += (uint32_t)__popc(__ballot_sync(0xffffffffu, (cnt_t >> bit) & 1u) & lt) << bit;
+        if (lane == 31) wtot[warp] = excl + cnt_t;
+    }
+    group_sync<NT, BAR>();                                                  // 5
+    if (dw) {
+        // this warp's first slot: the selected counts of the warps before it
+        const uint32_t v = lane < warp ? wtot[lane] : 0u;
+        uint32_t pos = __reduce_add_sync(0xffffffffu, v) + excl;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            if ((sel >> e) & 1u) {
+                if (pos < (uint32_t)kout) out[pos] = map((int64_t)(c0 + e));
+                ++pos;
+            }
+        }
+    }
+    return true;
+}
+
 // Top kout of n <= kSmallMax scores held in shared memory, for the common case: finite
 // scores, at least kout unmasked, a non-degenerate range and at most kSmallCand scores in
 // the k-th score's bin; anything else goes to block_topk. Warp w owns columns
@@ -308,6 +503,11 @@ __device__ void small_topk(const float *sc, int n, int kout, int32_t *out, Map m
     constexpr int NW = NT / 32, U = 4;
     const int tid = (int)threadIdx.x - TID0, lane = tid & 31, warp = tid >> 5;
     if (kout <= 0) return;
+    if (n <= 4 * NT) {
+        if (fast_topk<NT, BAR, TID0, 4>(sc, n, kout, out, map, sh)) return;
+    } else if (n <= 8 * NT) {
+        if (fast_topk<NT, BAR, TID0, 8>(sc, n, kout, out, map, sh)) return;
+    }
     const int seg = ((n + NW * 32 * U - 1) / (NW * 32 * U)) * (32 * U);
     const int lo = warp * seg, hi = lo + seg < n ? lo + seg : n;
     uint32_t *bits = reinterpret_cast<uint32_t *>(sh.cand + 2 * kSmallCand);   // selected columns

@@ -478,3 +478,57 @@ def test_block_filter_append_two_call_path():
             for j in range(data["wl"].L):
                 P.check_coarse(data, b, j, np_(prob.top_blk)[b * data["wl"].L + j], None,
                                data["wl"].index_block, data["wl"].index_keep)
+
+
+def test_selection_ties_equal_means_and_outliers():
+    """Selections where value bins cannot separate the scores. Sequences built from a few
+    distinct key rows give groups of bit-identical fine scores (64 equal ones with the k-th
+    at a group's edge, and 208 equal ones, more than a value bin resolves itself) and, with
+    16 distinct rows, block means that are all equal; a sequence whose blocks repeat with
+    period 7 ties both stages inside a group (10 blocks and 6 of 9; 6 of 10 equal fine
+    scores); one sequence holds a block of keys 1000 times larger than the rest, so the
+    other scores share a few bins. Equal scores are taken by ascending id, and the sets
+    equal the oracle's exactly (no near-ties here besides the exact ones). With 310 query
+    rows the first five are selected beside the next row's scoring and the last five by
+    the whole CTA, the two forms of the pipeline's select."""
+    B, Np = 310, 4096
+    special = [0, 1, 2, 3, 4, 304, 305, 306, 307, 308]
+    sizes = tuple(Np if b in special else 1024 for b in range(B))
+    wl = inputs.small_workload(name="ties", seed=61, B=B, H_i=64, D_i=128, index_block=64,
+                               index_keep=16, index_topk=512, q_idx_dtype="f32",
+                               key_dtype="bf16", Np=sizes, with_attention=False)
+    data = inputs.generate(wl)
+    keys = data["keys"]
+    r = np.arange(Np)
+    for b in special:
+        k0, kind = int(data["key_off"][b]), b % 304
+        if kind in (0, 1):
+            keys[k0:k0 + Np] = keys[k0 + r % (16 if kind == 0 else 5)]
+        elif kind == 2:
+            big = O.to_f64(keys[k0 + 7 * 64:k0 + 8 * 64]) * 1000.0
+            keys[k0 + 7 * 64:k0 + 8 * 64] = inputs.f32_to_bf16_bits(big.astype(np.float32))
+        elif kind == 3:                               # block beta is a copy of block beta % 7
+            keys[k0:k0 + Np] = keys[k0 + (r // 64 % 7) * 64 + r % 64]
+    prob = Problem(data)
+    cs = torch.full((B, Np // 64), 7.0, device="cuda")
+    fs = torch.full((B, 1024), 7.0, device="cuda")
+    prob.block_means()
+    prob.block_filter(cscores=cs)
+    prob.select_topk(fscores=fs)
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    tb, I, cs, fs = np_(prob.top_blk), np_(prob.I), np_(cs), np_(fs)
+    for b in (0, 304):                                # equal means: the first 16 blocks
+        assert np.all(cs[b, :64] == cs[b, 0])
+        assert np.array_equal(np.sort(tb[b]), np.arange(16))
+    for b in special + [5, 151, 152, 153, 303, 309]:
+        P.check_coarse(data, b, 0, tb[b], cs[b], 64, 16)
+        P.check_fine(data, b, 0, tb[b], I[b], fs[b], 64, 512)
+        s = P.seq(data, b)
+        q, w = data["q_idx"][b, 0], data["w"][b, 0]
+        if b % 304 != 1:     # rotated copies of rows round their block sums differently
+            _, c_top = O.hisa_coarse(q, w, O.block_means(s["keys"], 64), 16, 64)
+            assert set(tb[b].tolist()) == set(c_top.tolist()), f"top_blk[{b}]"
+        _, _, f_top = O.hisa_fine(q, w, s["keys"], np.sort(tb[b]), 64, 512)
+        assert set(I[b].tolist()) == set(f_top.tolist()), f"I[{b}]"
+        assert np.all(np.diff(I[b]) > 0)              # ascending ids
