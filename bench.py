@@ -385,6 +385,16 @@ def run_gpu(args, wl, R):
         for name in stages:
             calls[name](stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    scrub = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2(write_only=False):
+        """Evict the step's inputs from L2: write a buffer larger than L2, then read another
+        one, so that L2 holds clean lines of neither (a step does not write back the flush's
+        dirty lines). write_only keeps the dirty lines, for the comparison line."""
+        flush.zero_()
+        if not write_only:
+            torch.sum(scrub, dim=0, out=sink)
 
     def step(evs=None):
         """One step from the per-stage graphs, with an event after every stage."""
@@ -397,9 +407,9 @@ def run_gpu(args, wl, R):
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            flush.zero_()
+            flush_l2()
             g_step.replay()
-            flush.zero_()
+            flush_l2()
             step()
     stream.synchronize()
     assert prob.status(stream) == 0, "device status flags set during warm-up"
@@ -408,6 +418,8 @@ def run_gpu(args, wl, R):
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(K)]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    wo_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(K)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -416,18 +428,24 @@ def run_gpu(args, wl, R):
         t_wall = time.perf_counter()
         with torch.cuda.stream(stream):
             for i in range(K):                      # headline: whole-step graph
-                flush.zero_()                       # L2 flush outside the step's events
+                flush_l2()                          # L2 flush outside the step's events
                 step_ev[i][0].record(stream)
                 g_step.replay()
                 step_ev[i][1].record(stream)
             for i in range(K):                      # stage times: per-stage graphs
-                flush.zero_()
+                flush_l2()
                 step(evs[i])
+            for i in range(K):                      # the same step after a write-only flush
+                flush_l2(write_only=True)
+                wo_ev[i][0].record(stream)
+                g_step.replay()
+                wo_ev[i][1].record(stream)
         stream.synchronize()
         t_wall = time.perf_counter() - t_wall
         clk.mark_stop()
     torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    wo_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in wo_ev), dev) / K
     stage_ms = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]
                 for j, name in enumerate(stages)}
     total_ms = max_over_ranks(sum(step_ms), dev)
@@ -445,7 +463,7 @@ def run_gpu(args, wl, R):
               for _ in range(K)]
     with torch.cuda.stream(stream):
         for i in range(K):
-            flush.zero_()
+            flush_l2()
             e2e_ev[i][0].record(stream)
             prob.q_idx.copy_(host_in["q_idx"], non_blocking=True)
             prob.w.copy_(host_in["w"], non_blocking=True)
@@ -474,15 +492,18 @@ def run_gpu(args, wl, R):
         "config": {"workload": f"v4flash_decode x R={R} independent sequences per GPU "
                                f"(Np={args.Np} each, H_i=64x128, b=64, keep=16, k=512, "
                                f"H=64x512 bf16, W=128)",
-                   "R": R, "Np": int(args.Np), "l2": "256 MiB L2 flush between steps; "
-                                               f"{step_bytes * R / 1e6:.0f} MB touched per step"},
+                   "R": R, "Np": int(args.Np),
+                   "l2": "L2 flush between steps: 256 MiB written, then 256 MiB read (no step "
+                         "input and no dirty flush line in L2 when a step starts); "
+                         f"{step_bytes * R / 1e6:.0f} MB touched per step"},
+        "ms_per_step_after_write_only_flush": wo_ms,
         "step_hbm_gbs": step_bytes * R / (ms_per_step / 1e3) / 1e9,
         "step_bytes_per_query": step_bytes,
         "stages_us": {n: v * 1e3 for n, v in stage_avg.items()},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic},
-        "gpu_launches": 2 * K * launches_per_step(prob),   # whole-step pass + per-stage pass
+        "gpu_launches": 3 * K * launches_per_step(prob),   # whole-step, per-stage, write-only passes
         "e2e": {"value": job_value(world, R, 1, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "wall_s": t_wall,
