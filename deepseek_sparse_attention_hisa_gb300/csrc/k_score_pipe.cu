@@ -47,8 +47,13 @@ constexpr int pipe_threads() { return MODE == kCoarse ? (kWarpCvt + kCvtWarps) *
 // ---- shared memory (offsets from the 1024-aligned base) ----
 constexpr uint32_t kQPlane = kH * kD * 2;                 // [64 heads x 128 dims] bf16, 16 KiB
 constexpr uint32_t kOffQ = 0;                             // up to 3 planes, stacked along N
-constexpr uint32_t kOffReg = 3 * kQPlane;                 // streaming region
-constexpr int kFineSlots = 4;
+// fine: two q buffers, so the next query's planes are written while this one streams;
+// coarse keeps one (its shared memory holds the raw and converted means instead)
+template <int MODE>
+constexpr int q_bufs() { return MODE == kFine ? 2 : 1; }
+template <int MODE>
+constexpr uint32_t off_reg() { return q_bufs<MODE>() * 3 * kQPlane; }   // streaming region
+constexpr int kFineSlots = 3;
 constexpr uint32_t kTileBytes = kM * kD * 2;              // fine: one [128 x 128] bf16 key tile
 constexpr uint32_t kRawBytes = kM * 64 * 4;               // coarse: f32 means, 128 rows x 64 dims
 constexpr uint32_t kHalfPlane = kM * 128;                 // [128 rows x 64 dims] bf16, 16 KiB
@@ -60,7 +65,9 @@ template <int MODE>
 constexpr uint32_t region_bytes() {
     return MODE == kCoarse ? kRawSlots * kRawBytes + kPlaneSets * kPlaneSet : kFineSlots * kTileBytes;
 }
+constexpr uint32_t kOffReg = 3 * kQPlane;                 // coarse streaming region
 constexpr uint32_t kOffPlanes = kOffReg + kRawSlots * kRawBytes;
+static_assert(off_reg<kCoarse>() == kOffReg, "coarse layout");
 
 struct QMeta {            // one query row, double-buffered
     int row;              // b * L + j
@@ -74,15 +81,15 @@ struct QMeta {            // one query row, double-buffered
 };
 
 // barriers
-constexpr int kBarMetaFull = 0, kBarSlotFree = 2, kBarQFull = 4, kBarQEmpty = 5,
-              kBarAccFull = 6, kBarAccEmpty = 8, kBarScFull = 10, kBarDrain = 12,
-              kBarFull = 13,                                // fine: kFineSlots; coarse: 2 planes
-              kBarEmpty = kBarFull + kFineSlots, kBarMeansReady = kBarEmpty + kFineSlots,
+constexpr int kBarMetaFull = 0, kBarSlotFree = 2, kBarQFull = 4, kBarQEmpty = 6,
+              kBarAccFull = 8, kBarAccEmpty = 10, kBarScFull = 12, kBarDrain = 14,
+              kBarFull = 15,                                // fine: kFineSlots; coarse: 4
+              kBarEmpty = kBarFull + 4, kBarMeansReady = kBarEmpty + 4,
               kNumBars = kBarMeansReady + 2;
 
 template <int MODE>
 struct Layout {
-    static constexpr uint32_t meta = kOffReg + region_bytes<MODE>();
+    static constexpr uint32_t meta = off_reg<MODE>() + region_bytes<MODE>();
     static constexpr uint32_t bars = meta + 2 * sizeof(QMeta);
     static constexpr uint32_t misc = bars + kNumBars * 8;
     static constexpr uint32_t sc = (misc + 64 + 15) & ~15u;   // 2 x n_cap floats
@@ -91,13 +98,23 @@ struct Layout {
 
 // Largest scored-row count one query may have: shared memory holds two score rows.
 constexpr int kPipeMaxCoarse = 1024;
-constexpr int kPipeMaxFine = 64 * 64;
+constexpr int kPipeMaxFine = 48 * 64;
 static_assert(kPipeMaxFine <= kSmallMax && kPipeMaxCoarse <= kSmallMax, "select capacity");
 
 struct Misc {
     uint32_t tmem;
     int abort;
 };
+
+// 227 KiB of shared memory per CTA: the layout, two score rows at capacity and the static
+// select state (kept blocks and SelectShared of the whole CTA)
+template <int MODE>
+constexpr bool fits() {
+    constexpr int cap = MODE == kCoarse ? kPipeMaxCoarse : kPipeMaxFine;
+    return Layout<MODE>::fixed + 2 * cap * 4 + sizeof(SelectShared<pipe_threads<MODE>()>) + 256 <=
+           227 * 1024;
+}
+static_assert(fits<kCoarse>() && fits<kFine>(), "shared memory");
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
     return mbar_wait_abortable(bar, parity, abort);
@@ -164,6 +181,7 @@ template <int MODE, bool QBF16>
 __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     k_score_pipe(const __grid_constant__ ScoreTcParams P) {
     constexpr int NQ = QBF16 ? 1 : 3;                       // q planes
+    constexpr int kQB = q_bufs<MODE>();
     using Lay = Layout<MODE>;
     const ScoreParams &p = P.s;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -192,7 +210,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) {
             uint32_t cnt = 1;
-            if (b == kBarQFull || b == kBarAccEmpty || b == kBarAccEmpty + 1 || b == kBarScFull ||
+            if (b == kBarQFull || b == kBarQFull + 1 || b == kBarAccEmpty || b == kBarAccEmpty + 1 || b == kBarScFull ||
                 b == kBarScFull + 1 || b == kBarMeansReady || b == kBarMeansReady + 1)
                 cnt = kGroup;
             // coarse: Full / Empty + 0, 1 guard the plane sets, + 2, 3 the raw slots
@@ -308,14 +326,15 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 M.V = p.causal ? visible_len(t_row, p.r, Np) : Np;
                 mbar_arrive(&bars[kBarMetaFull + qb]);
                 // the q planes are free once the previous query's MMAs are done
-                w2 = i < 1 || wait_bar(&bars[kBarQEmpty], (i - 1) & 1, abort);
+                w2 = i < kQB || wait_bar(&bars[kBarQEmpty + i % kQB], (i / kQB - 1) & 1, abort);
             }
             if (!group_all(kBarBld, kGroup, w2)) { fail(); break; }
+            const uint32_t qoff = kOffQ + (uint32_t)(i % kQB) * (3 * kQPlane);
             if (QBF16) {
 #pragma unroll
                 for (int m = 0; m < kQU; ++m) {
                     const int u = bt + m * kGroup;
-                    *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(0, u >> 4, u & 15, NQ)) = qh[m];
+                    *reinterpret_cast<uint4 *>(smem + qoff + q_off(0, u >> 4, u & 15, NQ)) = qh[m];
                 }
             } else {
                 auto put = [&](int m, const float4 &a, const float4 &b) {
@@ -325,7 +344,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                     split3(x, pl);
 #pragma unroll
                     for (int k = 0; k < 3; ++k)
-                        *reinterpret_cast<uint4 *>(smem + kOffQ + q_off(k, u >> 4, u & 15, NQ)) = pl[k];
+                        *reinterpret_cast<uint4 *>(smem + qoff + q_off(k, u >> 4, u & 15, NQ)) = pl[k];
                 };
 #pragma unroll
                 for (int m = 0; m < kQHeld; ++m) put(m, qf[2 * m], qf[2 * m + 1]);
@@ -340,7 +359,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 }
             }
             fence_async_smem();
-            mbar_arrive(&bars[kBarQFull]);
+            mbar_arrive(&bars[kBarQFull + i % kQB]);
             if (MODE == kCoarse && P.append_keys) {
                 // block means of the newly completed blocks [first_block, nb): thread bt owns
                 // dims 8 (bt / 8) .. + 7 of rows bt % 8 + 8 m; eight partial sums in row order,
@@ -402,7 +421,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                         break;
                     }
                     const int nblk = p.keep - 2 * t < 2 ? p.keep - 2 * t : 2;
-                    const uint32_t slot = sbase + kOffReg + s * kTileBytes;
+                    const uint32_t slot = sbase + off_reg<MODE>() + s * kTileBytes;
                     mbar_arrive_expect_tx(&bars[kBarFull + s], (uint32_t)nblk * 16384u);
                     for (int hb = 0; hb < nblk; ++hb) {
                         const int32_t y = (int32_t)(M.base + (int64_t)M.blk[2 * t + hb] * 64);
@@ -466,16 +485,17 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
         const uint32_t id_all = idesc_bf16_f32(kM, 64 * NQ, 0, 0);
         const uint32_t id_two = idesc_bf16_f32(kM, 64 * (NQ > 1 ? NQ - 1 : 1), 0, 0);
         const uint32_t id_one = idesc_bf16_f32(kM, 64, 0, 0);
-        const uint64_t qd = smem_desc_sw128(sbase + kOffQ, 16, 1024);
+
         uint32_t g = 0, gs = 0, u = 0;                       // tiles, fine slots, coarse halves
         for (int i = 0; i < nql && ok; ++i) {
             const int qb = i & 1;
             if (!wait_bar_warp(&bars[kBarMetaFull + qb], (i >> 1) & 1, abort) ||
-                !wait_bar_warp(&bars[kBarQFull], i & 1, abort)) {
+                !wait_bar_warp(&bars[kBarQFull + i % kQB], (i / kQB) & 1, abort)) {
                 fail();
                 break;
             }
             fence_after_sync();
+            const uint64_t qd = smem_desc_sw128(sbase + kOffQ + (uint32_t)(i % kQB) * (3 * kQPlane), 16, 1024);
             const QMeta &M = meta[qb];
             const int T = M.state ? 0 : M.T;
             for (int t = 0; t < T; ++t, ++g) {
@@ -493,7 +513,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                         break;
                     }
                     fence_after_sync();
-                    const uint64_t rd = smem_desc_sw128(sbase + kOffReg + s * kTileBytes, 16, 1024);
+                    const uint64_t rd = smem_desc_sw128(sbase + off_reg<MODE>() + s * kTileBytes, 16, 1024);
 #pragma unroll
                     for (int ks = 0; ks < kD / 16; ++ks) {
                         const uint32_t ko = ks >> 2, kb = (ks & 3) * 32;
@@ -525,7 +545,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 mma_commit_warp(&bars[kBarAccFull + ab]);
             }
             if (!ok) break;
-            mma_commit_warp(&bars[kBarQEmpty]);
+            mma_commit_warp(&bars[kBarQEmpty + i % kQB]);
         }
         mma_commit_warp(&bars[kBarDrain]);
         mbar_wait(&bars[kBarDrain], 0, 1u << 24);
@@ -710,7 +730,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
 int score_pipe_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b, int keep) {
     if (H_i != kH || D_i != kD || n_max < 1) return 0;
     if (mode == kCoarse) return !rows_bf16 && n_max <= kPipeMaxCoarse;
-    if (mode == kFine) return rows_bf16 && b == 64 && keep >= 1 && keep <= 64 && n_max <= kPipeMaxFine;
+    if (mode == kFine) return rows_bf16 && b == 64 && keep >= 1 && keep <= 48 && n_max <= kPipeMaxFine;
     return 0;
 }
 

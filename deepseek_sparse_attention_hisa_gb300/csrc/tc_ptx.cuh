@@ -259,6 +259,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// Hint: bring [src, src + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                 :: "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes) : "memory");
+}
+
 // ---- cp.async (16-byte global -> shared copies) ---------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void *g) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(saddr), "l"(g) : "memory");
