@@ -10,8 +10,8 @@
 // form a pipeline, so that one query's set-up and top-k overlap the next query's
 // streaming and only the first set-up and the last top-k are exposed:
 //   warp 0      MMA issue (one elected lane) and TMEM owner
-//   warp 1      fine: TMA producer of the kept blocks' bf16 key tiles; coarse: bulk
-//               copies of the block means (256-byte row halves) into three raw slots
+//   warp 1      fine: TMA producer of the kept blocks' bf16 key tiles; coarse: TMA of
+//               the f32 block means, [128 rows x 32 dims] boxes into four raw slots
 //   warps 2-5   epilogue: TMEM -> relu, head weights, head sum -> scores in shared memory
 //   warps 6-9   builders: per-query checks, kept blocks, head weights, q planes
 //   warps 10-13 select: block top-k over the finished query's scores (named barrier 1)
@@ -55,10 +55,10 @@ template <int MODE>
 constexpr uint32_t off_reg() { return q_bufs<MODE>() * 3 * kQPlane; }   // streaming region
 constexpr int kFineSlots = 3;
 constexpr uint32_t kTileBytes = kM * kD * 2;              // fine: one [128 x 128] bf16 key tile
-constexpr uint32_t kRawBytes = kM * 64 * 4;               // coarse: f32 means, 128 rows x 64 dims
+constexpr uint32_t kRawBytes = kM * 32 * 4;               // coarse: f32 means, 128 rows x 32 dims
 constexpr uint32_t kHalfPlane = kM * 128;                 // [128 rows x 64 dims] bf16, 16 KiB
 constexpr uint32_t kPlaneSet = 3 * kHalfPlane;            // its three planes
-constexpr int kRawSlots = 2;                              // coarse raw units in flight
+constexpr int kRawSlots = 4;                              // coarse raw boxes in flight
 constexpr int kPlaneSets = 2;                             // coarse converted units
 // coarse: kRawSlots raw f32 units, then kPlaneSets plane sets; fine: the key tile ring
 template <int MODE>
@@ -83,8 +83,8 @@ struct QMeta {            // one query row, double-buffered
 // barriers
 constexpr int kBarMetaFull = 0, kBarSlotFree = 2, kBarQFull = 4, kBarQEmpty = 6,
               kBarAccFull = 8, kBarAccEmpty = 10, kBarScFull = 12, kBarDrain = 14,
-              kBarFull = 15,                                // fine: kFineSlots; coarse: 4
-              kBarEmpty = kBarFull + 4, kBarMeansReady = kBarEmpty + 4,
+              kBarFull = 15,                // fine: kFineSlots; coarse: 2 plane sets, 4 raw slots
+              kBarEmpty = kBarFull + 6, kBarMeansReady = kBarEmpty + 6,
               kNumBars = kBarMeansReady + 2;
 
 template <int MODE>
@@ -213,9 +213,9 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             if (b == kBarQFull || b == kBarQFull + 1 || b == kBarAccEmpty || b == kBarAccEmpty + 1 || b == kBarScFull ||
                 b == kBarScFull + 1 || b == kBarMeansReady || b == kBarMeansReady + 1)
                 cnt = kGroup;
-            // coarse: Full / Empty + 0, 1 guard the plane sets, + 2, 3 the raw slots
+            // coarse: Full / Empty + 0, 1 guard the plane sets, + 2 .. 5 the raw slots
             if (MODE == kCoarse && (b == kBarFull || b == kBarFull + 1)) cnt = kCvtThreads;
-            if (MODE == kCoarse && (b == kBarEmpty + 2 || b == kBarEmpty + 3)) cnt = kCvtThreads;
+            if (MODE == kCoarse && b >= kBarEmpty + 2 && b < kBarEmpty + 2 + kRawSlots) cnt = kCvtThreads;
             mbar_init(&bars[b], cnt);
         }
         mbar_fence_init();
@@ -438,11 +438,12 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
         }
     } else if (MODE == kCoarse && warp == kWarpTma) {
         // ---------------- coarse loader: block means by TMA ----------------
-        // Unit = one K half (64 dims) of one 128-row tile, into raw slot u % kRawSlots as two
-        // 128B-swizzled [128 rows x 32 dims] f32 boxes. Rows past the allocation read as 0;
-        // rows past the query's blocks are other data and never scored.
+        // Box v = one K quarter (32 dims) of one 128-row tile, a 128B-swizzled [128 rows x 32
+        // dims] f32 box into raw slot v % kRawSlots; small slots keep more bytes in flight
+        // beside the one being converted. Rows past the allocation read as 0; rows past the
+        // query's blocks are other data and never scored.
         if (lane == 0) {
-            uint32_t u = 0;                                    // units issued
+            uint32_t u = 0;                                    // boxes issued
             for (int i = 0; i < nql && ok; ++i) {
                 const int qb = i & 1;
                 if (!wait_bar(&bars[kBarMetaFull + qb], (i >> 1) & 1, abort)) { fail(); break; }
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                         fail();
                         break;
                     }
-                    for (int h = 0; h < 2; ++h, ++u) {
+                    for (int h = 0; h < 4; ++h, ++u) {
                         const uint32_t slot = u % kRawSlots, use = u / kRawSlots;
                         if (use >= 1 && !wait_bar(&bars[kBarEmpty + 2 + slot], (use - 1) & 1, abort)) {
                             fail();
@@ -469,10 +470,8 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                         }
                         mbar_arrive_expect_tx(&bars[kBarFull + 2 + slot], kRawBytes);
                         const int32_t y = (int32_t)(M.base + (int64_t)t * kM);
-#pragma unroll
-                        for (int c2 = 0; c2 < 2; ++c2)
-                            tma_load_2d(sbase + kOffReg + slot * kRawBytes + c2 * (kM * 128), &P.means_map,
-                                        h * 64 + c2 * 32, y, &bars[kBarFull + 2 + slot]);
+                        tma_load_2d(sbase + kOffReg + slot * kRawBytes, &P.means_map, h * 32, y,
+                                    &bars[kBarFull + 2 + slot]);
                     }
                 }
             }
@@ -632,22 +631,21 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     }
     else if (MODE == kCoarse && warp >= kWarpCvt && warp < kWarpCvt + kCvtWarps) {
         // ---------------- converters: f32 means -> three bf16 planes ----------------------
-        // Thread ct converts the 16-byte pieces c = m * kCvtThreads + ct (m < 8) of a raw
-        // unit: box c / 1024, row (c % 1024) / 8, dims 32 (c / 1024) + 4 (c % 8) .. + 3; a warp
-        // reads four whole swizzled rows (no bank conflict).
-        constexpr int kChunks = kM * 16 / kCvtThreads;          // 8
+        // Box v (32 dims of a tile) fills columns 32 (v % 2) .. + 31 of plane set (v / 2) % 2;
+        // thread ct converts the 16-byte pieces c = m * kCvtThreads + ct (m < 4): row c / 8,
+        // dims 4 (c % 8) .. + 3; a warp reads four whole swizzled rows (no bank conflict).
+        constexpr int kChunks = kM * 8 / kCvtThreads;           // 4
         const int ct = tid - kWarpCvt * 32;
-        uint32_t u = 0;                                        // units converted
+        uint32_t v = 0;                                        // boxes converted
         for (int i = 0; i < nql && ok; ++i) {
             const int qb = i & 1;
             if (!wait_bar(&bars[kBarMetaFull + qb], (i >> 1) & 1, abort)) { fail(); break; }
             const QMeta &M = meta[qb];
-            const int nunits = M.state ? 0 : 2 * M.T;
-            for (int e = 0; e < nunits; ++e, ++u) {
-                const uint32_t slot = u % kRawSlots;
-                const uint32_t pb = u & 1;
-                if (!wait_bar(&bars[kBarFull + 2 + slot], (u / kRawSlots) & 1, abort) ||
-                    (u >= 2 && !wait_bar(&bars[kBarEmpty + pb], ((u >> 1) - 1) & 1, abort))) {
+            const int nbox = M.state ? 0 : 4 * M.T;
+            for (int e = 0; e < nbox; ++e, ++v) {
+                const uint32_t slot = v % kRawSlots, hv = v >> 1, pb = hv & 1, col = (v & 1) * 32;
+                if (!wait_bar(&bars[kBarFull + 2 + slot], (v / kRawSlots) & 1, abort) ||
+                    ((v & 1) == 0 && hv >= 2 && !wait_bar(&bars[kBarEmpty + pb], ((hv >> 1) - 1) & 1, abort))) {
                     fail();
                     break;
                 }
@@ -655,37 +653,38 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 uint8_t *planes = smem + kOffPlanes + pb * kPlaneSet;
 #pragma unroll
                 for (int m = 0; m < kChunks; ++m) {
-                    const int c = m * kCvtThreads + ct, bx = c >> 10, r = (c >> 3) & 127, v = c & 7;
-                    const float4 a = *reinterpret_cast<const float4 *>(
-                        rawb + bx * (kM * 128) + r * 128 + ((v ^ (r & 7)) << 4));
+                    const int c = m * kCvtThreads + ct, r = c >> 3, pv = c & 7;
+                    const float4 a = *reinterpret_cast<const float4 *>(rawb + r * 128 + ((pv ^ (r & 7)) << 4));
                     // exact split by truncation: hi = top 8 significant bits, then the same
                     // of the (exact) remainder; the last remainder has at most 8 bits left
                     uint32_t w[3][2];
                     const float xs[4] = {a.x, a.y, a.z, a.w};
                     uint32_t pk[3][4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t b0 = __float_as_uint(xs[e]) & 0xffff0000u;
-                        const float r1 = xs[e] - __uint_as_float(b0);
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t b0 = __float_as_uint(xs[q]) & 0xffff0000u;
+                        const float r1 = xs[q] - __uint_as_float(b0);
                         const uint32_t b1 = __float_as_uint(r1) & 0xffff0000u;
                         const float r2 = r1 - __uint_as_float(b1);
-                        pk[0][e] = b0;
-                        pk[1][e] = b1;
-                        pk[2][e] = __float_as_uint(r2);
+                        pk[0][q] = b0;
+                        pk[1][q] = b1;
+                        pk[2][q] = __float_as_uint(r2);
                     }
 #pragma unroll
                     for (int k = 0; k < 3; ++k) {
                         w[k][0] = __byte_perm(pk[k][0], pk[k][1], 0x7632);   // {hi(e0), hi(e1)}
                         w[k][1] = __byte_perm(pk[k][2], pk[k][3], 0x7632);
                     }
-                    const uint32_t off = sw128_offset((uint32_t)r, (uint32_t)(bx * 32 + v * 4));
+                    const uint32_t off = sw128_offset((uint32_t)r, col + (uint32_t)pv * 4);
 #pragma unroll
                     for (int k = 0; k < 3; ++k)
                         *reinterpret_cast<uint2 *>(planes + k * kHalfPlane + off) = make_uint2(w[k][0], w[k][1]);
                 }
-                fence_async_smem();
-                mbar_arrive(&bars[kBarFull + pb]);
                 mbar_arrive(&bars[kBarEmpty + 2 + slot]);
+                if (v & 1) {
+                    fence_async_smem();
+                    mbar_arrive(&bars[kBarFull + pb]);
+                }
             }
         }
     }
