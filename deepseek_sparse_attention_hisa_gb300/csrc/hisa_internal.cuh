@@ -63,16 +63,20 @@ __device__ __forceinline__ int64_t visible_len(int64_t t, int r, int64_t Np) {
 
 // Sequence b's pooled rows [off[b], off[b+1]) are usable iff they are ordered, fit Np_max
 // and lie inside the allocation of `rows` rows.
-__device__ __forceinline__ bool seq_ok(const int64_t *off, int b, int64_t Np_max, int64_t rows) {
-    const int64_t a = off[b], e = off[b + 1];
+__device__ __forceinline__ bool seq_ok_v(int64_t a, int64_t e, int64_t Np_max, int64_t rows) {
     return a >= 0 && e >= a && e - a <= Np_max && e <= rows;
+}
+__device__ __forceinline__ bool seq_ok(const int64_t *off, int b, int64_t Np_max, int64_t rows) {
+    return seq_ok_v(off[b], off[b + 1], Np_max, rows);
 }
 
 // Sequence b's nb block-mean rows [moff[b], moff[b] + nb) fit its offsets and lie inside
 // the rows allocated in the block-mean array.
-__device__ __forceinline__ bool means_ok(const int64_t *moff, int b, int64_t nb, int64_t rows) {
-    const int64_t a = moff[b], e = moff[b + 1];
+__device__ __forceinline__ bool means_ok_v(int64_t a, int64_t e, int64_t nb, int64_t rows) {
     return a >= 0 && e - a >= nb && a + nb <= rows;
+}
+__device__ __forceinline__ bool means_ok(const int64_t *moff, int b, int64_t nb, int64_t rows) {
+    return means_ok_v(moff[b], moff[b + 1], nb, rows);
 }
 
 // Orderable key of an f32 score: larger float -> larger key; -0.0 == +0.0.

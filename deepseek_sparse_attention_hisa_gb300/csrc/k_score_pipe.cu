@@ -74,6 +74,7 @@ struct QMeta {            // one query row, double-buffered
     int state;            // 0: score it; else its selection is all -1
     int n;                // scored rows: blocks (coarse) or candidates (fine)
     int T;                // tiles of kM rows
+    int t_new;            // coarse, appending: the tile holding the first new block (T: none)
     long long base;       // first pooled row (fine) / first block-mean row (coarse)
     long long V;          // visible pooled rows of this query row
     int blk[64];          // kept blocks, ascending (fine)
@@ -273,6 +274,13 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             if (MODE == kFine && bt < p.keep) bv = __ldg(p.top_blk + (int64_t)row * p.keep + bt);
             // the offsets and position this row's checks need, fetched with q
             const int64_t k0 = p.key_off[bq], k1 = p.key_off[bq + 1];
+            int64_t m0 = 0, m1 = 0, fb = 0;
+            if (MODE == kCoarse) {
+                m0 = p.means_off[bq];
+                m1 = p.means_off[bq + 1];
+                if (P.append_keys && P.first_block) fb = P.first_block[bq];
+                fb = fb < 0 ? 0 : fb;
+            }
             const int64_t t_row = p.causal ? (int64_t)p.t0[bq] + j : 0;
             // meta slot qb is free once query i - 2 is selected
             const bool w1 = i < 2 || wait_bar(&bars[kBarSlotFree + qb], ((i >> 1) - 1) & 1, abort);
@@ -298,7 +306,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             if (bt == 0) {
                 int st = 0;
                 int64_t n = 0, base = k0;
-                if (!seq_ok(p.key_off, bq, p.Np_max, p.keys_rows)) {
+                if (!seq_ok_v(k0, k1, p.Np_max, p.keys_rows)) {
                     st = 1;
                     flag(p.status, HISA_DEV_BAD_OFFSETS);
                 } else if (Np < (int64_t)p.b * p.keep) {
@@ -306,8 +314,8 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                     flag(p.status, HISA_DEV_GATE);
                 } else if (MODE == kCoarse) {
                     n = Np / p.b;
-                    base = p.means_off[bq];
-                    if (!means_ok(p.means_off, bq, n, p.means_rows) || n > n_cap) {
+                    base = m0;
+                    if (!means_ok_v(m0, m1, n, p.means_rows) || n > n_cap) {
                         st = 1;
                         flag(p.status, HISA_DEV_BAD_OFFSETS);
                     }
@@ -322,6 +330,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 M.state = st;
                 M.n = (int)n;
                 M.T = (int)((n + kM - 1) / kM);
+                M.t_new = fb < n ? (int)(fb / kM) : M.T;
                 M.base = base;
                 M.V = p.causal ? visible_len(t_row, p.r, Np) : Np;
                 mbar_arrive(&bars[kBarMetaFull + qb]);
@@ -366,8 +375,6 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 // then the pairwise tree over the eight lanes of a dimension group
                 const QMeta &M = meta[qb];
                 if (!M.state) {
-                    int64_t fb = P.first_block ? (int64_t)P.first_block[bq] : 0;
-                    fb = fb < 0 ? 0 : fb;
                     const int k = bt & 7, gq = bt >> 3;
                     const uint4 *kv = reinterpret_cast<const uint4 *>(P.append_keys);
                     float *means_w = const_cast<float *>(reinterpret_cast<const float *>(p.rows));
@@ -450,13 +457,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 const QMeta &M = meta[qb];
                 const int T = M.state ? 0 : M.T;
                 // appended means: tiles from the one holding the first new block on wait for them
-                int t_new = T;
-                if (P.append_keys && T > 0) {
-                    const int row = (int)blockIdx.x + i * (int)gridDim.x;
-                    int64_t fb = P.first_block ? (int64_t)P.first_block[row / p.L] : 0;
-                    fb = fb < 0 ? 0 : fb;
-                    if (fb < M.n) t_new = (int)(fb / kM);
-                }
+                const int t_new = P.append_keys ? M.t_new : T;
                 for (int t = 0; t < T && ok; ++t) {
                     if (t == t_new && !wait_bar(&bars[kBarMeansReady + qb], (i >> 1) & 1, abort)) {
                         fail();
