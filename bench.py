@@ -302,6 +302,8 @@ def run_reference(args, wl, R):
 # GPU arm
 # ----------------------------------------------------------------------------
 def traffic_from_profile(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture, or None once the
+    kernel's sources have changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -310,7 +312,7 @@ def traffic_from_profile(kernel):
         if not ent:
             return None
         from deepseek_sparse_attention_hisa_gb300 import build
-        if ent.get("source_stamp") != build._stamp():
+        if ent.get("source_stamp") != build.kernel_stamp(kernel):
             return None
         return ent.get("bytes_per_launch")
     except Exception:
@@ -481,9 +483,9 @@ def run_gpu(args, wl, R):
     stage_avg = {n: statistics.mean(v) for n, v in stage_ms.items()}
     dom = max(stage_avg, key=stage_avg.get)
     achieved = per_stage_bytes[dom] * R / (stage_avg[dom] / 1e3) / 1e9
-    kernel_of = {"block_filter_append": "k_score_pipe (coarse, appending the newest block means)",
-                 "select_topk": "k_score_pipe (fine)", "sparse_attend": "k_attend_tc"}
-    traffic = traffic_from_profile(kernel_of[dom])
+    kernel_of = {"block_filter_append": "k_score_pipe", "select_topk": "k_score_pipe",
+                 "sparse_attend": "k_attend_tc"}
+    traffic = traffic_from_profile(kernel_of[dom]) if dom == "sparse_attend" else None
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,

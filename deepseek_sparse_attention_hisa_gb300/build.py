@@ -50,6 +50,26 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
+# The sources each profiled kernel is compiled from: its translation unit and the headers it
+# includes. A profile's counters stay valid while these bytes (and the flags) are unchanged.
+KERNEL_SOURCES = {
+    "k_attend_tc": ["k_attend_tc.cu", "hisa_internal.cuh", "tc_ptx.cuh"],
+    "k_score_pipe": ["k_score_pipe.cu", "select_core.cuh", "hisa_internal.cuh", "tc_ptx.cuh"],
+    "k_score_gemm": ["k_score_gemm.cu", "hisa_internal.cuh", "tc_ptx.cuh"],
+}
+
+
+def kernel_stamp(kernel: str) -> str:
+    """Hash of one kernel's sources and the compile flags (see KERNEL_SOURCES)."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(f.encode())
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(NVCC_FLAGS).encode())
+    return h.hexdigest()
+
+
 def build_library(force: bool = False, verbose: bool = False) -> str:
     """Compile libhisa.so in-tree if the sources changed; returns its path."""
     os.makedirs(BUILD, exist_ok=True)
