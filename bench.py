@@ -520,6 +520,9 @@ def run_gpu(args, wl, R):
                                 "sample": f"{n} queries of sequence 0 of the batch, {el:.1f} s"}
     if not args.no_prefill:
         line["prefill_scoring"] = run_prefill_scoring(args, dev, stream)
+    if not args.no_extra:
+        line["latency_one_query"] = run_latency(wl, dev, stream)
+        line["long_context_selection"] = run_long_context(dev, stream)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -566,6 +569,109 @@ def run_prefill_scoring(args, dev, stream):
             "peak_source": peak[1], "frac": flops / ms / 1e9 / peak[0]}
 
 
+class L2Flush:
+    """Evicts every input from L2 between timed iterations: a 256 MiB write, then a 256 MiB
+    read, so that L2 holds clean lines of neither (a timed region does not write back the
+    flush's own dirty lines)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self, write_only=False):
+        import torch
+        self.w.zero_()
+        if not write_only:
+            torch.sum(self.r, dim=0, out=self.sink)
+
+
+def timed_graph(g, stream, flush, n):
+    """Mean and median ms of n replays of CUDA graph g, each after an L2 flush (outside the
+    events), timed with events on the launching stream."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            flush()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+    stream.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    return statistics.mean(ms), statistics.median(ms)
+
+
+def capture(fn, stream):
+    import torch
+    with torch.cuda.stream(stream):
+        fn(stream)                                   # eager warm-up
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn(stream)
+    return g
+
+
+def run_latency(wl, dev, stream, n=50):
+    """One V4-Flash decode query (B = 1): the same three calls as the throughput step, as one
+    graph, L2 flushed before each replay."""
+    import torch
+
+    from deepseek_sparse_attention_hisa_gb300.problem import Problem
+    data = inputs.generate_device(wl.replace(B=1), device=dev, seed=2000)
+    prob = Problem(data, device=dev)
+    newest = torch.as_tensor(np.array([int(prob.nb[0]) - 1], dtype=np.int32), device=dev)
+    prob.block_means()
+    torch.cuda.synchronize()
+
+    def step(s):
+        prob.block_filter_append(first_block=newest, stream=s)
+        prob.select_topk(stream=s)
+        prob.attend(stream=s)
+    g = capture(step, stream)
+    mean, med = timed_graph(g, stream, L2Flush(dev), n)
+    assert prob.status(stream) == 0
+    return {"workload": "v4flash_decode, one query (B = 1, Np = 32768)", "us_mean": mean * 1e3,
+            "us_median": med * 1e3, "replays": n}
+
+
+def run_long_context(dev, stream, n=20):
+    """The long-context selection (Np = 262144, 1% of keys planted along q, selection only):
+    flat top-k against HiSA at keep 16 and 64 (block means cached), each timed as a graph
+    after an L2 flush; recall = |I_HiSA and I_flat| / k."""
+    import torch
+
+    from deepseek_sparse_attention_hisa_gb300.problem import Problem
+    data = inputs.generate("long_context")
+    flush = L2Flush(dev)
+    k = data["wl"].index_topk
+    flat = Problem(data, device=dev)
+    I_flat = torch.full((1, k), -1, dtype=torch.int32, device=dev)
+    g = capture(lambda s: flat.flat_topk(I=I_flat, stream=s), stream)
+    flat_ms, _ = timed_graph(g, stream, flush, n)
+    assert flat.status(stream) == 0
+    ref = set(int(x) for x in I_flat.cpu().numpy().ravel() if x >= 0)
+    out = {"workload": "long_context: Np = 262144 bf16 keys, f32 q, 1% planted, selection only",
+           "flat_us": flat_ms * 1e3, "hisa_us": {}, "recall": {}}
+    for keep in (16, 64):
+        prob = Problem(data, device=dev, index_keep=keep)
+        prob.block_means()
+        torch.cuda.synchronize()
+
+        def sel(s, prob=prob):
+            prob.block_filter(stream=s)
+            prob.select_topk(stream=s)
+        g = capture(sel, stream)
+        ms, _ = timed_graph(g, stream, flush, n)
+        assert prob.status(stream) == 0
+        got = set(int(x) for x in prob.I.cpu().numpy().ravel() if x >= 0)
+        out["hisa_us"][str(keep)] = ms * 1e3
+        out["recall"][str(keep)] = len(got & ref) / k
+    return out
+
+
 def launches_per_step(prob):
     """Kernels this library launches per step for the V4 decode shape: the coarse filter
     with the newest block means appended 1 and the fine top-k 1 (each scores and selects
@@ -588,6 +694,8 @@ def main():
     ap.add_argument("--ref-queries", type=int, default=4, help="oracle queries per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill scoring leg")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the one-query latency and long-context selection legs")
     ap.add_argument("--Np", type=int, default=32768,
                     help="pooled rows per sequence (32768 = the V4-Flash 131072-token prefix)")
     args = ap.parse_args()
