@@ -123,12 +123,40 @@ ScoreParams score_params(const hisa_index_desc *d, int mode, const void *q, cons
     return p;
 }
 
+int device_sms() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (counts[dev] == 0) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = c;
+    }
+    return counts[dev];
+}
+
+// A few long coarse / fine rows (a single long-context query, a small batch): one CTA per
+// row would leave most SMs idle, so each row's tiles are split over CTAs and a separate
+// select follows.
+bool split_rows(const hisa_index_desc *d, int mode, int64_t n) {
+    const int sms = device_sms();
+    return sms > 0 && n >= 2048 && n_rows(d) * 8 <= sms &&
+           score_tc_split_ok(mode, d->H_i, d->D_i, mode == kFine ? d->k_dtype == HISA_BF16 : 0,
+                             d->index_block);
+}
+
 // Runs one scoring pass: for the V4 indexer shape the persistent tcgen05 pipeline (coarse
 // and fine, which also select) or the per-query tcgen05 kernel, else CUDA cores. With
-// `sel` the tensor-core coarse / fine kernels also select (returns true in *fused).
+// `sel` the tensor-core coarse / fine kernels also select (returns true in *fused); with
+// `split` the rows' tiles are spread over CTAs and the scores go to p.out.
 cudaError_t run_scores(const ScoreParams &p, int32_t *sel, int k_sel, bool *fused,
-                       cudaStream_t s) {
+                       cudaStream_t s, bool split = false) {
     *fused = false;
+    if (split) {
+        ScoreTcParams t{};
+        t.s = p;
+        return launch_score_tc(t, s);
+    }
     if (sel && p.mode != kFlat &&
         score_pipe_supported(p.mode, p.H_i, p.D_i, p.rows_bf16, p.n_max, p.b, p.keep) &&
         (p.mode == kCoarse ? p.means_rows > 0 : p.keys_rows > 0)) {
@@ -272,14 +300,15 @@ hisa_status hisa_block_filter(const hisa_index_desc *d, const void *q, const flo
     if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_BLOCK_FILTER, d))) != HISA_OK)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool tc = score_tc_supported(kCoarse, d->H_i, d->D_i, 0, nb_max, d->index_block);
+    const bool split = split_rows(d, kCoarse, nb_max);
+    const bool tc = !split && score_tc_supported(kCoarse, d->H_i, d->D_i, 0, nb_max, d->index_block);
     float *buf = cscores ? cscores : (tc ? nullptr : scratch_of(ws));
     const int64_t ld = cscores ? ld_cscores : (nb_max > 0 ? nb_max : 1);
     ScoreParams p = score_params(d, kCoarse, q, w, means, 0, key_off, t0, buf, ld, ws);
     p.means_off = means_off;
     p.n_max = nb_max;
     bool fused = false;
-    cudaError_t e = run_scores(p, top_blk, d->index_keep, &fused, s);
+    cudaError_t e = run_scores(p, top_blk, d->index_keep, &fused, s, split);
     if (e != cudaSuccess) return HISA_ECUDA;
     if (fused) return HISA_OK;
     SelectParams sp{};
@@ -342,15 +371,16 @@ hisa_status hisa_select_topk(const hisa_index_desc *d, const void *q, const floa
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t C = (int64_t)d->index_block * d->index_keep;
-    const bool tc = score_tc_supported(kFine, d->H_i, d->D_i, d->k_dtype == HISA_BF16, C,
-                                       d->index_block) && d->keys_rows > 0;
+    const bool split = split_rows(d, kFine, C) && d->keys_rows > 0;
+    const bool tc = !split && score_tc_supported(kFine, d->H_i, d->D_i, d->k_dtype == HISA_BF16, C,
+                                                 d->index_block) && d->keys_rows > 0;
     float *buf = fscores ? fscores : (tc ? nullptr : scratch_of(ws));
     ScoreParams p = score_params(d, kFine, q, w, keys, d->k_dtype == HISA_BF16, key_off, t0, buf,
                                  C, ws);
     p.top_blk = top_blk;
     p.n_max = C;
     bool fused = false;
-    cudaError_t e = run_scores(p, I, d->index_topk, &fused, s);
+    cudaError_t e = run_scores(p, I, d->index_topk, &fused, s, split);
     if (e != cudaSuccess) return HISA_ECUDA;
     if (fused) return HISA_OK;
     SelectParams sp{};
@@ -384,6 +414,7 @@ hisa_status hisa_flat_topk(const hisa_index_desc *d, const void *q, const float 
     sp.k = d->index_topk;
     sp.scores = buf; sp.ld = ld; sp.key_off = key_off; sp.out = I;
     sp.Np_max = d->Np_max; sp.keys_rows = d->keys_rows; sp.status = status_of(ws);
+    sp.work = buf;                       // the scores are scratch: long rows reduce in place
     return from_cuda(launch_select(sp, d->Np_max, s));
 }
 

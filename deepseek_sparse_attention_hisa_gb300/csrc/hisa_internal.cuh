@@ -117,6 +117,11 @@ struct SelectParams {
     int B, L, b, keep, k;
     const float *scores;      // [B*L, ld]
     int64_t ld;
+    // flat rows longer than the shared-memory form holds: when work == scores (writable),
+    // each chunk of those rows is reduced in place to its top k (score, id) pairs and one
+    // CTA per row selects among them; null: one CTA per row selects over the whole row
+    float *work;
+    int smem_n;               // set by launch_select: scores its CTAs can hold in shared memory
     const int64_t *key_off;
     const int32_t *top_blk;   // fine: [B*L, keep]
     int32_t *out;             // [B*L, k]
@@ -191,6 +196,8 @@ bool encode_bf16_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t
 // ---------------------------------------------------------------------------
 cudaError_t launch_scores_simt(const ScoreParams &p, cudaStream_t s);
 cudaError_t launch_select(const SelectParams &p, int64_t n_max, cudaStream_t s);
+// whether launch_select can take flat rows of up to ld scores and k ids in chunks
+bool chunked_select_fits(int64_t ld, int k);
 cudaError_t launch_block_means(const MeansParams &p, int64_t nb_max, cudaStream_t s);
 cudaError_t launch_attend_simt(const AttnParams &p, cudaStream_t s);
 cudaError_t launch_attend_combine(const AttnParams &p, cudaStream_t s);
@@ -200,6 +207,8 @@ int attend_tc_supported(int H, int Dh, int kv_bf16);
 int attend_chunk_rows();
 cudaError_t launch_score_tc(const ScoreTcParams &p, cudaStream_t s);
 int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b);
+// coarse / fine rows split over CTAs (scores to memory, then launch_select): any n
+int score_tc_split_ok(int mode, int H_i, int D_i, int rows_bf16, int b);
 // Persistent coarse / fine scoring + select pipeline (one CTA per SM over all query rows).
 cudaError_t launch_score_pipe(const ScoreTcParams &p, cudaStream_t s);
 int score_pipe_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b, int keep);

@@ -110,6 +110,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_score_tc(const __grid_constant_
     constexpr int NQ = QBF16 ? 1 : 3;                    // q planes
     constexpr int NR = (MODE == kCoarse) ? 3 : 1;        // row planes
     const ScoreParams &p = P.s;
+    // flat, and coarse / fine for a few long rows: CTAs own ranges of tiles of a row and
+    // write its scores to p.out (selected by a later kernel); else one CTA per row selects
+    const bool split = MODE == kFlat || P.tiles_per_cta > 0;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ SelectShared<kThreads> sel_sh;
     __shared__ int s_state;
@@ -166,8 +169,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_score_tc(const __grid_constant_
         } else if (MODE != kFlat && Np < (int64_t)p.b * p.keep) {
             st = 1;
             flag(p.status, HISA_DEV_GATE);
-        } else if (MODE == kCoarse &&
-                   (!means_ok(p.means_off, bq, Np / p.b, p.means_rows) || Np / p.b > kMaxSel)) {
+        } else if (MODE == kCoarse && (!means_ok(p.means_off, bq, Np / p.b, p.means_rows) ||
+                                       (!split && Np / p.b > kMaxSel))) {
             st = 1;
             flag(p.status, HISA_DEV_BAD_OFFSETS);
         } else if (MODE == kFine) {
@@ -194,14 +197,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_score_tc(const __grid_constant_
     }
     __syncthreads();
     if (s_state) {
-        if (MODE != kFlat)
+        if (MODE != kFlat && P.sel)
             for (int e = tid; e < P.k_sel; e += kThreads) P.sel[(int64_t)row * P.k_sel + e] = -1;
         return;
     }
     const int64_t n = MODE == kFlat ? Np : (MODE == kCoarse ? Np / p.b : (int64_t)p.keep * p.b);
     const int T_all = (int)((n + kTile - 1) / kTile);
     int t_begin = 0, t_end = T_all;
-    if (MODE == kFlat) {
+    if (split) {
         t_begin = (int)blockIdx.y * P.tiles_per_cta;
         t_end = t_begin + P.tiles_per_cta < T_all ? t_begin + P.tiles_per_cta : T_all;
         if (t_begin >= t_end) return;
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_score_tc(const __grid_constant_
                     pos = (int64_t)blk[q32] * p.b + (c32 - q32 * b32);
                 }
                 const float score = pos < V ? acc : kNeg;
-                if (MODE != kFlat) sc[cidx] = score;
+                if (!split) sc[cidx] = score;
                 if (p.out) p.out[(int64_t)row * p.ld_out + cidx] = score;
             }
         }
@@ -396,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_score_tc(const __grid_constant_
         fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (MODE != kFlat) {
+    if (!split) {
         int32_t *out = P.sel + (int64_t)row * P.k_sel;
         const int aborted = misc->abort;
         const int64_t kout = aborted ? 0 : (n < P.k_sel ? n : (int64_t)P.k_sel);
@@ -424,6 +427,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_score_tc(const __grid_constant_
 
 namespace hisa {
 
+int score_tc_split_ok(int mode, int H_i, int D_i, int rows_bf16, int b) {
+    if (H_i != kH || D_i != kD) return 0;
+    if (mode == kCoarse) return !rows_bf16;
+    if (mode == kFine) return rows_bf16 && b == 64;
+    return 0;
+}
+
 int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b) {
     if (H_i != kH || D_i != kD) return 0;
     if (mode == kCoarse) return !rows_bf16 && n_max <= kMaxSel;
@@ -437,8 +447,8 @@ static cudaError_t launch_t(const ScoreTcParams &p, dim3 grid, cudaStream_t s) {
         k_score_tc<MODE, QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         (int)(kSmemFixed + kMaxSel * 4));
     if (attr != cudaSuccess) return attr;
-    // the fused select keeps n scores in shared memory; the flat mode keeps none
-    const size_t smem = kSmemFixed + (MODE == kFlat ? 0 : (size_t)p.s.n_max * 4);
+    // the fused select keeps n scores in shared memory; split launches keep none
+    const size_t smem = kSmemFixed + (p.tiles_per_cta > 0 ? 0 : (size_t)p.s.n_max * 4);
     k_score_tc<MODE, QBF16><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
@@ -450,8 +460,9 @@ cudaError_t launch_score_tc(const ScoreTcParams &p_in, cudaStream_t s) {
         !encode_bf16_map(&p.keys_map, p.s.rows, (uint64_t)p.s.keys_rows, kD, 64, 64))
         return cudaErrorInvalidValue;
     dim3 grid((unsigned)rows, 1);
-    if (p.s.mode == kFlat) {
-        const int64_t tiles = (p.s.Np_max + kTile - 1) / kTile;
+    const bool split = p.s.mode == kFlat || !p.sel;
+    if (split) {
+        const int64_t tiles = (p.s.n_max + kTile - 1) / kTile;
         if (tiles == 0) return cudaSuccess;
         int64_t tpc = (rows * tiles + kTargetCtas - 1) / kTargetCtas;
         if (tpc < 1) tpc = 1;

@@ -5,6 +5,12 @@
 
 namespace hisa {
 
+// Rows of at most kSmemSel scores are selected from shared memory (the short form); longer
+// flat rows in chunks of kChunk when the caller provides candidate space.
+constexpr int kSmemSel = 8192;
+constexpr int kChunk = 8192;
+constexpr size_t kMergeSmem = 200 * 1024;                 // candidate scores + ids of one row
+
 template <int NT>
 __global__ void __launch_bounds__(NT) k_select(SelectParams p) {
     __shared__ SelectShared<NT> sh;
@@ -52,7 +58,21 @@ __global__ void __launch_bounds__(NT) k_select(SelectParams p) {
     }
     const float *sc = p.scores + (int64_t)row * p.ld;
     const int64_t kout = n < (int64_t)p.k ? n : (int64_t)p.k;
-    if (p.mode == kFine) {
+    extern __shared__ __align__(16) float s_sc[];
+    if (n <= p.smem_n) {
+        // the row in shared memory, then the short-form select (short rows are the common case)
+        for (int64_t e = tid; e < n; e += NT) s_sc[e] = sc[e];
+        __syncthreads();
+        if (p.mode == kFine) {
+            const int b = p.b;
+            small_topk<NT, 0, 0>(s_sc, (int)n, (int)kout, out,
+                                 [&](int64_t i) { return (int32_t)((int64_t)s_blk[i / b] * b + (i % b)); },
+                                 sh, p.status);
+        } else {
+            small_topk<NT, 0, 0>(s_sc, (int)n, (int)kout, out, [](int64_t i) { return (int32_t)i; }, sh,
+                                 p.status);
+        }
+    } else if (p.mode == kFine) {
         const int b = p.b;
         block_topk<NT>(sc, n, kout, out,
                        [&](int64_t i) { return (int32_t)((int64_t)s_blk[i / b] * b + (i % b)); },
@@ -63,13 +83,119 @@ __global__ void __launch_bounds__(NT) k_select(SelectParams p) {
     for (int64_t e = kout + tid; e < p.k; e += NT) out[e] = -1;
 }
 
+// Chunked flat select, first level. CTA (row, c) owns scores [c kChunk, c kChunk + len).
+// A chunk longer than 2k is reduced in place: its top k, as (score, id) pairs in
+// ascending id order, overwrite its first 2k floats (the chunk is in shared memory by
+// then, and no other CTA touches it). Shorter chunks are left as they are. The global top
+// k lies in the union of the chunks' top k, ties included, since every chunk keeps its
+// equal scores by ascending id.
+template <int NT>
+__global__ void __launch_bounds__(NT) k_select_chunks(SelectParams p) {
+    __shared__ SelectShared<NT> sh;
+    __shared__ int32_t s_col[kMaxTopk];
+    extern __shared__ __align__(16) float s_sc[];
+    const int row = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
+    const int bq = row / p.L;
+    if (!seq_ok(p.key_off, bq, p.Np_max, p.keys_rows)) return;   // the merge flags it
+    const int64_t Np = p.key_off[bq + 1] - p.key_off[bq];
+    int64_t len = Np - (int64_t)c * kChunk;
+    len = len > kChunk ? kChunk : len;
+    if (len <= 2 * (int64_t)p.k) return;
+    float *w = p.work + (int64_t)row * p.ld + (int64_t)c * kChunk;
+    for (int64_t e = tid; e < len; e += NT) s_sc[e] = w[e];
+    __syncthreads();
+    small_topk<NT, 0, 0>(s_sc, (int)len, p.k, s_col, [](int64_t i) { return (int32_t)i; }, sh, p.status);
+    __syncthreads();
+    for (int e = tid; e < p.k; e += NT) {
+        w[2 * e] = s_sc[s_col[e]];
+        w[2 * e + 1] = __int_as_float(c * kChunk + s_col[e]);
+    }
+}
+
+// Second level: one CTA per row gathers every chunk's candidates in chunk order (so ids
+// ascend), selects the top k among them and writes their ids; bad rows are all -1.
+template <int NT>
+__global__ void __launch_bounds__(NT) k_select_merge(SelectParams p, int cap) {
+    __shared__ SelectShared<NT> sh;
+    __shared__ int s_m;
+    extern __shared__ __align__(16) float s_sc[];
+    int32_t *s_id = reinterpret_cast<int32_t *>(s_sc + cap);
+    const int row = blockIdx.x, tid = threadIdx.x;
+    const int bq = row / p.L;
+    int32_t *out = p.out + (int64_t)row * p.k;
+    int64_t n = 0;
+    if (!seq_ok(p.key_off, bq, p.Np_max, p.keys_rows)) {
+        if (tid == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
+    } else {
+        n = p.key_off[bq + 1] - p.key_off[bq];
+    }
+    const int64_t kout = n < (int64_t)p.k ? n : (int64_t)p.k;
+    const float *w = p.work + (int64_t)row * p.ld;
+    int m = 0;
+    for (int64_t c = 0; c * kChunk < n; ++c) {
+        int64_t len = n - c * kChunk;
+        len = len > kChunk ? kChunk : len;
+        const float *wc = w + c * kChunk;
+        if (len > 2 * (int64_t)p.k) {
+            for (int e = tid; e < p.k; e += NT) {
+                s_sc[m + e] = wc[2 * e];
+                s_id[m + e] = __float_as_int(wc[2 * e + 1]);
+            }
+            m += p.k;
+        } else {
+            for (int e = tid; e < (int)len; e += NT) {
+                s_sc[m + e] = wc[e];
+                s_id[m + e] = (int32_t)(c * kChunk + e);
+            }
+            m += (int)len;
+        }
+    }
+    __syncthreads();
+    if (kout > 0)
+        small_topk<NT, 0, 0>(s_sc, m, (int)kout, out, [&](int64_t i) { return s_id[i]; }, sh, p.status);
+    for (int64_t e = kout + tid; e < p.k; e += NT) out[e] = -1;
+}
+
+// Candidates of a row of at most ld scores after the first level.
+int64_t chunked_candidates(int64_t ld, int k) {
+    const int64_t nchunk = (ld + kChunk - 1) / kChunk;
+    return (nchunk - 1) * (int64_t)k + 2 * (int64_t)k;
+}
+
 cudaError_t launch_select(const SelectParams &p, int64_t n_max, cudaStream_t s) {
     const unsigned rows = (unsigned)(p.B * p.L);
-    if (n_max <= 256)
-        k_select<256><<<rows, 256, 0, s>>>(p);
-    else
-        k_select<1024><<<rows, 1024, 0, s>>>(p);
+    if (rows == 0) return cudaSuccess;
+    if (p.mode == kFlat && p.work && chunked_select_fits(p.ld, p.k) && n_max > kSmemSel) {
+        const int64_t nchunk = (p.ld + kChunk - 1) / kChunk;
+        const int cap = (int)chunked_candidates(p.ld, p.k);
+        static const cudaError_t a1 = cudaFuncSetAttribute(
+            k_select_chunks<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunk * 4);
+        static const cudaError_t a2 = cudaFuncSetAttribute(
+            k_select_merge<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMergeSmem);
+        if (a1 != cudaSuccess) return a1;
+        if (a2 != cudaSuccess) return a2;
+        k_select_chunks<1024><<<dim3(rows, (unsigned)nchunk), 1024, kChunk * 4, s>>>(p);
+        k_select_merge<1024><<<rows, 1024, (size_t)cap * 8, s>>>(p, cap);
+        return cudaGetLastError();
+    }
+    SelectParams q = p;
+    q.smem_n = n_max <= kSmemSel ? (int)n_max : 0;
+    const size_t smem = (size_t)q.smem_n * 4;
+    if (n_max <= 256) {
+        k_select<256><<<rows, 256, smem, s>>>(q);
+    } else {
+        static const cudaError_t a = cudaFuncSetAttribute(
+            k_select<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemSel * 4);
+        if (a != cudaSuccess) return a;
+        k_select<1024><<<rows, 1024, smem, s>>>(q);
+    }
     return cudaGetLastError();
+}
+
+bool chunked_select_fits(int64_t ld, int k) {
+    if (ld <= kSmemSel || k < 1 || 2 * k > kChunk || k > kMaxTopk) return false;
+    const int64_t cap = chunked_candidates(ld, k);
+    return cap <= kSmallMax && (size_t)cap * 8 <= kMergeSmem;
 }
 
 }  // namespace hisa
