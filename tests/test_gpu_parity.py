@@ -532,3 +532,32 @@ def test_selection_ties_equal_means_and_outliers():
         _, _, f_top = O.hisa_fine(q, w, s["keys"], np.sort(tb[b]), 64, 512)
         assert set(I[b].tolist()) == set(f_top.tolist()), f"I[{b}]"
         assert np.all(np.diff(I[b]) > 0)              # ascending ids
+
+
+def test_long_rows_split_scoring_and_chunked_flat_select():
+    """Few long rows: coarse and fine scoring split over CTAs with a separate select (nb and
+    keep * b of 2048 and more), and flat rows longer than 8192 selected chunk by chunk (last
+    chunks shorter and longer than 2k, and exact ties across chunks: keys repeat every 5000
+    rows in sequence 1, so equal scores straddle chunk edges and must go by ascending id)."""
+    B = 3
+    Np = (131072 + 700, 140000, 8192 * 2 + 3000)
+    wl = inputs.small_workload(name="long_rows", seed=71, B=B, H_i=64, D_i=128, index_block=64,
+                               index_keep=32, index_topk=512, q_idx_dtype="f32", key_dtype="bf16",
+                               Np=Np, with_attention=False)
+    data = inputs.generate(wl)
+    k0 = int(data["key_off"][1])
+    r = np.arange(Np[1])
+    data["keys"][k0:k0 + Np[1]] = data["keys"][k0 + r % 5000]
+    prob = Problem(data)
+    res = run_hisa(prob)
+    for b in range(B):
+        P.check_coarse(data, b, 0, res["top_blk"][b], res["cs"][b], 64, 32)
+        P.check_fine(data, b, 0, res["top_blk"][b], res["I"][b], res["fs"][b], 64, 512)
+    I, sc = run_flat(prob)
+    for b in range(B):
+        P.check_flat(data, b, 0, I[b], 512, sc[b])
+    # sequence 1: every score repeats every 5000 rows; the selection is exactly the oracle's
+    s = P.seq(data, 1)
+    o = O.flat_scores(data["q_idx"][1, :1], data["w"][1, :1], s["keys"], s["t0"], wl.r)[0]
+    assert set(I[1].tolist()) == set(O.top_k(o, 512).tolist())
+    assert np.all(np.diff(I[1]) > 0)
