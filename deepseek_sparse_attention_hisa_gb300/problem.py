@@ -83,7 +83,25 @@ class Problem:
             need = max(need, hb.workspace_bytes(hb.OP_SPARSE_ATTEND, self.adesc))
         if need == 0:
             raise ValueError("descriptor rejected by hisa_workspace_bytes")
+        self.ws_bytes = need
         self.ws = hb.alloc_workspace(need, dev)
+
+    def io_clone(self):
+        """A second set of the per-step buffers (query inputs, selections, output, workspace)
+        sharing this problem's keys, block-mean cache and KV, so that one step's inputs can be
+        copied in (or its results copied out) while another step computes."""
+        import copy
+        import torch
+        c = copy.copy(self)
+        c.q_idx = self.q_idx.clone()
+        c.w = self.w.clone()
+        c.top_blk = torch.empty_like(self.top_blk)
+        c.I = torch.empty_like(self.I)
+        if self.has_attention:
+            c.q_attn = self.q_attn.clone()
+            c.out = torch.empty_like(self.out)
+        c.ws = hb.alloc_workspace(self.ws_bytes, self.device)
+        return c
 
     # ---- stages -------------------------------------------------------------
     def block_means(self, first_block=None, stream=None):
