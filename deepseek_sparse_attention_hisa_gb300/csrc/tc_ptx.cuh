@@ -109,18 +109,12 @@ __device__ __forceinline__ void mma_bf16_warp(uint32_t d_tmem, uint64_t a_desc, 
         :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
-// Warp-wide: one elected lane commits (see mma_commit).
+// Warp-wide: one elected lane arranges an arrival (once) on mbar for when all MMAs this
+// thread issued before have completed.
 __device__ __forceinline__ void mma_commit_warp(uint64_t *mbar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
-        :: "r"(smem_u32(mbar)) : "memory");
-}
-
-// One thread: arrive (once) on an mbarrier when all previously issued MMAs complete.
-__device__ __forceinline__ void mma_commit(uint64_t *mbar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
         :: "r"(smem_u32(mbar)) : "memory");
 }
 
@@ -194,16 +188,6 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t *mbar, uint32_t parit
         : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
     return ok;
 }
-// Non-blocking test of the same condition (try_wait may hold the thread for a while).
-__device__ __forceinline__ uint32_t mbar_test_wait(uint64_t *mbar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
-    return ok;
-}
 // A waiter gives up after about kWaitCycles SM cycles (a quarter second at 2 GHz), far
 // beyond any legitimate wait of these kernels, so a stuck pipeline ends promptly.
 constexpr long long kWaitCycles = 1ll << 29;
@@ -250,21 +234,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
-// One thread: copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
-// to shared memory, counted in bytes on mbar.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *mbar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(mbar))
-        : "memory");
-}
-
-// Hint: bring [src, src + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                 :: "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes) : "memory");
-}
-
 // ---- cp.async (16-byte global -> shared copies) ---------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void *g) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(saddr), "l"(g) : "memory");
@@ -282,15 +251,6 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *mbar) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
-}
-// Close the current group of this thread's cp.async copies.
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-// Wait until at most N of this thread's committed groups are still in flight.
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 }  // namespace tc
