@@ -66,7 +66,7 @@ def kernel_stamp(kernel: str) -> str:
         h.update(f.encode())
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(fh.read())
-    h.update(" ".join(NVCC_FLAGS).encode())
+    h.update(" ".join(f for f in NVCC_FLAGS if f != INCLUDE).encode())   # not where the tree lives
     return h.hexdigest()
 
 

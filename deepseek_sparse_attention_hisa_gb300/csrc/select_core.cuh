@@ -92,8 +92,10 @@ constexpr float kMaskedBelow = -1e29f;
 // Block-wide radix select over the full keys: four 8-bit passes; resolves any input.
 // Leaves the k-th key in sh.prefix and the count of its equals to take in sh.kk.
 // The selecting threads are threadIdx.x in [TID0, TID0 + NT) (TID0 a multiple of 32).
+// The general paths below are rare (non-finite or heavily tied scores, long rows): they
+// are kept out of line so that the selecting kernels' hot code stays small.
 template <int NT, int BAR = 0, int TID0 = 0>
-__device__ void block_radix_threshold(const float *sc, int64_t n, uint32_t kout,
+__device__ __noinline__ void block_radix_threshold(const float *sc, int64_t n, uint32_t kout,
                                       SelectShared<NT> &sh) {
     const int tid = (int)threadIdx.x - TID0, lane = tid & 31, warp = tid >> 5;
     uint32_t prefix = 0u, mask = 0u, kk = kout;
@@ -120,7 +122,7 @@ __device__ void block_radix_threshold(const float *sc, int64_t n, uint32_t kout,
 // every selecting thread (threadIdx.x in [TID0, TID0 + NT)) must call it with the same
 // arguments.
 template <int NT, int BAR = 0, int TID0 = 0, typename Map>
-__device__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *out, Map map,
+__device__ __noinline__ void block_topk(const float *sc, int64_t n, int64_t kout, int32_t *out, Map map,
                            SelectShared<NT> &sh, uint32_t *status) {
     constexpr int NW = NT / 32;
     const int tid = (int)threadIdx.x - TID0, lane = tid & 31, warp = tid >> 5;
@@ -498,16 +500,28 @@ __device__ bool fast_topk(const float *sc, int n, int kout, int32_t *out, Map ma
 // Caller guarantees 0 <= kout <= n <= kSmallMax. Contains group_sync<NT, BAR>().
 constexpr int kSmallMax = (kCand - 2 * kSmallCand) * 32;
 template <int NT, int BAR, int TID0, typename Map>
+__device__ __noinline__ void small_topk_binned(const float *sc, int n, int kout, int32_t *out, Map map,
+                                               SelectShared<NT> &sh, uint32_t *status);
+
+template <int NT, int BAR, int TID0, typename Map>
 __device__ void small_topk(const float *sc, int n, int kout, int32_t *out, Map map,
                            SelectShared<NT> &sh, uint32_t *status) {
-    constexpr int NW = NT / 32, U = 4;
-    const int tid = (int)threadIdx.x - TID0, lane = tid & 31, warp = tid >> 5;
     if (kout <= 0) return;
     if (n <= 4 * NT) {
         if (fast_topk<NT, BAR, TID0, 4>(sc, n, kout, out, map, sh)) return;
     } else if (n <= 8 * NT) {
         if (fast_topk<NT, BAR, TID0, 8>(sc, n, kout, out, map, sh)) return;
     }
+    small_topk_binned<NT, BAR, TID0>(sc, n, kout, out, map, sh, status);
+}
+
+// small_topk's general form (see above): value bins over the range, the threshold bin's
+// candidates ranked exactly, block_topk for anything it does not resolve.
+template <int NT, int BAR, int TID0, typename Map>
+__device__ __noinline__ void small_topk_binned(const float *sc, int n, int kout, int32_t *out, Map map,
+                                               SelectShared<NT> &sh, uint32_t *status) {
+    constexpr int NW = NT / 32, U = 4;
+    const int tid = (int)threadIdx.x - TID0, lane = tid & 31, warp = tid >> 5;
     const int seg = ((n + NW * 32 * U - 1) / (NW * 32 * U)) * (32 * U);
     const int lo = warp * seg, hi = lo + seg < n ? lo + seg : n;
     uint32_t *bits = reinterpret_cast<uint32_t *>(sh.cand + 2 * kSmallCand);   // selected columns
