@@ -532,6 +532,7 @@ def run_gpu(args, wl, R):
     if not args.no_extra:
         line["latency_one_query"] = run_latency(wl, dev, stream)
         line["long_context_selection"] = run_long_context(dev, stream)
+        line["prefill_hisa_step"] = run_prefill_hisa(dev, stream)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -621,6 +622,37 @@ def capture(fn, stream):
     with torch.cuda.graph(g, stream=stream):
         fn(stream)
     return g
+
+
+def run_prefill_hisa(dev, stream, n=10):
+    """The HiSA batched path on the prefill workload (one sequence, L = 4096 new rows,
+    Np = 16384 pooled rows, bf16 q and keys): block means once, then per step the coarse
+    filter with per-row eligibility, the fine top-k with the causal re-mask and the sparse
+    combine over each row's window and selected rows; each stage timed as a graph after an
+    L2 flush."""
+    import torch
+
+    from deepseek_sparse_attention_hisa_gb300.problem import Problem
+    wl = inputs.WORKLOADS["prefill"]
+    data = inputs.generate_device(wl, device=dev, seed=4000)
+    prob = Problem(data, device=dev)
+    prob.block_means()
+    torch.cuda.synchronize()
+    flush = L2Flush(dev)
+    out = {"workload": "prefill: L = 4096 rows x Np = 16384 (64 x 128 indexer, bf16 q and keys), "
+                       "64 x 512 attention over 128 cached + 4096 new local rows, window 128, k = 512"}
+    total = 0.0
+    for name, fn in (("block_filter", lambda s: prob.block_filter(stream=s)),
+                     ("select_topk", lambda s: prob.select_topk(stream=s)),
+                     ("sparse_attend", lambda s: prob.attend(stream=s))):
+        g = capture(fn, stream)
+        ms, _ = timed_graph(g, stream, flush, n)
+        out[name + "_us"] = ms * 1e3
+        total += ms
+    assert prob.status(stream) == 0
+    out["step_us"] = total * 1e3
+    out["rows_per_s"] = wl.L / (total / 1e3)
+    return out
 
 
 def e2e_pipelined(prob, host_in, host_out, calls_for, K, dev):

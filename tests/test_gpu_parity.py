@@ -561,3 +561,22 @@ def test_long_rows_split_scoring_and_chunked_flat_select():
     o = O.flat_scores(data["q_idx"][1, :1], data["w"][1, :1], s["keys"], s["t0"], wl.r)[0]
     assert set(I[1].tolist()) == set(O.top_k(o, 512).tolist())
     assert np.all(np.diff(I[1]) > 0)
+
+
+@pytest.mark.parametrize("L,t0", [(1, None), (4, 3000)])
+def test_per_token_indexer_r1(L, t0):
+    """The per-token indexer variant (every token is a key, r = 1): flat scoring and top-k,
+    and the HiSA stages, on the V4 indexer shape. Decode (L = 1, V = Np) and a four-token
+    verify block whose causal edge V(t0 + j) = t0 + j + 1 falls inside the keys."""
+    wl = inputs.small_workload(name="r1", seed=81, B=2, L=L, r=1, H_i=64, D_i=128, index_block=64,
+                               index_keep=16, index_topk=512, q_idx_dtype="f32",
+                               key_dtype="bf16", Np=(4096, 3500), t0=t0, with_attention=False)
+    data = inputs.generate(wl)
+    prob = Problem(data)
+    I, sc = run_flat(prob)
+    res = run_hisa(prob)
+    for b in range(wl.B):
+        for j in range(L):
+            r_ = b * L + j
+            P.check_flat(data, b, j, I[r_], 512, sc[r_])
+    check_rows(data, prob, res, [(b, j) for b in range(wl.B) for j in range(L)])
