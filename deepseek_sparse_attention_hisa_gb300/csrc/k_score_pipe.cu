@@ -10,10 +10,13 @@
 // form a pipeline, so that one query's set-up and top-k overlap the next query's
 // streaming and only the first set-up and the last top-k are exposed:
 //   warp 0      MMA issue (one elected lane) and TMEM owner
-//   warp 1      fine: TMA producer of the kept blocks' bf16 key tiles; coarse: TMA of
-//               the f32 block means, [128 rows x 32 dims] boxes into four raw slots
+//   warp 1      fine: TMA producer of the kept blocks' bf16 key tiles (a three-slot
+//               ring); coarse: TMA of the f32 block means, [128 rows x 32 dims] boxes
+//               into four raw slots
 //   warps 2-5   epilogue: TMEM -> relu, head weights, head sum -> scores in shared memory
-//   warps 6-9   builders: per-query checks, kept blocks, head weights, q planes
+//   warps 6-9   builders: per-query checks, kept blocks, head weights, q planes (fine:
+//               two q buffers, so the next query's are written while this one streams);
+//               coarse, appending: the means of the newly completed blocks
 //   warps 10-13 select: block top-k over the finished query's scores (named barrier 1)
 //   warps 14-21 coarse: converters, f32 block means -> three bf16 planes
 //
