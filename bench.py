@@ -527,9 +527,10 @@ def run_gpu(args, wl, R):
         line["cpu_baseline"] = {"value": n / el, "unit": UNIT, "cores": cores_used(),
                                 "kind": "oracle",
                                 "sample": f"{n} queries of sequence 0 of the batch, {el:.1f} s"}
-    if not args.no_prefill:
+    # single-GPU side legs (a multi-GPU run reports the scaling line only)
+    if not args.no_prefill and world == 1:
         line["prefill_scoring"] = run_prefill_scoring(args, dev, stream)
-    if not args.no_extra:
+    if not args.no_extra and world == 1:
         line["latency_one_query"] = run_latency(wl, dev, stream)
         line["long_context_selection"] = run_long_context(dev, stream)
         line["prefill_hisa_step"] = run_prefill_hisa(dev, stream)
