@@ -28,7 +28,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kH = 64, kDH = 512, kTR = 32, kSlots = 4;
+constexpr int kH = 64, kDH = 512, kTR = 32, kSlots = 5;
 constexpr int kRPL = kTR / 32;                        // tile rows per producer lane
 constexpr int kSoftWarps = 4, kMmaWarp = 4, kProdWarp0 = 5, kProdWarps = 4;
 constexpr int kPvWarp = kProdWarp0 + kProdWarps;
@@ -36,7 +36,11 @@ constexpr int kEpiWarp0 = kPvWarp + 1, kEpiWarps = 4;
 constexpr int kProdThreads = 32 * kProdWarps;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kBarSoft = 1, kBarProd = 2;             // named barriers (0 = __syncthreads)
-constexpr uint32_t kQBytes = kH * kDH * 2;            // 64 KiB, K-major, 8 chunks of 64 dims
+// q: dims [0, kQT) are the A operand of the S products from TMEM (copied there through a
+// ring slot at the start of each item), dims [kQT, 512) from shared memory
+constexpr int kQT = 256;
+constexpr uint32_t kQChunk = kH * 128;                // one 64-dim chunk of q, 8 KiB
+constexpr uint32_t kQBytes = (kDH - kQT) / 64 * kQChunk;   // 32 KiB in shared memory
 constexpr uint32_t kSlotBytes = kTR * kDH * 2;        // 32 KiB per staged tile
 constexpr uint32_t kPBytes = kH * 128;                // P^T: 64 heads x 64 rows bf16
 constexpr int kPBufs = 3;                              // P tiles in flight (softmax ahead of PV)
@@ -44,18 +48,23 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kQBytes;
 constexpr uint32_t kOffP = kOffKV + kSlots * kSlotBytes;
 constexpr uint32_t kOffBar = kOffP + kPBufs * kPBytes;
-// barriers: full[4] empty[4] s_full[2] s_free[2] p_full[3] p_free[3]; per item: q_full,
-// q_free (the item's S products are done), o_full (its PV products are done), o_free (the
-// epilogue has read O^T), stat (the softmax wrote the item's per-head statistics); drain
-constexpr int kBarFull = 0, kBarEmpty = 4, kBarSFull = 8, kBarSFree = 10, kBarPFull = 12,
-              kBarPFree = kBarPFull + kPBufs, kBarQ = kBarPFree + kPBufs, kBarQFree = kBarQ + 1,
+// barriers: full[5] empty[5] s_full[2] s_free[2] p_full[3] p_free[3]; per item: q_full
+// (q's shared-memory dims landed), q_tmem (its TMEM dims written), q_free (the item's S
+// products are done), o_full (its PV products are done), o_free (the epilogue has read
+// O^T), stat (the softmax wrote the item's per-head statistics); drain
+constexpr int kBarFull = 0, kBarEmpty = kSlots, kBarSFull = 2 * kSlots, kBarSFree = kBarSFull + 2,
+              kBarPFull = kBarSFree + 2, kBarPFree = kBarPFull + kPBufs, kBarQ = kBarPFree + kPBufs,
+              kBarQT = kBarQ + 1, kBarQFree = kBarQT + 1,
               kBarOFull = kBarQFree + 1, kBarOFree = kBarOFull + 1, kBarStat = kBarOFree + 1,
               kBarDrain = kBarStat + 1, kNumBars = kBarDrain + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffIds = kOffMisc + 1536;          // an item's slice of I (<= kMaxTopk)
 constexpr uint32_t kSmemBytes = kOffIds + kMaxTopk * 4 + 1024;  // + 1 KiB alignment slack
-constexpr uint32_t kTmemCols = 512;                   // S: cols [0,128), O^T: [128, 384)
-constexpr uint32_t kColO = 128;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+constexpr uint32_t kTmemCols = 512;                   // S: [0, 64), O^T: [64, 320), q: [320, 448)
+constexpr uint32_t kColO = 64;
+constexpr uint32_t kColQ = 320;
+static_assert(kColO + 256 <= kColQ && kColQ + kQT / 2 <= kTmemCols, "TMEM columns");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;
 
@@ -166,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 b == kBarStat)
                 cnt = kSoftWarps * 32;
             if (b == kBarQ) cnt = kProdThreads;
+            if (b == kBarQT) cnt = kSoftWarps * 32;
             if (b == kBarOFree) cnt = kEpiWarps * 32;
             if (b == kBarDrain) cnt = 2;                  // one commit from each issuing warp
             mbar_init(&bars[b], cnt);
@@ -214,14 +224,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 const int64_t kk = kk0 + pt + kProdThreads * m;
                 pre[m] = (Irow && kk < kk1) ? Irow[kk] : -1;
             }
-            // q of this item, once the previous item's S products are done with the last one
+            const __nv_bfloat16 *qrow = reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)x.row * kH * kDH;
+            {
+                // q dims [0, kQT) into the next ring slot (its Full barrier, like a tile's);
+                // the softmax warps move them into TMEM and free the slot
+                const int s = g % kSlots;
+                const bool w = g < (uint32_t)kSlots || wait_bar(&bars[kBarEmpty + s], ((g / kSlots) - 1) & 1, abort);
+                if (!group_all(kBarProd, kProdThreads, w)) { fail(); break; }
+                const uint32_t slot = sbase + kOffKV + s * kSlotBytes;
+                const int qu = pt & 31;                         // 16-byte unit of dims [0, kQT)
+                for (int h = pt >> 5; h < kH; h += kProdThreads / 32)
+                    cp_async16(slot + (qu >> 3) * kQChunk + sw128_offset(h, (qu & 7) * 8), qrow + h * kDH + qu * 8);
+                cp_async_arrive(&bars[kBarFull + s]);
+                if (pt == 0) mbar_arrive(&bars[kBarFull + s]);
+                ++g;
+            }
+            // q dims [kQT, 512), once the previous item's S products are done with them
             const bool wq = n < 1 || wait_bar(&bars[kBarQFree], (n - 1) & 1, abort);
             if (!group_all(kBarProd, kProdThreads, wq)) { fail(); break; }
-            const uint32_t qb = sbase + kOffQ;
-            const __nv_bfloat16 *qrow = reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)x.row * kH * kDH;
-            for (int h = pr0; h < kH; h += kRowStep)
-                cp_async16(qb + (pu >> 3) * (kH * 128) + sw128_offset(h, (pu & 7) * 8), qrow + h * kDH + pu * 8);
-            cp_async_arrive(&bars[kBarQ]);
+            {
+                const uint32_t qb = sbase + kOffQ;
+                const int qu = pt & 31;                         // unit of dims [kQT, 512)
+                for (int h = pt >> 5; h < kH; h += kProdThreads / 32)
+                    cp_async16(qb + (qu >> 3) * kQChunk + sw128_offset(h, (qu & 7) * 8),
+                               qrow + h * kDH + kQT + qu * 8);
+                cp_async_arrive(&bars[kBarQ]);
+            }
             // gathers tile i of the item into slot g % kSlots, once that slot is free
             auto issue_tile = [&](int i) -> bool {
                 const int s = g % kSlots;
@@ -311,18 +339,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
         const uint32_t id_s = idesc_bf16_f32(64, kTR, 0, 0);   // N = kTR rows
         const uint32_t id_o = idesc_bf16_f32(128, 64, 1, 0);
         const uint64_t qd = smem_desc_sw128(sbase + kOffQ, 16, 1024);
-        uint32_t g = 0;                                   // list tiles (all items)
+        uint32_t g = 0;                                   // ring entries (q slots and list tiles)
+        uint32_t gt = 0;                                  // list tiles (all items)
         int n = 0;
         for (int id = blockIdx.x; id < items && ok; id += gridDim.x, ++n) {
             const Item x = item_of(p, id);
+            ++g;                                          // the ring entry that carried q
             if (warp == kMmaWarp) {
                 // S = Q . K^T of every tile of the item, then release q to the producers
-                if (!wait_bar_warp(&bars[kBarQ], n & 1, abort)) { fail(); break; }
+                if (!wait_bar_warp(&bars[kBarQ], n & 1, abort) || !wait_bar_warp(&bars[kBarQT], n & 1, abort)) {
+                    fail();
+                    break;
+                }
                 fence_after_sync();
-                for (int i = 0; i < x.T; ++i, ++g) {
-                    const int s = g % kSlots, sb = g & 1;
+                for (int i = 0; i < x.T; ++i, ++g, ++gt) {
+                    const int s = g % kSlots, sb = gt & 1;
                     if (!wait_bar_warp(&bars[kBarFull + s], (g / kSlots) & 1, abort) ||
-                        (g >= 2 && !wait_bar_warp(&bars[kBarSFree + sb], ((g >> 1) - 1) & 1, abort))) {
+                        (gt >= 2 && !wait_bar_warp(&bars[kBarSFree + sb], ((gt >> 1) - 1) & 1, abort))) {
                         fail();
                         break;
                     }
@@ -330,10 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                     const uint64_t bd = smem_desc_sw128(sbase + kOffKV + s * kSlotBytes, 16, 1024);
                     const uint32_t d = tmem + sb * kTR;
 #pragma unroll
-                    for (int ks = 0; ks < kDH / 16; ++ks) {
+                    for (int ks = 0; ks < kQT / 16; ++ks) {        // q dims from TMEM
                         const uint32_t ko = (ks >> 2), kb = (ks & 3) * 32;
-                        mma_bf16_warp(d, desc_add(qd, ko * (kH * 128) + kb), desc_add(bd, ko * (kTR * 128) + kb),
-                                      id_s, ks > 0);
+                        mma_bf16_tmem_a_warp(d, tmem + kColQ + ks * 8, desc_add(bd, ko * (kTR * 128) + kb), id_s,
+                                             ks > 0);
+                    }
+#pragma unroll
+                    for (int ks = kQT / 16; ks < kDH / 16; ++ks) { // q dims from shared memory
+                        const uint32_t ko = (ks >> 2), kb = (ks & 3) * 32;
+                        mma_bf16_warp(d, desc_add(qd, (ko - kQT / 64) * kQChunk + kb),
+                                      desc_add(bd, ko * (kTR * 128) + kb), id_s, 1u);
                     }
                     mma_commit_warp(&bars[kBarSFull + sb]);
                 }
@@ -344,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 // epilogue has read it, and is handed to the epilogue after the last tile
                 if (n >= 1 && !wait_bar_warp(&bars[kBarOFree], (n - 1) & 1, abort)) { fail(); break; }
                 fence_after_sync();
-                for (int i = 0; i < x.T; ++i, ++g) {
-                    const int s = g % kSlots, pb = g % kPBufs;
-                    if (!wait_bar_warp(&bars[kBarPFull + pb], (g / kPBufs) & 1, abort)) { fail(); break; }
+                for (int i = 0; i < x.T; ++i, ++g, ++gt) {
+                    const int s = g % kSlots, pb = gt % kPBufs;
+                    if (!wait_bar_warp(&bars[kBarPFull + pb], (gt / kPBufs) & 1, abort)) { fail(); break; }
                     fence_after_sync();
                     const uint64_t ad = smem_desc_sw128(sbase + kOffKV + s * kSlotBytes, kTR * 128, 1024);
                     const uint64_t bd = smem_desc_sw128(sbase + kOffP + pb * kPBytes, 16, 1024);
@@ -390,15 +429,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             return true;
         };
         constexpr int kHR = kTR / 2;                    // rows per lane
-        uint32_t g = 0;                                 // list tiles (all items)
+        uint32_t g = 0;                                 // ring entries (q slots and list tiles)
+        uint32_t gt = 0;                                // list tiles (all items)
         int n = 0;
         for (int id = blockIdx.x; id < items; id += gridDim.x, ++n) {
             const Item x = item_of(p, id);
             float m2 = -INFINITY, l = 0.f;
-            for (int i = 0; i < x.T; ++i, ++g) {
-                const int s = g % kSlots, sb = g & 1;
+            {
+                // q dims [0, kQT) of this item, from the ring slot the producers filled, into
+                // TMEM (the previous item's S products, whose scores this warp has read, no
+                // longer need the old ones); lane l < 16 of warp w holds head 16 w + l, as the
+                // M = 64 A operand wants; then the slot is free again
+                const int s = g % kSlots;
+                const bool wq = wait_bar(&bars[kBarFull + s], (g / kSlots) & 1, abort);
+                if (!group_all(kBarSoft, kSoftWarps * 32, wq)) { fail(); break; }
+                const uint8_t *qs = smem + kOffKV + s * kSlotBytes;
+                const int hq = warp * 16 + (lane & 15);
+#pragma unroll 2
+                for (int c0 = 0; c0 < kQT / 2; c0 += 16) {   // 16 columns = 32 dims = 4 units
+                    float v[16];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
+                        if (lane < 16) {
+                            const int qu = c0 / 4 + u;            // dims 8 qu .. + 7
+                            w4 = *reinterpret_cast<const uint4 *>(qs + (qu >> 3) * kQChunk +
+                                                                  sw128_offset(hq, (qu & 7) * 8));
+                        }
+                        v[4 * u] = __uint_as_float(w4.x);
+                        v[4 * u + 1] = __uint_as_float(w4.y);
+                        v[4 * u + 2] = __uint_as_float(w4.z);
+                        v[4 * u + 3] = __uint_as_float(w4.w);
+                    }
+                    tmem_st16(tmem + ((uint32_t)(32 * warp) << 16) + kColQ + c0, v);
+                }
+                tmem_st_wait();
+                fence_before_sync();
+                mbar_arrive(&bars[kBarQT]);
+                named_or_soft(0u);                          // every lane has read the slot
+                if (tid == 0) mbar_arrive(&bars[kBarEmpty + s]);
+                ++g;
+            }
+            for (int i = 0; i < x.T; ++i, ++g, ++gt) {
+                const int s = g % kSlots, sb = gt & 1;
                 const bool w = wait_bar(&bars[kBarFull + s], (g / kSlots) & 1, abort) &&
-                               wait_bar(&bars[kBarSFull + sb], (g >> 1) & 1, abort);
+                               wait_bar(&bars[kBarSFull + sb], (gt >> 1) & 1, abort);
                 if (!group_all(kBarSoft, kSoftWarps * 32, w)) { fail(); break; }
                 fence_after_sync();
                 const uint32_t mask = (uint32_t)(misc->mask[s] >> (kHR * half));
@@ -443,12 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
 #pragma unroll
                     for (int r = 0; r < wd; ++r) pr[r] += pr[r + wd];
                 const float sum = pr[0] + __shfl_xor_sync(0xffffffffu, pr[0], 16);
-                // P buffer g % kPBufs is free once PV(g - kPBufs) has completed
-                const bool wp = g < (uint32_t)kPBufs || wait_pfree(g % kPBufs, g / kPBufs - 1);
+                // P buffer gt % kPBufs is free once PV(gt - kPBufs) has completed
+                const bool wp = gt < (uint32_t)kPBufs || wait_pfree(gt % kPBufs, gt / kPBufs - 1);
                 if (!group_all(kBarSoft, kSoftWarps * 32, wp)) { fail(); break; }
                 l = l * alpha + sum;
                 {
-                    uint8_t *pbuf = smem + kOffP + (g % kPBufs) * kPBytes;
+                    uint8_t *pbuf = smem + kOffP + (gt % kPBufs) * kPBytes;
 #pragma unroll
                     for (int u = 0; u < kHR / 8; ++u)
                         *reinterpret_cast<uint4 *>(pbuf + sw128_offset(h, (half * (kHR / 8) + u) * 8)) =
@@ -458,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                     // rescale O^T columns of the heads whose reference max moved up, once the
                     // previous tile's PV product (this item's) has landed
                     if (lead) misc->alpha[h] = alpha;
-                    const bool wr = i < 1 || wait_pfree((g - 1) % kPBufs, (g - 1) / kPBufs);
+                    const bool wr = i < 1 || wait_pfree((gt - 1) % kPBufs, (gt - 1) / kPBufs);
                     if (!group_all(kBarSoft, kSoftWarps * 32, wr)) { fail(); break; }
                     fence_after_sync();
 #pragma unroll 1
@@ -477,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 }
                 fence_async_smem();
                 fence_before_sync();
-                mbar_arrive(&bars[kBarPFull + (g % kPBufs)]);
+                mbar_arrive(&bars[kBarPFull + (gt % kPBufs)]);
             }
             if (!ok) break;
             // the item's per-head statistics, for the epilogue warps: written once the epilogue

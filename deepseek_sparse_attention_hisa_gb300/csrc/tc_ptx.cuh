@@ -109,6 +109,19 @@ __device__ __forceinline__ void mma_bf16_warp(uint32_t d_tmem, uint64_t a_desc, 
         :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// The same with A read from TMEM (a_tmem: its first column). An M = 64 A operand holds
+// row r in lane 32 (r / 16) + r % 16, two bf16 per 32-bit column (the even element in the
+// low half); a K step of 16 spans 8 columns.
+__device__ __forceinline__ void mma_bf16_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                     uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // Warp-wide: one elected lane arranges an arrival (once) on mbar for when all MMAs this
 // thread issued before have completed.
 __device__ __forceinline__ void mma_commit_warp(uint64_t *mbar) {
