@@ -117,7 +117,6 @@ __global__ void __launch_bounds__(NT) k_select_chunks(SelectParams p) {
 template <int NT>
 __global__ void __launch_bounds__(NT) k_select_merge(SelectParams p, int cap) {
     __shared__ SelectShared<NT> sh;
-    __shared__ int s_m;
     extern __shared__ __align__(16) float s_sc[];
     int32_t *s_id = reinterpret_cast<int32_t *>(s_sc + cap);
     const int row = blockIdx.x, tid = threadIdx.x;
