@@ -12,21 +12,23 @@
 //   warp 0      MMA issue (one elected lane) and TMEM owner
 //   warp 1      fine: TMA producer of the kept blocks' bf16 key tiles (a three-slot
 //               ring); coarse: TMA of the f32 block means, [128 rows x 32 dims] boxes
-//               into four raw slots
+//               into seven raw slots
 //   warps 2-5   epilogue: TMEM -> relu, head weights, head sum -> scores in shared memory
-//   warps 6-9   builders: per-query checks, kept blocks, head weights, q planes (fine:
-//               two q buffers, so the next query's are written while this one streams);
+//   warps 6-9   builders: per-query checks, kept blocks, head weights, q planes (two
+//               q buffers, so the next query's are written while this one streams);
 //               coarse, appending: the means of the newly completed blocks
 //   warps 10-13 select: block top-k over the finished query's scores (named barrier 1)
-//   warps 14-21 coarse: converters, f32 block means -> three bf16 planes
+//   warps 14-21 coarse: converters, f32 block means -> three bf16 planes in TMEM, where
+//               they are the MMA's A operand (an eight-box ring)
 //
-// A tile is 128 scored rows, D[128 rows x 64 * planes] = rows . q^T (M = 128, K = 128) in
-// one of two TMEM accumulators. Scoring is f32 on the page; f32 operands are split
+// A tile is 128 scored rows, D = rows . q^T (M = 128, K = 128) in one of two TMEM
+// accumulators (fine: [128 x 64 * q planes], coarse: [128 x 64]). Scoring is f32 on the page; f32 operands are split
 // exactly into bf16 planes x = x1 + x2 + x3 (q: each plane the bf16 rounding of the
 // remainder; block means: the remainder truncated to its top 8 significant bits, which is
 // cheaper to form), so every bf16 product is exact in the f32 accumulator. The q planes
 // are stacked along N. bf16 keys take one MMA per K step over all q planes. f32 block
-// means take six of the nine plane products (x1 y1, x1 y2, x1 y3, x2 y1, x2 y2, x3 y1):
+// means take six of the nine plane products (x1 y1, x1 y2, x1 y3, x2 y1, x2 y2, x3 y1), one
+// N = 64 MMA each, all accumulated into the same [128 x 64] accumulator:
 // with |x2| < 2^-7 |x|, |x3| < 2^-14 |x|, |y2| <= 2^-8 |y| and |y3| <= 2^-16 |y|, the three
 // left out (x2 y3, x3 y2, x3 y3) add up to less than 2^-21 of |x y|.
 // Every wait is bounded; a timeout raises HISA_DEV_TIMEOUT, and the CTA drains and exits.
@@ -50,26 +52,29 @@ constexpr int pipe_threads() { return MODE == kCoarse ? (kWarpCvt + kCvtWarps) *
 // ---- shared memory (offsets from the 1024-aligned base) ----
 constexpr uint32_t kQPlane = kH * kD * 2;                 // [64 heads x 128 dims] bf16, 16 KiB
 constexpr uint32_t kOffQ = 0;                             // up to 3 planes, stacked along N
-// fine: two q buffers, so the next query's planes are written while this one streams;
-// coarse keeps one (its shared memory holds the raw and converted means instead)
+// two q buffers, so that the next query's planes are written while this one streams
 template <int MODE>
-constexpr int q_bufs() { return MODE == kFine ? 2 : 1; }
+constexpr int q_bufs() { return 2; }
 template <int MODE>
 constexpr uint32_t off_reg() { return q_bufs<MODE>() * 3 * kQPlane; }   // streaming region
 constexpr int kFineSlots = 3;
 constexpr uint32_t kTileBytes = kM * kD * 2;              // fine: one [128 x 128] bf16 key tile
 constexpr uint32_t kRawBytes = kM * 32 * 4;               // coarse: f32 means, 128 rows x 32 dims
-constexpr uint32_t kHalfPlane = kM * 128;                 // [128 rows x 64 dims] bf16, 16 KiB
-constexpr uint32_t kPlaneSet = 3 * kHalfPlane;            // its three planes
-constexpr int kRawSlots = 4;                              // coarse raw boxes in flight
-constexpr int kPlaneSets = 2;                             // coarse converted units
-// coarse: kRawSlots raw f32 units, then kPlaneSets plane sets; fine: the key tile ring
+constexpr int kRawSlots = 7;                              // coarse raw boxes in flight
+// coarse TMEM: two [128 x 64] f32 accumulators in columns 0-127, then kASlots converted
+// boxes, each three bf16 planes of 16 columns (the MMA's A operand, lane = tile row)
+constexpr int kASlots = 8;
+constexpr uint32_t kAColBase = 128, kABoxCols = 48;
+static_assert(kAColBase + kASlots * kABoxCols <= 512, "coarse TMEM");
+// coarse: kRawSlots raw f32 boxes; fine: the key tile ring
 template <int MODE>
 constexpr uint32_t region_bytes() {
-    return MODE == kCoarse ? kRawSlots * kRawBytes + kPlaneSets * kPlaneSet : kFineSlots * kTileBytes;
+    return MODE == kCoarse ? kRawSlots * kRawBytes : kFineSlots * kTileBytes;
 }
-constexpr uint32_t kOffReg = 3 * kQPlane;                 // coarse streaming region
-constexpr uint32_t kOffPlanes = kOffReg + kRawSlots * kRawBytes;
+// TMEM columns between the two accumulators
+template <int MODE>
+constexpr uint32_t acc_stride() { return MODE == kCoarse ? 64 : 256; }
+constexpr uint32_t kOffReg = 2 * 3 * kQPlane;             // coarse streaming region
 static_assert(off_reg<kCoarse>() == kOffReg, "coarse layout");
 
 struct QMeta {            // one query row, double-buffered
@@ -87,8 +92,8 @@ struct QMeta {            // one query row, double-buffered
 // barriers
 constexpr int kBarMetaFull = 0, kBarSlotFree = 2, kBarQFull = 4, kBarQEmpty = 6,
               kBarAccFull = 8, kBarAccEmpty = 10, kBarScFull = 12, kBarDrain = 14,
-              kBarFull = 15,                // fine: kFineSlots; coarse: 2 plane sets, 4 raw slots
-              kBarEmpty = kBarFull + 6, kBarMeansReady = kBarEmpty + 6,
+              kBarFull = 15,                // fine: kFineSlots; coarse: kASlots TMEM boxes, then kRawSlots raw
+              kBarEmpty = kBarFull + kASlots + kRawSlots, kBarMeansReady = kBarEmpty + kASlots + kRawSlots,
               kNumBars = kBarMeansReady + 2;
 
 template <int MODE>
@@ -217,9 +222,11 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             if (b == kBarQFull || b == kBarQFull + 1 || b == kBarAccEmpty || b == kBarAccEmpty + 1 || b == kBarScFull ||
                 b == kBarScFull + 1 || b == kBarMeansReady || b == kBarMeansReady + 1)
                 cnt = kGroup;
-            // coarse: Full / Empty + 0, 1 guard the plane sets, + 2 .. 5 the raw slots
-            if (MODE == kCoarse && (b == kBarFull || b == kBarFull + 1)) cnt = kCvtThreads;
-            if (MODE == kCoarse && b >= kBarEmpty + 2 && b < kBarEmpty + 2 + kRawSlots) cnt = kCvtThreads;
+            // coarse: Full / Empty + 0 .. kASlots - 1 guard the TMEM boxes, the next kRawSlots
+            // the raw slots
+            if (MODE == kCoarse && b >= kBarFull && b < kBarFull + kASlots) cnt = kCvtThreads;
+            if (MODE == kCoarse && b >= kBarEmpty + kASlots && b < kBarEmpty + kASlots + kRawSlots)
+                cnt = kCvtThreads;
             mbar_init(&bars[b], cnt);
         }
         mbar_fence_init();
@@ -449,9 +456,9 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     } else if (MODE == kCoarse && warp == kWarpTma) {
         // ---------------- coarse loader: block means by TMA ----------------
         // Box v = one K quarter (32 dims) of one 128-row tile, a 128B-swizzled [128 rows x 32
-        // dims] f32 box into raw slot v % kRawSlots; small slots keep more bytes in flight
-        // beside the one being converted. Rows past the allocation read as 0; rows past the
-        // query's blocks are other data and never scored.
+        // dims] f32 box into raw slot v % kRawSlots; many small slots keep the bytes in flight
+        // that the latency under load asks for. Rows past the allocation read as 0; rows past
+        // the query's blocks are other data and never scored.
         if (lane == 0) {
             uint32_t u = 0;                                    // boxes issued
             for (int i = 0; i < nql && ok; ++i) {
@@ -468,28 +475,27 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                     }
                     for (int h = 0; h < 4; ++h, ++u) {
                         const uint32_t slot = u % kRawSlots, use = u / kRawSlots;
-                        if (use >= 1 && !wait_bar(&bars[kBarEmpty + 2 + slot], (use - 1) & 1, abort)) {
+                        if (use >= 1 && !wait_bar(&bars[kBarEmpty + kASlots + slot], (use - 1) & 1, abort)) {
                             fail();
                             break;
                         }
-                        mbar_arrive_expect_tx(&bars[kBarFull + 2 + slot], kRawBytes);
+                        mbar_arrive_expect_tx(&bars[kBarFull + kASlots + slot], kRawBytes);
                         const int32_t y = (int32_t)(M.base + (int64_t)t * kM);
                         tma_load_2d(sbase + kOffReg + slot * kRawBytes, &P.means_map, h * 32, y,
-                                    &bars[kBarFull + 2 + slot]);
+                                    &bars[kBarFull + kASlots + slot]);
                     }
                 }
             }
             if (!ok)   // let the copies in flight land before the CTA can exit
                 for (uint32_t v = u > kRawSlots ? u - kRawSlots : 0; v < u; ++v)
-                    mbar_wait(&bars[kBarFull + 2 + v % kRawSlots], (v / kRawSlots) & 1, 1u << 20);
+                    mbar_wait(&bars[kBarFull + kASlots + v % kRawSlots], (v / kRawSlots) & 1, 1u << 20);
         }
     } else if (warp == kWarpMma) {
         // ---------------- MMA issue (warp-uniform loop, one elected lane issues) ----------
         const uint32_t id_all = idesc_bf16_f32(kM, 64 * NQ, 0, 0);
-        const uint32_t id_two = idesc_bf16_f32(kM, 64 * (NQ > 1 ? NQ - 1 : 1), 0, 0);
         const uint32_t id_one = idesc_bf16_f32(kM, 64, 0, 0);
 
-        uint32_t g = 0, gs = 0, u = 0;                       // tiles, fine slots, coarse halves
+        uint32_t g = 0, gs = 0, u = 0;                       // tiles, fine slots, coarse boxes
         for (int i = 0; i < nql && ok; ++i) {
             const int qb = i & 1;
             if (!wait_bar_warp(&bars[kBarMetaFull + qb], (i >> 1) & 1, abort) ||
@@ -508,7 +514,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                     break;
                 }
                 fence_after_sync();
-                const uint32_t d = tmem + ab * 256;
+                const uint32_t d = tmem + ab * acc_stride<MODE>();
                 if (MODE == kFine) {
                     const uint32_t s = gs % kFineSlots;
                     if (!wait_bar_warp(&bars[kBarFull + s], (gs / kFineSlots) & 1, abort)) {
@@ -527,21 +533,24 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                     ++gs;
                 } else {
                     bool good = true;
-                    for (int h = 0; h < 2; ++h, ++u) {
-                        const uint32_t pb = u & 1;               // plane set of unit u
-                        if (!wait_bar_warp(&bars[kBarFull + pb], (u >> 1) & 1, abort)) { good = false; break; }
+                    for (int h = 0; h < 4; ++h, ++u) {           // the tile's four boxes
+                        const uint32_t as = u % kASlots;
+                        if (!wait_bar_warp(&bars[kBarFull + as], (u / kASlots) & 1, abort)) { good = false; break; }
                         fence_after_sync();
-                        const uint64_t pd = smem_desc_sw128(sbase + kOffPlanes + pb * kPlaneSet, 16, 1024);
+                        const uint32_t a0 = tmem + kAColBase + as * kABoxCols;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t kb = kk * 32;
-                            const uint64_t bq = desc_add(qd, h * (NQ * kH * 128) + kb);
-                            // rows plane ra against q planes 0 .. NQ-1-ra (all of them for bf16 q)
-                            mma_bf16_warp(d, desc_add(pd, kb), bq, id_all, (h | kk) ? 1u : 0u);
-                            mma_bf16_warp(d, desc_add(pd, kHalfPlane + kb), bq, id_two, 1u);
-                            mma_bf16_warp(d, desc_add(pd, 2 * kHalfPlane + kb), bq, id_one, 1u);
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint32_t dim = h * 32 + kk * 16;
+                            const uint64_t bq = desc_add(qd, (dim >> 6) * (NQ * kH * 128) + (dim & 63) * 2);
+                            // rows plane ra against q plane qa, for ra + qa <= 2
+#pragma unroll
+                            for (int ra = 0; ra < 3; ++ra)
+#pragma unroll
+                                for (int qa = 0; qa < NQ && ra + qa <= 2; ++qa)
+                                    mma_bf16_tmem_a_warp(d, a0 + ra * 16 + kk * 8, desc_add(bq, qa * (kH * 128)),
+                                                         id_one, (h | kk | ra | qa) ? 1u : 0u);
                         }
-                        mma_commit_warp(&bars[kBarEmpty + pb]);
+                        mma_commit_warp(&bars[kBarEmpty + as]);
                     }
                     if (!good) { fail(); break; }
                 }
@@ -572,19 +581,20 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 const uint32_t ab = g & 1;
                 if (!wait_bar(&bars[kBarAccFull + ab], (g >> 1) & 1, abort)) { fail(); break; }
                 fence_after_sync();
-                const uint32_t ta = tmem + ab * 256 + ((uint32_t)(quad * 32) << 16);
+                const uint32_t ta = tmem + ab * acc_stride<MODE>() + ((uint32_t)(quad * 32) << 16);
+                constexpr int NS = MODE == kCoarse ? 1 : NQ;   // column groups to sum
                 float acc = 0.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {               // 16 heads at a time
-                    float v[NQ][16];
+                    float v[NS][16];
 #pragma unroll
-                    for (int qa = 0; qa < NQ; ++qa) tmem_ld16(ta + qa * 64 + c * 16, v[qa]);
+                    for (int qa = 0; qa < NS; ++qa) tmem_ld16(ta + qa * 64 + c * 16, v[qa]);
                     tmem_ld_wait();
 #pragma unroll
                     for (int h = 0; h < 16; ++h) {
                         float dot = v[0][h];
 #pragma unroll
-                        for (int qa = 1; qa < NQ; ++qa) dot += v[qa][h];
+                        for (int qa = 1; qa < NS; ++qa) dot += v[qa][h];
                         acc = fmaf(M.w[c * 16 + h], fmaxf(dot, 0.f), acc);
                     }
                 }
@@ -634,12 +644,15 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
         }
     }
     else if (MODE == kCoarse && warp >= kWarpCvt && warp < kWarpCvt + kCvtWarps) {
-        // ---------------- converters: f32 means -> three bf16 planes ----------------------
-        // Box v (32 dims of a tile) fills columns 32 (v % 2) .. + 31 of plane set (v / 2) % 2;
-        // thread ct converts the 16-byte pieces c = m * kCvtThreads + ct (m < 4): row c / 8,
-        // dims 4 (c % 8) .. + 3; a warp reads four whole swizzled rows (no bank conflict).
-        constexpr int kChunks = kM * 8 / kCvtThreads;           // 4
-        const int ct = tid - kWarpCvt * 32;
+        // ---------------- converters: f32 means -> three bf16 planes in TMEM ---------------
+        // Box v (32 dims of a tile, raw slot v % kRawSlots) becomes TMEM box v % kASlots:
+        // plane k in columns 16 k .. + 15, dims 2 c and 2 c + 1 in column c. TMEM lane = tile
+        // row, so warp w converts rows 32 (w % 4) .. + 31 (its lane quadrant), dims 16 hf .. + 15,
+        // hf = which of the quadrant's two converter warps it is. Each lane reads four 16-byte
+        // pieces of its own swizzled row; eight consecutive rows cover all banks.
+        const int quad = warp & 3, hf = (warp - kWarpCvt) >> 2;
+        const int r = quad * 32 + lane;
+        const uint32_t tlane = tmem + ((uint32_t)(quad * 32) << 16) + kAColBase + (uint32_t)hf * 8;
         uint32_t v = 0;                                        // boxes converted
         for (int i = 0; i < nql && ok; ++i) {
             const int qb = i & 1;
@@ -647,22 +660,24 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             const QMeta &M = meta[qb];
             const int nbox = M.state ? 0 : 4 * M.T;
             for (int e = 0; e < nbox; ++e, ++v) {
-                const uint32_t slot = v % kRawSlots, hv = v >> 1, pb = hv & 1, col = (v & 1) * 32;
-                if (!wait_bar(&bars[kBarFull + 2 + slot], (v / kRawSlots) & 1, abort) ||
-                    ((v & 1) == 0 && hv >= 2 && !wait_bar(&bars[kBarEmpty + pb], ((hv >> 1) - 1) & 1, abort))) {
+                const uint32_t slot = v % kRawSlots, as = v % kASlots;
+                if (!wait_bar(&bars[kBarFull + kASlots + slot], (v / kRawSlots) & 1, abort) ||
+                    (v >= kASlots && !wait_bar(&bars[kBarEmpty + as], (v / kASlots - 1) & 1, abort))) {
                     fail();
                     break;
                 }
-                const uint8_t *rawb = smem + kOffReg + slot * kRawBytes;
-                uint8_t *planes = smem + kOffPlanes + pb * kPlaneSet;
+                const uint8_t *rowp = smem + kOffReg + slot * kRawBytes + r * 128;
+                float4 a[4];
 #pragma unroll
-                for (int m = 0; m < kChunks; ++m) {
-                    const int c = m * kCvtThreads + ct, r = c >> 3, pv = c & 7;
-                    const float4 a = *reinterpret_cast<const float4 *>(rawb + r * 128 + ((pv ^ (r & 7)) << 4));
-                    // exact split by truncation: hi = top 8 significant bits, then the same
-                    // of the (exact) remainder; the last remainder has at most 8 bits left
-                    uint32_t w[3][2];
-                    const float xs[4] = {a.x, a.y, a.z, a.w};
+                for (int ch = 0; ch < 4; ++ch)
+                    a[ch] = *reinterpret_cast<const float4 *>(rowp + (((4 * hf + ch) ^ (r & 7)) << 4));
+                mbar_arrive(&bars[kBarEmpty + kASlots + slot]);
+                // exact split by truncation: hi = top 8 significant bits, then the same of the
+                // (exact) remainder; the last remainder has at most 8 bits left
+                uint32_t pl[3][8];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const float xs[4] = {a[ch].x, a[ch].y, a[ch].z, a[ch].w};
                     uint32_t pk[3][4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -676,19 +691,16 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                     }
 #pragma unroll
                     for (int k = 0; k < 3; ++k) {
-                        w[k][0] = __byte_perm(pk[k][0], pk[k][1], 0x7632);   // {hi(e0), hi(e1)}
-                        w[k][1] = __byte_perm(pk[k][2], pk[k][3], 0x7632);
+                        pl[k][2 * ch] = __byte_perm(pk[k][0], pk[k][1], 0x7632);   // {hi(e0), hi(e1)}
+                        pl[k][2 * ch + 1] = __byte_perm(pk[k][2], pk[k][3], 0x7632);
                     }
-                    const uint32_t off = sw128_offset((uint32_t)r, col + (uint32_t)pv * 4);
+                }
+                fence_after_sync();                    // after the wait for the MMAs that read the box
 #pragma unroll
-                    for (int k = 0; k < 3; ++k)
-                        *reinterpret_cast<uint2 *>(planes + k * kHalfPlane + off) = make_uint2(w[k][0], w[k][1]);
-                }
-                mbar_arrive(&bars[kBarEmpty + 2 + slot]);
-                if (v & 1) {
-                    fence_async_smem();
-                    mbar_arrive(&bars[kBarFull + pb]);
-                }
+                for (int k = 0; k < 3; ++k) tmem_st8(tlane + as * kABoxCols + k * 16, pl[k]);
+                tmem_st_wait();
+                fence_before_sync();
+                mbar_arrive(&bars[kBarFull + as]);
             }
         }
     }

@@ -109,9 +109,9 @@ __device__ __forceinline__ void mma_bf16_warp(uint32_t d_tmem, uint64_t a_desc, 
         :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
-// The same with A read from TMEM (a_tmem: its first column). An M = 64 A operand holds
-// row r in lane 32 (r / 16) + r % 16, two bf16 per 32-bit column (the even element in the
-// low half); a K step of 16 spans 8 columns.
+// The same with A read from TMEM (a_tmem: its first column). Two bf16 per 32-bit column
+// (the even element in the low half); a K step of 16 spans 8 columns. An M = 128 A operand
+// holds row r in lane r, an M = 64 one row r in lane 32 (r / 16) + r % 16.
 __device__ __forceinline__ void mma_bf16_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                      uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -174,6 +174,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
            "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])),
            "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
            "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+// Warp-wide: store 8 consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+        :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
         : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() {
