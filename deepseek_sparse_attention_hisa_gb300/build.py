@@ -54,7 +54,7 @@ def _stamp() -> str:
 # includes. A profile's counters stay valid while these bytes (and the flags) are unchanged.
 KERNEL_SOURCES = {
     "k_attend_tc": ["k_attend_tc.cu", "hisa_internal.cuh", "tc_ptx.cuh"],
-    "k_score_pipe": ["k_score_pipe.cu", "select_core.cuh", "hisa_internal.cuh", "tc_ptx.cuh"],
+    "k_score_pipe": ["k_score_pipe.cu", "pipe_common.cuh", "select_core.cuh", "hisa_internal.cuh", "tc_ptx.cuh"],
     "k_score_gemm": ["k_score_gemm.cu", "hisa_internal.cuh", "tc_ptx.cuh"],
 }
 

@@ -32,17 +32,15 @@
 // with |x2| < 2^-7 |x|, |x3| < 2^-14 |x|, |y2| <= 2^-8 |y| and |y3| <= 2^-16 |y|, the three
 // left out (x2 y3, x3 y2, x3 y3) add up to less than 2^-21 of |x y|.
 // Every wait is bounded; a timeout raises HISA_DEV_TIMEOUT, and the CTA drains and exits.
-#include "select_core.cuh"
-#include "tc_ptx.cuh"
+#include "pipe_common.cuh"
 
 namespace hisa {
 namespace {
 
 using namespace tc;
+using namespace pipe;
 
-constexpr int kH = 64, kD = 128, kM = 128;
 constexpr int kWarpMma = 0, kWarpTma = 1, kWarpEpi = 2, kWarpBld = 6, kWarpSel = 10, kWarpCvt = 14;
-constexpr int kGroup = 128;                               // threads of each 4-warp role
 constexpr int kCvtWarps = 8, kCvtThreads = kCvtWarps * 32;  // coarse converters
 constexpr int kBarSel = 1, kBarBld = 2;                   // named barriers (0 = __syncthreads)
 
@@ -50,7 +48,6 @@ template <int MODE>
 constexpr int pipe_threads() { return MODE == kCoarse ? (kWarpCvt + kCvtWarps) * 32 : 14 * 32; }
 
 // ---- shared memory (offsets from the 1024-aligned base) ----
-constexpr uint32_t kQPlane = kH * kD * 2;                 // [64 heads x 128 dims] bf16, 16 KiB
 constexpr uint32_t kOffQ = 0;                             // up to 3 planes, stacked along N
 // two q buffers, so that the next query's planes are written while this one streams
 template <int MODE>
@@ -110,11 +107,6 @@ constexpr int kPipeMaxCoarse = 1024;
 constexpr int kPipeMaxFine = 48 * 64;
 static_assert(kPipeMaxFine <= kSmallMax && kPipeMaxCoarse <= kSmallMax, "select capacity");
 
-struct Misc {
-    uint32_t tmem;
-    int abort;
-};
-
 // 227 KiB of shared memory per CTA: the layout, two score rows at capacity and the static
 // select state (kept blocks and SelectShared of the whole CTA)
 template <int MODE>
@@ -125,67 +117,14 @@ constexpr bool fits() {
 }
 static_assert(fits<kCoarse>() && fits<kFine>(), "shared memory");
 
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    return mbar_wait_abortable(bar, parity, abort);
-}
-
-__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort));
-}
-
-__device__ __forceinline__ void named_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Exact three-way split of 8 f32 values into bf16 planes, packed as 3 x uint4.
-__device__ __forceinline__ void split3(const float (&x)[8], uint4 (&pl)[3]) {
-    uint32_t w[3][4];
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-        float r0 = x[e], r1 = x[e + 1];
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-            const __nv_bfloat162 b = __floats2bfloat162_rn(r0, r1);
-            w[k][e / 2] = *reinterpret_cast<const uint32_t *>(&b);
-            if (k < 2) {
-                const float2 f = __bfloat1622float2(b);
-                r0 -= f.x;
-                r1 -= f.y;
-            }
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < 3; ++k) pl[k] = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
-}
-
-// Byte offset of 16-byte unit u (dims 8u..8u+7) of head h of q plane `plane` when nq
-// planes are stacked along N: per 64-dim chunk, plane 0's 64 heads, then plane 1's, ...
-__device__ __forceinline__ uint32_t q_off(uint32_t plane, uint32_t h, uint32_t u, uint32_t nq) {
-    return (u >> 3) * (nq * kH * 128u) + plane * (kH * 128u) + sw128_offset(h, (u & 7u) * 8u);
-}
-
 }  // namespace
 }  // namespace hisa
 
 namespace hisa {
 namespace {
 
-// True on every participating thread iff v is true on all of them (named barrier id).
-__device__ __forceinline__ bool group_all(int id, int n, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(n)
-        : "memory");
-    return r != 0u;
-}
-
-// Registers: 14 or 18 warps spread over the SM's four 16K-register sub-partitions,
-// so at most 128 (fine) or 96 (coarse) registers per thread.
+// Registers: 14 (fine) or 22 (coarse) warps spread over the SM's four 16K-register
+// sub-partitions, so at most 128 or 88 registers per thread.
 template <int MODE, bool QBF16>
 __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     k_score_pipe(const __grid_constant__ ScoreTcParams P) {
@@ -250,7 +189,6 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     if (warp >= kWarpBld && warp < kWarpBld + 4) {
         // ---------------- builders: checks, kept blocks, weights, q planes ----------------
         const int bt = tid - kWarpBld * 32;
-        constexpr int kQU = kH * 16 / kGroup;                 // 16-byte q units per thread
         for (int i = 0; i < nql; ++i) {
             const int qb = i & 1;
             const int row = (int)blockIdx.x + i * (int)gridDim.x;
@@ -258,27 +196,8 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             // this row's q, weights and kept blocks first: the loads overlap the waits. With
             // 22 warps (coarse, f32 q) only half of q is held in registers; the other half is
             // prefetched into L2 and read once the previous query's planes are free.
-            constexpr bool kHalves = MODE == kCoarse && !QBF16;
-            constexpr int kQHeld = kHalves ? kQU / 2 : kQU;
-            float4 qf[QBF16 ? 1 : 2 * kQHeld];
-            uint4 qh[QBF16 ? kQU : 1];
-            const float4 *q4 = reinterpret_cast<const float4 *>(
-                reinterpret_cast<const float *>(p.q) + (int64_t)row * kH * kD);
-            if (QBF16) {
-                const uint4 *q16 = reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)row * kH * kD);
-#pragma unroll
-                for (int m = 0; m < kQU; ++m) qh[m] = __ldg(q16 + bt + m * kGroup);
-            } else {
-#pragma unroll
-                for (int m = 0; m < kQHeld; ++m) {
-                    qf[2 * m] = __ldg(q4 + 2 * (bt + m * kGroup));
-                    qf[2 * m + 1] = __ldg(q4 + 2 * (bt + m * kGroup) + 1);
-                }
-#pragma unroll
-                for (int m = kQHeld; m < kQU; ++m)
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(q4 + 2 * (bt + m * kGroup)));
-            }
+            QRegs<QBF16, MODE == kCoarse> qr;
+            qr.load(p.q, row, bt);
             const float wv = bt < kH ? __ldg(p.w + (int64_t)row * kH + bt) : 0.f;
             int bv = 0;
             if (MODE == kFine && bt < p.keep) bv = __ldg(p.top_blk + (int64_t)row * p.keep + bt);
@@ -349,73 +268,15 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             }
             if (!group_all(kBarBld, kGroup, w2)) { fail(); break; }
             const uint32_t qoff = kOffQ + (uint32_t)(i % kQB) * (3 * kQPlane);
-            if (QBF16) {
-#pragma unroll
-                for (int m = 0; m < kQU; ++m) {
-                    const int u = bt + m * kGroup;
-                    *reinterpret_cast<uint4 *>(smem + qoff + q_off(0, u >> 4, u & 15, NQ)) = qh[m];
-                }
-            } else {
-                auto put = [&](int m, const float4 &a, const float4 &b) {
-                    const int u = bt + m * kGroup;
-                    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                    uint4 pl[3];
-                    split3(x, pl);
-#pragma unroll
-                    for (int k = 0; k < 3; ++k)
-                        *reinterpret_cast<uint4 *>(smem + qoff + q_off(k, u >> 4, u & 15, NQ)) = pl[k];
-                };
-#pragma unroll
-                for (int m = 0; m < kQHeld; ++m) put(m, qf[2 * m], qf[2 * m + 1]);
-                if (kHalves) {
-#pragma unroll
-                    for (int m = kQHeld; m < kQU; ++m) {
-                        qf[2 * (m - kQHeld)] = __ldg(q4 + 2 * (bt + m * kGroup));
-                        qf[2 * (m - kQHeld) + 1] = __ldg(q4 + 2 * (bt + m * kGroup) + 1);
-                    }
-#pragma unroll
-                    for (int m = kQHeld; m < kQU; ++m) put(m, qf[2 * (m - kQHeld)], qf[2 * (m - kQHeld) + 1]);
-                }
-            }
+            qr.store(smem + qoff, bt);
             fence_async_smem();
             mbar_arrive(&bars[kBarQFull + i % kQB]);
             if (MODE == kCoarse && P.append_keys) {
-                // block means of the newly completed blocks [first_block, nb): thread bt owns
-                // dims 8 (bt / 8) .. + 7 of rows bt % 8 + 8 m; eight partial sums in row order,
-                // then the pairwise tree over the eight lanes of a dimension group
+                // block means of the newly completed blocks [first_block, nb)
                 const QMeta &M = meta[qb];
                 if (!M.state) {
-                    const int k = bt & 7, gq = bt >> 3;
-                    const uint4 *kv = reinterpret_cast<const uint4 *>(P.append_keys);
-                    float *means_w = const_cast<float *>(reinterpret_cast<const float *>(p.rows));
-                    for (int64_t beta = fb; beta < M.n; ++beta) {
-                        const uint4 *src = kv + (k0 + beta * 64) * (kD / 8);
-                        uint4 u[8];
-#pragma unroll
-                        for (int m = 0; m < 8; ++m) u[m] = __ldg(src + (8 * m + k) * (kD / 8) + gq);
-                        float ps[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) ps[e] = 0.f;
-#pragma unroll
-                        for (int m = 0; m < 8; ++m) {
-                            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&u[m]);
-#pragma unroll
-                            for (int e2 = 0; e2 < 4; ++e2) {
-                                const float2 f = __bfloat1622float2(h2[e2]);
-                                ps[2 * e2] += f.x;
-                                ps[2 * e2 + 1] += f.y;
-                            }
-                        }
-#pragma unroll
-                        for (int off = 1; off < 8; off <<= 1)
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) ps[e] += __shfl_xor_sync(0xffffffffu, ps[e], off);
-                        if (k == 0) {
-                            float4 *dst = reinterpret_cast<float4 *>(means_w + (M.base + beta) * kD + gq * 8);
-                            dst[0] = make_float4(ps[0] / 64.f, ps[1] / 64.f, ps[2] / 64.f, ps[3] / 64.f);
-                            dst[1] = make_float4(ps[4] / 64.f, ps[5] / 64.f, ps[6] / 64.f, ps[7] / 64.f);
-                        }
-                    }
+                    append_block_means(reinterpret_cast<const uint4 *>(P.append_keys), k0, fb, M.n,
+                                       const_cast<float *>(reinterpret_cast<const float *>(p.rows)), M.base, bt);
                     fence_async_global();               // the loader reads them by TMA
                 }
                 mbar_arrive(&bars[kBarMeansReady + qb]);
@@ -672,29 +533,8 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 for (int ch = 0; ch < 4; ++ch)
                     a[ch] = *reinterpret_cast<const float4 *>(rowp + (((4 * hf + ch) ^ (r & 7)) << 4));
                 mbar_arrive(&bars[kBarEmpty + kASlots + slot]);
-                // exact split by truncation: hi = top 8 significant bits, then the same of the
-                // (exact) remainder; the last remainder has at most 8 bits left
                 uint32_t pl[3][8];
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const float xs[4] = {a[ch].x, a[ch].y, a[ch].z, a[ch].w};
-                    uint32_t pk[3][4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t b0 = __float_as_uint(xs[q]) & 0xffff0000u;
-                        const float r1 = xs[q] - __uint_as_float(b0);
-                        const uint32_t b1 = __float_as_uint(r1) & 0xffff0000u;
-                        const float r2 = r1 - __uint_as_float(b1);
-                        pk[0][q] = b0;
-                        pk[1][q] = b1;
-                        pk[2][q] = __float_as_uint(r2);
-                    }
-#pragma unroll
-                    for (int k = 0; k < 3; ++k) {
-                        pl[k][2 * ch] = __byte_perm(pk[k][0], pk[k][1], 0x7632);   // {hi(e0), hi(e1)}
-                        pl[k][2 * ch + 1] = __byte_perm(pk[k][2], pk[k][3], 0x7632);
-                    }
-                }
+                split3_trunc16(a, pl);
                 fence_after_sync();                    // after the wait for the MMAs that read the box
 #pragma unroll
                 for (int k = 0; k < 3; ++k) tmem_st8(tlane + as * kABoxCols + k * 16, pl[k]);
