@@ -12,13 +12,17 @@
 namespace hisa {
 
 // ---- programmatic dependent launch ------------------------------------------------
-// Kernels of a step are launched with programmatic stream serialization: the launch of a
-// kernel is prepared while the previous kernel on the stream runs and is released when it
-// completes (none of these kernels triggers its dependents early: measured, an early or a
-// late trigger made the step slower). Every such kernel executes grid_dep_wait() before
-// its first global-memory access, which waits until the previous grid has completed and
-// its writes are visible, so results never depend on the overlap.
+// Kernels are launched with programmatic stream serialization: the launch of a kernel is
+// prepared while the previous kernel on the stream runs. grid_dep_wait() waits until the
+// previous grid has completed and its writes are visible. Most kernels execute it before
+// their first global-memory access. Two kinds of kernel let their successor start early,
+// once all of their CTAs have finished streaming (grid_dep_trigger): the coarse / fine
+// scoring pipeline, whose fine form reads q, w and the offsets before it waits and only
+// the kept blocks (the coarse output) after; and the combine, which waits before its first
+// selected id (the fine output) and first output write, after its first item's q and local
+// rows are on their way. Those early reads are of inputs no library call writes.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

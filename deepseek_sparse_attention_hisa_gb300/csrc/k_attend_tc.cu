@@ -191,7 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = misc->tmem;
-    grid_dep_wait();                                    // before the first global access
+    // no grid_dep_wait() here: the producers wait before their first selected id and the
+    // epilogue before its first output write; the first item's q and local rows go first
     bool ok = true;
     auto fail = [&]() {
         ok = false;
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
         int32_t *ids = reinterpret_cast<int32_t *>(smem + kOffIds);
         uint32_t g = 0;                                       // list tiles issued (all items)
         int n = 0;
+        bool waited = false;                                  // grid_dep_wait() done
         for (int id = blockIdx.x; id < items; id += gridDim.x, ++n) {
             const Item x = item_of(p, id);
             if (x.bad_off && x.split == 0 && pt == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
@@ -217,13 +219,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             const int32_t *Irow = p.I ? p.I + (int64_t)x.row * p.k : nullptr;
             const int64_t kk0 = x.e0 > x.nloc ? x.e0 - x.nloc : 0;
             const int64_t kk1 = x.e1 > x.nloc ? x.e1 - x.nloc : 0;
-            // the first 512 selected ids of the item, fetched now, staged after the local tiles
+            // the first 512 selected ids of the item, fetched now (the first item: once its q
+            // and local tiles are issued and the previous grid is done), staged after the local tiles
             int32_t pre[kPre];
+            auto fetch_pre = [&]() {
 #pragma unroll
-            for (int m = 0; m < kPre; ++m) {
-                const int64_t kk = kk0 + pt + kProdThreads * m;
-                pre[m] = (Irow && kk < kk1) ? Irow[kk] : -1;
-            }
+                for (int m = 0; m < kPre; ++m) {
+                    const int64_t kk = kk0 + pt + kProdThreads * m;
+                    pre[m] = (Irow && kk < kk1) ? Irow[kk] : -1;
+                }
+            };
+            if (waited) fetch_pre();
             const __nv_bfloat16 *qrow = reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)x.row * kH * kDH;
             {
                 // q dims [0, kQT) into the next ring slot (its Full barrier, like a tile's);
@@ -307,6 +313,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 good = issue_tile(i++);
             }
             if (!good) { fail(); break; }
+            if (!waited) {
+                grid_dep_wait();
+                waited = true;
+                fetch_pre();
+            }
             if (Irow) {
 #pragma unroll
                 for (int m = 0; m < kPre; ++m) {
@@ -582,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 break;
             }
             fence_after_sync();
+            if (n == 0) grid_dep_wait();                // before the first output write
             const bool have_o = x.T > 0;
             if (p.nsplit == 1) {
                 float *out = p.out + (int64_t)x.row * kH * kDH;

@@ -179,7 +179,9 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = misc->tmem;
-    grid_dep_wait();                                    // before the first global access
+    // coarse: before the first global access; fine: its builders wait before the first kept
+    // blocks (the coarse output), so that q, w and the offsets load while the coarse stage ends
+    if (MODE == kCoarse) grid_dep_wait();
     bool ok = true;
     auto fail = [&]() {
         ok = false;
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             QRegs<QBF16, MODE == kCoarse> qr;
             qr.load(p.q, row, bt);
             const float wv = bt < kH ? __ldg(p.w + (int64_t)row * kH + bt) : 0.f;
+            if (MODE == kFine && i == 0) grid_dep_wait();
             int bv = 0;
             if (MODE == kFine && bt < p.keep) bv = __ldg(p.top_blk + (int64_t)row * p.keep + bt);
             // the offsets and position this row's checks need, fetched with q
@@ -548,6 +551,9 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     if (!ok) flag(p.status, HISA_DEV_TIMEOUT);
     fence_before_sync();
     __syncthreads();
+    // every role of this CTA is done streaming: the next kernel may take over the SM once
+    // this CTA exits (it waits for this grid before it reads what this grid writes)
+    grid_dep_trigger();
     if (warp == kWarpMma) {
         fence_after_sync();
         tmem_dealloc(tmem, 512);

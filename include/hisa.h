@@ -13,6 +13,14 @@
  *    allocates, never frees, never synchronises the stream and keeps no state
  *    between calls; it is safe to call from several host threads on different
  *    streams with different workspaces.
+ *  - Consecutive calls overlap: kernels are launched as programmatic dependents
+ *    of the previous kernel on the stream. After hisa_block_filter(_append) or
+ *    hisa_select_topk, the next call may start before that call has finished:
+ *    hisa_select_topk then reads q, w, key_off and t0, and hisa_sparse_attend
+ *    reads q, local_kv, local_len, local_pos0, kv_off, t0 and sinks early, and
+ *    each waits before it reads the previous call's outputs (top_blk, I). So an
+ *    input of a call must not be an output of the library call just before it
+ *    on the same stream, other than top_blk / I as documented.
  *  - Ragged batches: sequence b owns pooled rows [key_off[b], key_off[b+1]) of the
  *    packed key / KV arrays, so Np_b = key_off[b+1] - key_off[b] (int64, device).
  *  - Positions: t0[b] (int32, device) is the absolute token position of query
