@@ -17,7 +17,9 @@
 // split each head's tile rows), 4 S = Q.K^T issue and TMEM owner, 5-8 producers (cp.async
 // gather, 128-byte swizzle, zero-fill of rows that are invisible or past the list), 9
 // O += V^T.P^T issue (two issuing warps, so that neither product waits behind the other),
-// 10-13 epilogue (O^T -> out while the other warps start the next item). Every mbarrier
+// 10-13 epilogue (each item's q dims 0-255 from its ring slot into TMEM, the next item's
+// as soon as this item's S products are done, then O^T -> out while the other warps
+// start the next item). Every mbarrier
 // wait is bounded; a timeout sets HISA_DEV_TIMEOUT, raises a shared abort flag and the CTA
 // drains and exits.
 #include "hisa_internal.cuh"
@@ -35,7 +37,7 @@ constexpr int kPvWarp = kProdWarp0 + kProdWarps;
 constexpr int kEpiWarp0 = kPvWarp + 1, kEpiWarps = 4;
 constexpr int kProdThreads = 32 * kProdWarps;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
-constexpr int kBarSoft = 1, kBarProd = 2;             // named barriers (0 = __syncthreads)
+constexpr int kBarSoft = 1, kBarProd = 2, kBarEpi = 3; // named barriers (0 = __syncthreads)
 // q: dims [0, kQT) are the A operand of the S products from TMEM (copied there through a
 // ring slot at the start of each item), dims [kQT, 512) from shared memory
 constexpr int kQT = 256;
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 b == kBarStat)
                 cnt = kSoftWarps * 32;
             if (b == kBarQ) cnt = kProdThreads;
-            if (b == kBarQT) cnt = kSoftWarps * 32;
+            if (b == kBarQT) cnt = kEpiWarps * 32;
             if (b == kBarOFree) cnt = kEpiWarps * 32;
             if (b == kBarDrain) cnt = 2;                  // one commit from each issuing warp
             mbar_init(&bars[b], cnt);
@@ -446,41 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
         for (int id = blockIdx.x; id < items; id += gridDim.x, ++n) {
             const Item x = item_of(p, id);
             float m2 = -INFINITY, l = 0.f;
-            {
-                // q dims [0, kQT) of this item, from the ring slot the producers filled, into
-                // TMEM (the previous item's S products, whose scores this warp has read, no
-                // longer need the old ones); lane l < 16 of warp w holds head 16 w + l, as the
-                // M = 64 A operand wants; then the slot is free again
-                const int s = g % kSlots;
-                const bool wq = wait_bar(&bars[kBarFull + s], (g / kSlots) & 1, abort);
-                if (!group_all(kBarSoft, kSoftWarps * 32, wq)) { fail(); break; }
-                const uint8_t *qs = smem + kOffKV + s * kSlotBytes;
-                const int hq = warp * 16 + (lane & 15);
-#pragma unroll 2
-                for (int c0 = 0; c0 < kQT / 2; c0 += 16) {   // 16 columns = 32 dims = 4 units
-                    float v[16];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
-                        if (lane < 16) {
-                            const int qu = c0 / 4 + u;            // dims 8 qu .. + 7
-                            w4 = *reinterpret_cast<const uint4 *>(qs + (qu >> 3) * kQChunk +
-                                                                  sw128_offset(hq, (qu & 7) * 8));
-                        }
-                        v[4 * u] = __uint_as_float(w4.x);
-                        v[4 * u + 1] = __uint_as_float(w4.y);
-                        v[4 * u + 2] = __uint_as_float(w4.z);
-                        v[4 * u + 3] = __uint_as_float(w4.w);
-                    }
-                    tmem_st16(tmem + ((uint32_t)(32 * warp) << 16) + kColQ + c0, v);
-                }
-                tmem_st_wait();
-                fence_before_sync();
-                mbar_arrive(&bars[kBarQT]);
-                named_or_soft(0u);                          // every lane has read the slot
-                if (tid == 0) mbar_arrive(&bars[kBarEmpty + s]);
-                ++g;
-            }
+            ++g;                                        // the ring entry that carried q (the epilogue's)
             for (int i = 0; i < x.T; ++i, ++g, ++gt) {
                 const int s = g % kSlots, sb = gt & 1;
                 const bool w = wait_bar(&bars[kBarFull + s], (g / kSlots) & 1, abort) &&
@@ -583,11 +551,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             mbar_arrive(&bars[kBarStat]);
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
-        // ---------------- epilogue (warps 10-13): O^T -> out, beside the next item ------
+        // ---------------- epilogue (warps 10-13): q -> TMEM, O^T -> out, beside the stream ------
         const int quad = warp & 3;                      // TMEM lanes 32 quad .. + 31 = dims
+        const int et = tid - kEpiWarp0 * 32;
+        // q dims [0, kQT) of an item, from the ring entry gq the producers filled, into TMEM:
+        // lane l < 16 of the warp of lane quadrant c holds head 16 c + l, as the M = 64 A operand
+        // wants; then the slot is free again
+        auto copy_q = [&](uint32_t gq) -> bool {
+            const int s = gq % kSlots;
+            const bool wq = wait_bar(&bars[kBarFull + s], (gq / kSlots) & 1, abort);
+            if (!group_all(kBarEpi, kEpiWarps * 32, wq)) return false;
+            const uint8_t *qs = smem + kOffKV + s * kSlotBytes;
+            const int hq = quad * 16 + (lane & 15);
+#pragma unroll 2
+            for (int c0 = 0; c0 < kQT / 2; c0 += 16) {   // 16 columns = 32 dims = 4 units
+                float v[16];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
+                    if (lane < 16) {
+                        const int qu = c0 / 4 + u;            // dims 8 qu .. + 7
+                        w4 = *reinterpret_cast<const uint4 *>(qs + (qu >> 3) * kQChunk +
+                                                              sw128_offset(hq, (qu & 7) * 8));
+                    }
+                    v[4 * u] = __uint_as_float(w4.x);
+                    v[4 * u + 1] = __uint_as_float(w4.y);
+                    v[4 * u + 2] = __uint_as_float(w4.z);
+                    v[4 * u + 3] = __uint_as_float(w4.w);
+                }
+                tmem_st16(tmem + ((uint32_t)(32 * quad) << 16) + kColQ + c0, v);
+            }
+            tmem_st_wait();
+            fence_before_sync();
+            mbar_arrive(&bars[kBarQT]);
+            asm volatile("bar.sync %0, %1;" ::"n"(kBarEpi), "n"(kEpiWarps * 32) : "memory");   // slot read
+            if (et == 0) mbar_arrive(&bars[kBarEmpty + s]);
+            return true;
+        };
+        uint32_t gq = 0;                                // ring entry of this item's q
         int n = 0;
         for (int id = blockIdx.x; id < items; id += gridDim.x, ++n) {
             const Item x = item_of(p, id);
+            if (n == 0 && !copy_q(0)) { fail(); break; }
+            // the next item's q, as soon as this item's S products no longer read the old one
+            if (id + (int)gridDim.x < items) {
+                const bool wf = wait_bar(&bars[kBarQFree], n & 1, abort);
+                if (!group_all(kBarEpi, kEpiWarps * 32, wf)) { fail(); break; }
+                fence_after_sync();
+                gq += 1u + (uint32_t)x.T;
+                if (!copy_q(gq)) { fail(); break; }
+            }
             if (!wait_bar(&bars[kBarStat], n & 1, abort) || !wait_bar(&bars[kBarOFull], n & 1, abort)) {
                 fail();
                 break;
