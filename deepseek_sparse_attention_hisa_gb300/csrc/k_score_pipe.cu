@@ -195,16 +195,11 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             const int qb = i & 1;
             const int row = (int)blockIdx.x + i * (int)gridDim.x;
             const int bq = row / p.L, j = row - bq * p.L;
-            // this row's q, weights and kept blocks first: the loads overlap the waits. With
-            // 22 warps (coarse, f32 q) only half of q is held in registers; the other half is
-            // prefetched into L2 and read once the previous query's planes are free.
-            QRegs<QBF16, MODE == kCoarse> qr;
-            qr.load(p.q, row, bt);
+            // this row's weights, offsets and position first (the row's checks and the loader's
+            // first copies wait on them), then q, then the kept blocks: the loads overlap the
+            // waits. With 22 warps (coarse, f32 q) only half of q is held in registers; the other
+            // half is prefetched into L2 and read once the previous query's planes are free.
             const float wv = bt < kH ? __ldg(p.w + (int64_t)row * kH + bt) : 0.f;
-            if (MODE == kFine && i == 0) grid_dep_wait();
-            int bv = 0;
-            if (MODE == kFine && bt < p.keep) bv = __ldg(p.top_blk + (int64_t)row * p.keep + bt);
-            // the offsets and position this row's checks need, fetched with q
             const int64_t k0 = p.key_off[bq], k1 = p.key_off[bq + 1];
             int64_t m0 = 0, m1 = 0, fb = 0;
             if (MODE == kCoarse) {
@@ -214,6 +209,11 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 fb = fb < 0 ? 0 : fb;
             }
             const int64_t t_row = p.causal ? (int64_t)p.t0[bq] + j : 0;
+            QRegs<QBF16, MODE == kCoarse> qr;
+            qr.load(p.q, row, bt);
+            if (MODE == kFine && i == 0) grid_dep_wait();
+            int bv = 0;
+            if (MODE == kFine && bt < p.keep) bv = __ldg(p.top_blk + (int64_t)row * p.keep + bt);
             // meta slot qb is free once query i - 2 is selected
             const bool w1 = i < 2 || wait_bar(&bars[kBarSlotFree + qb], ((i >> 1) - 1) & 1, abort);
             if (!group_all(kBarBld, kGroup, w1)) { fail(); break; }
