@@ -72,6 +72,19 @@ def stage_bytes(wl, nb):
     return dict(block_filter_append=means + filt, select_topk=sel, sparse_attend=att), step
 
 
+def step_bytes_rows(wl, nb, L):
+    """Unique algorithmic bytes of one sequence's step with L query rows (decode: L = 1):
+    per sequence the newest block's keys in and its mean out, all nb block means, the local
+    rows (window + L - 1) and the sinks; per row q, w, the kept blocks' keys, top_blk, I,
+    the attention q, the gathered rows and the output (rows select their own sets)."""
+    H_i, D_i, b, keep, k, H, Dh, W = (wl.H_i, wl.D_i, wl.index_block, wl.index_keep,
+                                      wl.index_topk, wl.H, wl.Dh, wl.window)
+    per_seq = b * D_i * 2 + D_i * 4 + nb * D_i * 4 + (W + L - 1) * Dh * 2 + H * 4
+    per_row = (H_i * D_i * 4 + H_i * 4 + keep * b * D_i * 2 + keep * 4 + k * 4 +
+               H * Dh * 2 + k * Dh * 2 + H * Dh * 4)
+    return per_seq + L * per_row
+
+
 # ----------------------------------------------------------------------------
 # clocks during the timed region
 # ----------------------------------------------------------------------------
@@ -369,8 +382,8 @@ def run_gpu(args, wl, R):
     def calls_for(pr):
         return {
             "block_filter_append": lambda s: pr.block_filter_append(first_block=newest, stream=s),
-            "select_topk": lambda s: pr.select_topk(stream=s),
-            "sparse_attend": lambda s: pr.attend(stream=s),
+            "select_topk": lambda s: pr.select_topk(stream=s, chained=True),
+            "sparse_attend": lambda s: pr.attend(stream=s, chained=True),
         }
     calls = calls_for(prob)
     stream.wait_stream(torch.cuda.current_stream())
@@ -534,6 +547,11 @@ def run_gpu(args, wl, R):
         line["latency_one_query"] = run_latency(wl, dev, stream)
         line["long_context_selection"] = run_long_context(dev, stream)
         line["prefill_hisa_step"] = run_prefill_hisa(dev, stream)
+        line["ragged_decode_b32"] = run_ragged(dev, stream)
+        line["verify_L4"] = run_verify(dev, stream)
+        line["compressor_append"] = run_compress(dev, stream, R)
+    if not args.no_np_sweep and world == 1:
+        line["decode_np_sweep"] = run_np_sweep(dev, stream, R)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -625,6 +643,136 @@ def capture(fn, stream):
     return g
 
 
+def decode_leg(wl, dev, stream, flush, n, seed, what):
+    """One step over wl's batch (newest block means appended, coarse filter, fine top-k,
+    combine; the last two chained), captured as one graph and timed after an L2 flush.
+    Bytes are the step's unique algorithmic bytes (step_bytes_rows) summed over sequences."""
+    import torch
+
+    from deepseek_sparse_attention_hisa_gb300.problem import Problem
+    data = inputs.generate_device(wl, device=dev, seed=seed)
+    prob = Problem(data, device=dev)
+    newest = torch.as_tensor((prob.nb - 1).astype(np.int32), device=dev)
+    prob.block_means()
+    torch.cuda.synchronize()
+
+    stages = {"block_filter_append": lambda s: prob.block_filter_append(first_block=newest, stream=s),
+              "select_topk": lambda s: prob.select_topk(stream=s, chained=True),
+              "sparse_attend": lambda s: prob.attend(stream=s, chained=True)}
+
+    def step(s):
+        for fn in stages.values():
+            fn(s)
+    g = capture(step, stream)
+    mean, med = timed_graph(g, stream, flush, n)
+    stage_us = {k: timed_graph(capture(fn, stream), stream, flush, n)[0] * 1e3
+                for k, fn in stages.items()}
+    assert prob.status(stream) == 0, f"device status flags set in the {what} leg"
+    nbytes = sum(step_bytes_rows(wl, int(nb), wl.L) for nb in prob.nb)
+    peak, src = peaks()
+    rows = wl.B * wl.L
+    out = {"us_per_step": mean * 1e3, "us_median": med * 1e3, "stages_us": stage_us,
+           "rows_per_step": rows,
+           "rows_per_s": rows / (mean / 1e3), "ns_per_row": mean * 1e6 / rows,
+           "bytes_per_step": nbytes, "hbm_gbs": nbytes / (mean / 1e3) / 1e9,
+           "frac": nbytes / (mean / 1e3) / 1e9 / peak, "peak_source": src}
+    del prob, data, g
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_np_sweep(dev, stream, R, n=10):
+    """Decode step time against context length: R independent V4-Flash decode queries per
+    step at Np = 4K .. 256K pooled rows (16K .. 1M tokens). HiSA's work per query is
+    O(nb + keep * b + k), so only the coarse stage's nb * 512 B of block means grows."""
+    wl = inputs.WORKLOADS["v4flash_decode"]
+    flush = L2Flush(dev)
+    out = {"workload": f"v4flash_decode, R = {R} queries per step, keep = 16, k = 512", "points": []}
+    for Np in (4096, 16384, 32768, 65536, 131072, 262144):
+        r = decode_leg(wl.replace(B=R, Np=(Np,)), dev, stream, flush, n, 5000 + Np, f"Np={Np}")
+        r["Np"] = Np
+        r["bytes_per_query"] = r.pop("bytes_per_step") // R
+        out["points"].append(r)
+    return out
+
+
+def run_ragged(dev, stream, n=20):
+    """The batched ragged decode workload itself: B = 32 sequences with Np_b drawn uniformly
+    from [4096, 65536] (the workload's own seed-2 draw), one step per batch of 32."""
+    wl = inputs.WORKLOADS["ragged_decode"]
+    r = decode_leg(wl, dev, stream, L2Flush(dev), n, wl.seed, "ragged")
+    r["workload"] = "ragged_decode: B = 32, Np_b ~ U[4096, 65536] (seed 2), one batch per step"
+    return r
+
+
+def run_verify(dev, stream, L=4, R=304, n=10):
+    """Multi-token verify on the HiSA batched path: R / L sequences of Np = 32768 pooled rows,
+    L draft tokens each at t0 .. t0 + L - 1 = 4 Np - L .. 4 Np - 1 (the first rows see one
+    pooled row fewer), so the step holds R query rows like the decode step."""
+    wl = inputs.WORKLOADS["v4flash_decode"]
+    B = R // L
+    r = decode_leg(wl.replace(B=B, L=L, Np=(32768,), t0=4 * 32768 - L), dev, stream, L2Flush(dev),
+                   n, 6000 + L, "verify")
+    r["workload"] = f"verify: B = {B} sequences x L = {L} draft tokens, Np = 32768"
+    return r
+
+
+def run_compress(dev, stream, R, n=20):
+    """The indexer compressor (hisa_compress_append; DeepSeek-V4 indexer shape: D_i = 128,
+    r = 4, overlap, RoPE on 64 dims, bf16 cache, block means of 64 rows): (a) decode, R
+    sequences appending one pooled row each, the row that completes block 511 (so each
+    also writes a block mean from the 64 stored rows); (b) prefill, one sequence appending
+    1024 pooled rows (4096 tokens, 16 blocks). Projected token rows drawn on the device."""
+    import torch
+
+    from deepseek_sparse_attention_hisa_gb300 import binding as hb
+    flush = L2Flush(dev)
+    out = {}
+    for name, B, p0, nn in (("decode", R, 32767, 1), ("prefill", 1, 0, 1024)):
+        D, r, C = 128, 4, 256
+        cap = p0 + nn
+        T = (nn + 1) * r
+        g = torch.Generator(device=dev)
+        g.manual_seed(7000 + B)
+        kv = torch.randn((B * T, C), generator=g, device=dev)
+        gate = torch.randn((B * T, C), generator=g, device=dev)
+        ape = torch.randn((r, C), generator=g, device=dev)
+        norm_w = 1.0 + 0.1 * torch.randn((D,), generator=g, device=dev)
+        keys = torch.randn((B * cap, D), generator=g, device=dev).to(torch.bfloat16)
+        tok_off = torch.arange(B + 1, device=dev, dtype=torch.int64) * T
+        key_off = torch.arange(B + 1, device=dev, dtype=torch.int64) * cap
+        nb = cap // 64
+        means_off = torch.arange(B + 1, device=dev, dtype=torch.int64) * nb
+        means = torch.zeros((B * nb, D), device=dev)
+        p_first = torch.full((B,), p0, dtype=torch.int32, device=dev)
+        n_new = torch.full((B,), nn, dtype=torch.int32, device=dev)
+        desc = hb.CompressDesc(B=B, D_i=D, r=r, overlap=1, rope_dims=64, index_block=64,
+                               n_new_max=nn, k_dtype=hb.HISA_BF16, rope_theta=160000.0,
+                               eps=1e-6, tok_rows=B * T, keys_rows=B * cap, means_rows=B * nb)
+        ws = hb.alloc_workspace(hb.workspace_bytes(hb.OP_COMPRESS, desc), dev)
+
+        def call(s, desc=desc, kv=kv, gate=gate, tok_off=tok_off, p_first=p_first, n_new=n_new,
+                 ape=ape, norm_w=norm_w, keys=keys, key_off=key_off, means=means,
+                 means_off=means_off, ws=ws):
+            hb.compress_append(desc, kv, gate, tok_off, p_first, n_new, ape, norm_w, keys,
+                               key_off, means, means_off, ws, s)
+        gr = capture(call, stream)
+        mean, med = timed_graph(gr, stream, flush, n)
+        assert hb.device_status(ws, stream) == 0
+        # bytes: the token rows (kv and gate of the previous and new windows), ape and norm
+        # weight, the new rows out, and per completed block its 64 rows in and its mean out
+        blocks = B * ((p0 + nn) // 64 - p0 // 64)
+        nbytes = (B * T * C * 4 * 2 + r * C * 4 + D * 4 + B * nn * D * 2 +
+                  blocks * (64 * D * 2 + D * 4))
+        peak, src = peaks()
+        out[name] = {"sequences": B, "new_rows_each": nn, "us": mean * 1e3, "us_median": med * 1e3,
+                     "bytes": nbytes, "hbm_gbs": nbytes / (mean / 1e3) / 1e9,
+                     "frac": nbytes / (mean / 1e3) / 1e9 / peak, "peak_source": src}
+        del kv, gate, keys, means, gr
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_prefill_hisa(dev, stream, n=10):
     """The HiSA batched path on the prefill workload (one sequence, L = 4096 new rows,
     Np = 16384 pooled rows, bf16 q and keys): block means once, then per step the coarse
@@ -653,6 +801,17 @@ def run_prefill_hisa(dev, stream, n=10):
     assert prob.status(stream) == 0
     out["step_us"] = total * 1e3
     out["rows_per_s"] = wl.L / (total / 1e3)
+    # per-stage tensor-core work (plain multiply-add counts; masked work included) against
+    # the bf16 peak: coarse L x nb x H_i x D_i, fine L x keep*b x H_i x D_i, combine
+    # L x (window + k) x H x Dh for S and again for PV
+    Lr, nb = wl.L, int(wl.Np[0]) // wl.index_block
+    flops = {"block_filter": Lr * nb * wl.H_i * wl.D_i * 2,
+             "select_topk": Lr * wl.index_keep * wl.index_block * wl.H_i * wl.D_i * 2,
+             "sparse_attend": Lr * (wl.window + wl.index_topk) * wl.H * wl.Dh * 4}
+    peak, src = bf16_peak()
+    out["tensor_frac"] = {k: v / (out[k + "_us"] * 1e-6) / 1e12 / peak for k, v in flops.items()}
+    out["tensor_peak_tflops"] = peak
+    out["tensor_peak_source"] = src
     return out
 
 
@@ -722,8 +881,8 @@ def run_latency(wl, dev, stream, n=50):
 
     def step(s):
         prob.block_filter_append(first_block=newest, stream=s)
-        prob.select_topk(stream=s)
-        prob.attend(stream=s)
+        prob.select_topk(stream=s, chained=True)
+        prob.attend(stream=s, chained=True)
     g = capture(step, stream)
     mean, med = timed_graph(g, stream, L2Flush(dev), n)
     assert prob.status(stream) == 0
@@ -790,6 +949,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill scoring leg")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the one-query latency and long-context selection legs")
+    ap.add_argument("--no-np-sweep", action="store_true",
+                    help="skip the decode step time at Np = 4K .. 256K (R queries each)")
     ap.add_argument("--Np", type=int, default=32768,
                     help="pooled rows per sequence (32768 = the V4-Flash 131072-token prefix)")
     args = ap.parse_args()

@@ -17,9 +17,11 @@ LIB_PATH = os.path.join(_PKG, "libhisa.so")
 
 HISA_OK, HISA_EINVAL, HISA_EDTYPE, HISA_EWORKSPACE, HISA_ECUDA, HISA_EDEVICE = 0, -1, -2, -3, -4, -5
 HISA_F32, HISA_BF16 = 0, 1
+FLAG_CHAINED = 0x1
 DEV_BAD_OFFSETS, DEV_GATE, DEV_BAD_ID, DEV_NONFINITE, DEV_BAD_BLOCK, DEV_TIMEOUT = \
     0x1, 0x2, 0x4, 0x8, 0x10, 0x20
 FLAT_NOALLOC_MAX_SCORES = 1 << 22
+OP_COMPRESS = 6
 OP_INDEX_SCORES, OP_BLOCK_MEANS, OP_BLOCK_FILTER, OP_SELECT_TOPK, OP_FLAT_TOPK, OP_SPARSE_ATTEND = \
     range(6)
 
@@ -36,7 +38,7 @@ class IndexDesc(ctypes.Structure):
                 ("index_block", ctypes.c_int32), ("index_keep", ctypes.c_int32),
                 ("Np_max", ctypes.c_int64), ("keys_rows", ctypes.c_int64),
                 ("means_rows", ctypes.c_int64),
-                ("q_dtype", ctypes.c_int32), ("k_dtype", ctypes.c_int32)]
+                ("q_dtype", ctypes.c_int32), ("k_dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class AttnDesc(ctypes.Structure):
@@ -44,7 +46,16 @@ class AttnDesc(ctypes.Structure):
                 ("Dh", ctypes.c_int32), ("window", ctypes.c_int32), ("W_max", ctypes.c_int32),
                 ("r", ctypes.c_int32), ("k", ctypes.c_int32), ("Np_max", ctypes.c_int64),
                 ("kv_rows", ctypes.c_int64), ("scale", ctypes.c_float), ("q_dtype", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int32)]
+                ("kv_dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+class CompressDesc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("D_i", ctypes.c_int32), ("r", ctypes.c_int32),
+                ("overlap", ctypes.c_int32), ("rope_dims", ctypes.c_int32),
+                ("index_block", ctypes.c_int32), ("n_new_max", ctypes.c_int32),
+                ("k_dtype", ctypes.c_int32), ("rope_theta", ctypes.c_float), ("eps", ctypes.c_float),
+                ("tok_rows", ctypes.c_int64), ("keys_rows", ctypes.c_int64),
+                ("means_rows", ctypes.c_int64), ("flags", ctypes.c_int32)]
 
 
 _lib = None
@@ -63,6 +74,7 @@ _SIG = {
     "hisa_block_filter_append": (ctypes.c_int32, [_P] * 11 + [ctypes.c_int64, _P, ctypes.c_size_t, _P]),
     "hisa_flat_topk_noalloc": (ctypes.c_int32, [_P] * 9),
     "hisa_sparse_attend": (ctypes.c_int32, [_P] * 12 + [ctypes.c_size_t, _P]),
+    "hisa_compress_append": (ctypes.c_int32, [_P] * 13 + [ctypes.c_size_t, _P]),
 }
 
 
@@ -204,6 +216,15 @@ def sparse_attend(desc, q, local_kv, local_len, local_pos0, pooled_kv, kv_off, I
                                     _ptr(local_pos0), _ptr(pooled_kv), _ptr(kv_off), _ptr(I),
                                     _ptr(sinks), _ptr(t0), _ptr(out), _ptr(ws), ws.numel(),
                                     _stream(stream)), "hisa_sparse_attend")
+
+
+def compress_append(desc, kv, gate, tok_off, p_first, n_new, ape, norm_w, keys, key_off, means,
+                    means_off, ws, stream=None):
+    _check(lib().hisa_compress_append(ctypes.byref(desc), _ptr(kv), _ptr(gate), _ptr(tok_off),
+                                      _ptr(p_first), _ptr(n_new), _ptr(ape), _ptr(norm_w),
+                                      _ptr(keys), _ptr(key_off), _ptr(means), _ptr(means_off),
+                                      _ptr(ws), ws.numel(), _stream(stream)),
+           "hisa_compress_append")
 
 
 # ----------------------------------------------------------------------------

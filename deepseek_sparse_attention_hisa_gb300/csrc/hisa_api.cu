@@ -28,6 +28,7 @@ hisa_status check_index_desc(const hisa_index_desc *d) {
     if (d->keys_rows < 0 || d->keys_rows > 0x7fffffffLL) return HISA_EINVAL;
     if (d->means_rows < 0 || d->means_rows > 0x7fffffffLL) return HISA_EINVAL;
     if ((int64_t)d->B * d->L > 0x7fffffffLL) return HISA_EINVAL;
+    if (d->flags & ~(int32_t)HISA_FLAG_CHAINED) return HISA_EINVAL;
     if (!dtype_ok(d->q_dtype) || !dtype_ok(d->k_dtype)) return HISA_EDTYPE;
     if (d->D_i != 32 && d->D_i != 64 && d->D_i != 128) return HISA_EDTYPE;
     return HISA_OK;
@@ -51,9 +52,28 @@ hisa_status check_attn_desc(const hisa_attn_desc *d) {
     if (d->Np_max < 0 || d->Np_max > 0x7fffffffLL) return HISA_EINVAL;
     if (d->kv_rows < 0 || d->kv_rows > 0x7fffffffLL) return HISA_EINVAL;
     if ((int64_t)d->B * d->L > 0x7fffffffLL) return HISA_EINVAL;
+    if (d->flags & ~(int32_t)HISA_FLAG_CHAINED) return HISA_EINVAL;
     if (!dtype_ok(d->q_dtype) || !dtype_ok(d->kv_dtype) || d->q_dtype != d->kv_dtype)
         return HISA_EDTYPE;
     if (!attend_simt_supported(d->H, d->Dh)) return HISA_EDTYPE;
+    return HISA_OK;
+}
+
+hisa_status check_compress_desc(const hisa_compress_desc *d) {
+    if (!d) return HISA_EINVAL;
+    if (d->B < 1 || d->r < 1 || d->r > 128 || (d->overlap != 0 && d->overlap != 1)) return HISA_EINVAL;
+    if (d->rope_dims < 0 || d->rope_dims > d->D_i || (d->rope_dims & 1)) return HISA_EINVAL;
+    if (d->index_block < 0 || d->index_block > 8192) return HISA_EINVAL;
+    if (d->n_new_max < 0 || d->n_new_max > (1 << 20)) return HISA_EINVAL;
+    if (!(d->rope_theta > 1.f) || !(d->eps > 0.f)) return HISA_EINVAL;
+    if (d->tok_rows < 0 || d->keys_rows < 0 || d->means_rows < 0) return HISA_EINVAL;
+    if (d->flags & ~(int32_t)HISA_FLAG_CHAINED) return HISA_EINVAL;
+    if (!dtype_ok(d->k_dtype)) return HISA_EDTYPE;
+    if (d->D_i != 32 && d->D_i != 64 && d->D_i != 128) return HISA_EDTYPE;
+    if ((int64_t)d->B * (d->n_new_max / (d->index_block > 0 ? d->index_block : 64) + 2) >
+        ((int64_t)1 << 31))
+        return HISA_EINVAL;
+    if (d->B > 65535) return HISA_EINVAL;
     return HISA_OK;
 }
 
@@ -120,6 +140,7 @@ ScoreParams score_params(const hisa_index_desc *d, int mode, const void *q, cons
     p.keys_rows = d->keys_rows;
     p.means_rows = d->means_rows;
     p.status = status_of(ws);
+    p.chained = (d->flags & HISA_FLAG_CHAINED) != 0;
     return p;
 }
 
@@ -135,12 +156,12 @@ int device_sms() {
     return counts[dev];
 }
 
-// A few long coarse / fine rows (a single long-context query, a small batch): one CTA per
-// row would leave most SMs idle, so each row's tiles are split over CTAs and a separate
-// select follows.
+// Few coarse / fine rows (a small batch, a single query, a long-context query): one CTA
+// per row would leave most SMs idle, so when the rows fill less than half of the SMs each
+// row's tiles are split over CTAs and a separate select follows.
 bool split_rows(const hisa_index_desc *d, int mode, int64_t n) {
     const int sms = device_sms();
-    return sms > 0 && n >= 2048 && n_rows(d) * 8 <= sms &&
+    return sms > 0 && n >= 256 && n_rows(d) * 2 <= sms &&
            score_tc_split_ok(mode, d->H_i, d->D_i, mode == kFine ? d->k_dtype == HISA_BF16 : 0,
                              d->index_block);
 }
@@ -200,6 +221,9 @@ const char *hisa_status_string(int32_t status) {
 
 size_t hisa_workspace_bytes(int32_t op, const void *desc) {
     if (!desc) return 0;
+    if (op == HISA_OP_COMPRESS)
+        return check_compress_desc(static_cast<const hisa_compress_desc *>(desc)) == HISA_OK
+                   ? kStatusBytes : 0;
     if (op == HISA_OP_SPARSE_ATTEND) {
         const hisa_attn_desc *d = static_cast<const hisa_attn_desc *>(desc);
         if (check_attn_desc(d) != HISA_OK) return 0;
@@ -281,6 +305,7 @@ hisa_status hisa_block_means(const hisa_index_desc *d, const void *keys, const i
     p.key_off = key_off; p.means_off = means_off; p.first_block = first_block;
     p.means = means; p.Np_max = d->Np_max; p.keys_rows = d->keys_rows;
     p.means_rows = d->means_rows; p.status = status_of(ws);
+    p.chained = (d->flags & HISA_FLAG_CHAINED) != 0;
     return from_cuda(launch_block_means(p, d->Np_max / d->index_block,
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -336,7 +361,7 @@ hisa_status hisa_block_filter_append(const hisa_index_desc *d, const void *q, co
     if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_BLOCK_FILTER, d))) != HISA_OK)
         return st;
     const bool fused = d->L == 1 && d->k_dtype == HISA_BF16 && d->index_block == 64 && d->D_i == 128 &&
-                       d->means_rows > 0 && d->keys_rows > 0 &&
+                       d->means_rows > 0 && d->keys_rows > 0 && !split_rows(d, kCoarse, nb_max) &&
                        score_pipe_supported(kCoarse, d->H_i, d->D_i, 0, nb_max, d->index_block,
                                             d->index_keep);
     if (!fused) {
@@ -418,6 +443,37 @@ hisa_status hisa_flat_topk(const hisa_index_desc *d, const void *q, const float 
     return from_cuda(launch_select(sp, d->Np_max, s));
 }
 
+hisa_status hisa_compress_append(const hisa_compress_desc *d, const float *kv, const float *gate,
+                                 const int64_t *tok_off, const int32_t *p_first,
+                                 const int32_t *n_new, const float *ape, const float *norm_w,
+                                 void *keys, const int64_t *key_off, float *means,
+                                 const int64_t *means_off, void *ws, size_t ws_bytes,
+                                 hisa_stream_t stream) {
+    hisa_status st = check_compress_desc(d);
+    if (st != HISA_OK) return st;
+    if (!kv || !gate || !tok_off || !p_first || !n_new || !ape || !norm_w || !keys || !key_off)
+        return HISA_EINVAL;
+    if (means && !means_off) return HISA_EINVAL;
+    if (!aligned(kv, 4) || !aligned(gate, 4) || !aligned(ape, 4) || !aligned(norm_w, 4) ||
+        !aligned(keys, d->k_dtype == HISA_BF16 ? 2 : 4) || (means && !aligned(means, 4)))
+        return HISA_EINVAL;
+    if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_COMPRESS, d))) != HISA_OK)
+        return st;
+    CompressParams p{};
+    p.B = d->B; p.D = d->D_i; p.C = d->overlap ? 2 * d->D_i : d->D_i; p.r = d->r;
+    p.overlap = d->overlap; p.rope_dims = d->rope_dims; p.b = d->index_block;
+    p.n_new_max = d->n_new_max; p.k_bf16 = d->k_dtype == HISA_BF16; p.eps = d->eps;
+    p.log_theta = std::log((double)d->rope_theta);
+    p.kv = kv; p.gate = gate; p.ape = ape; p.norm_w = norm_w;
+    p.tok_off = tok_off; p.p_first = p_first; p.n_new = n_new;
+    p.keys = keys; p.key_off = key_off;
+    p.means = d->index_block > 0 ? means : nullptr; p.means_off = means_off;
+    p.tok_rows = d->tok_rows; p.keys_rows = d->keys_rows; p.means_rows = d->means_rows;
+    p.status = status_of(ws);
+    p.chained = (d->flags & HISA_FLAG_CHAINED) != 0;
+    return from_cuda(launch_compress(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 hisa_status hisa_sparse_attend(const hisa_attn_desc *d, const void *q, const void *local_kv,
                                const int32_t *local_len, const int32_t *local_pos0,
                                const void *pooled_kv, const int64_t *kv_off, const int32_t *I,
@@ -450,6 +506,7 @@ hisa_status hisa_sparse_attend(const hisa_attn_desc *d, const void *q, const voi
     p.rows_per_split = (int)per;
     p.kv_bf16 = d->kv_dtype == HISA_BF16;
     p.status = status_of(ws);
+    p.chained = (d->flags & HISA_FLAG_CHAINED) != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (attend_tc_supported(d->H, d->Dh, p.kv_bf16)) return from_cuda(launch_attend_tc(p, s));
     return from_cuda(launch_attend_simt(p, s));

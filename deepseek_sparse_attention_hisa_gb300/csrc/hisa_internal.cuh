@@ -7,26 +7,31 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/hisa.h"
 
 namespace hisa {
 
 // ---- programmatic dependent launch ------------------------------------------------
-// Kernels are launched with programmatic stream serialization: the launch of a kernel is
-// prepared while the previous kernel on the stream runs. grid_dep_wait() waits until the
-// previous grid has completed and its writes are visible. Most kernels execute it before
-// their first global-memory access. Two kinds of kernel let their successor start early,
-// once all of their CTAs have finished streaming (grid_dep_trigger): the coarse / fine
-// scoring pipeline, whose fine form reads q, w and the offsets before it waits and only
-// the kept blocks (the coarse output) after; and the combine, which waits before its first
-// selected id (the fine output) and first output write, after its first item's q and local
-// rows are on their way. Those early reads are of inputs no library call writes.
+// A call made with HISA_FLAG_CHAINED launches its kernels with programmatic stream
+// serialization: the launch is prepared, and may start, while the previous kernel on the
+// stream runs. grid_dep_wait() waits until the previous grid has completed and its writes
+// are visible (without the attribute it returns at once: the kernel started after the
+// previous work completed). Most kernels execute it before their first global-memory
+// access. Two kinds of kernel let their successor start early, once all of their CTAs have
+// finished streaming (grid_dep_trigger): the coarse / fine scoring pipeline, whose fine
+// form reads q, w and the offsets before it waits and only the kept blocks (the coarse
+// output) after; and the combine, which waits before its first selected id (the fine
+// output) and first output write, after its first item's q and local rows are on their
+// way. The flag's contract (include/hisa.h) is that no such early-read input is written
+// by the kernel just before the call.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t s, Args... args) {
+                       cudaStream_t s, int chained, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -36,8 +41,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = chained ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// cudaFuncSetAttribute(Kernel, MaxDynamicSharedMemorySize, bytes), made once per device
+// (the attribute belongs to the device's context) and its result cached per device.
+// Concurrent first calls may both set it, which is harmless.
+template <auto Kernel>
+cudaError_t smem_attr_once(int bytes) {
+    static std::atomic<int> state[64];      // 0: not yet set; else 1 + the cudaError_t
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64)
+        return cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const int st = state[dev].load(std::memory_order_acquire);
+    if (st != 0) return (cudaError_t)(st - 1);
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    state[dev].store(1 + (int)e, std::memory_order_release);
+    return e;
 }
 
 
@@ -114,6 +137,7 @@ struct ScoreParams {
     int64_t keys_rows;        // rows allocated in the key array
     int64_t means_rows;       // rows allocated in the block-mean array (coarse)
     uint32_t *status;
+    int chained;              // launch as a programmatic dependent (HISA_FLAG_CHAINED)
 };
 
 struct SelectParams {
@@ -146,6 +170,7 @@ struct MeansParams {
     int64_t keys_rows;
     int64_t means_rows;
     uint32_t *status;
+    int chained;              // launch as a programmatic dependent (HISA_FLAG_CHAINED)
 };
 
 struct AttnParams {
@@ -169,6 +194,29 @@ struct AttnParams {
     int rows_per_split;       // multiple of the chunk size
     int kv_bf16;
     uint32_t *status;
+    int chained;              // launch as a programmatic dependent (HISA_FLAG_CHAINED)
+};
+
+struct CompressParams {
+    int B, D, C, r, overlap, rope_dims, b;
+    int n_new_max;
+    int k_bf16;
+    float eps;
+    double log_theta;         // ln(rope theta)
+    const float *kv;          // [tok_rows, C] wkv(x)
+    const float *gate;        // [tok_rows, C] wgate(x)
+    const float *ape;         // [r, C]
+    const float *norm_w;      // [D]
+    const int64_t *tok_off;   // [B+1]
+    const int32_t *p_first;   // [B]
+    const int32_t *n_new;     // [B]
+    void *keys;               // [keys_rows, D] out
+    const int64_t *key_off;   // [B+1]
+    float *means;             // [means_rows, D] out, or nullptr
+    const int64_t *means_off; // [B+1]
+    int64_t tok_rows, keys_rows, means_rows;
+    uint32_t *status;
+    int chained;
 };
 
 // Tensor-core scoring (H_i = 64, D_i = 128): `s` describes the rows and inputs; the
@@ -218,6 +266,8 @@ cudaError_t launch_score_pipe(const ScoreTcParams &p, cudaStream_t s);
 int score_pipe_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b, int keep);
 // Dense scoring of many query rows per sequence (batched prefill): flat scores to p.out.
 cudaError_t launch_score_gemm(const ScoreParams &p, cudaStream_t s);
+// The indexer compressor: new pooled rows and the block means they complete.
+cudaError_t launch_compress(const CompressParams &p, cudaStream_t s);
 int score_gemm_supported(int H_i, int D_i, int q_bf16, int rows_bf16, int B, int L);
 
 }  // namespace hisa

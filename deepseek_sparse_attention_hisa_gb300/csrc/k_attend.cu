@@ -265,8 +265,7 @@ cudaError_t launch_attend_combine(const AttnParams &p, cudaStream_t s) {
 template <int H, int DH, typename T>
 static cudaError_t launch_attend_t(const AttnParams &p, cudaStream_t s) {
     using S = AttnSmem<H, DH, T>;
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        k_attend_simt<H, DH, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
+    const cudaError_t attr = smem_attr_once<k_attend_simt<H, DH, T>>((int)S::bytes);
     if (attr != cudaSuccess) return attr;
     dim3 grid((unsigned)(p.B * p.L), (unsigned)p.nsplit);
     k_attend_simt<H, DH, T><<<grid, kAttnThreads, S::bytes, s>>>(p);

@@ -5,7 +5,7 @@
 // A work item is a range of one query row's attended-row list (the visible local window
 // rows, then the gathered pooled rows). One CTA per SM walks the items blockIdx.x,
 // blockIdx.x + gridDim.x, ...; the list tiles of consecutive items stream through the
-// same four slots, so an item's start (q, first tiles) and end (the epilogue) overlap its
+// same kSlots = 5 ring slots, so an item's start (q, first tiles) and end (the epilogue) overlap its
 // neighbours' streaming. The list streams in tiles of kTR = 32 rows; per tile:
 //   S  = Q . K^T      tcgen05, M = 64 heads, N = kTR rows, K = 512   (TMEM, 2 buffers)
 //   P  = exp2(S * scale*log2e - m) per head, in the thread that owns the head's TMEM lane
@@ -667,8 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
 int attend_tc_supported(int H, int Dh, int kv_bf16) { return H == kH && Dh == kDH && kv_bf16; }
 
 cudaError_t launch_attend_tc(const AttnParams &p, cudaStream_t s) {
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        k_attend_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    const cudaError_t attr = smem_attr_once<k_attend_tc>((int)kSmemBytes);
     if (attr != cudaSuccess) return attr;
     // persistent: one CTA per SM walks the items (query row, split)
     int dev = 0;
@@ -679,7 +678,7 @@ cudaError_t launch_attend_tc(const AttnParams &p, cudaStream_t s) {
     const int64_t items = (int64_t)p.B * p.L * p.nsplit;
     if (items == 0) return cudaSuccess;
     dim3 grid((unsigned)(items < nsm ? items : nsm));
-    cudaError_t e = launch_pdl(k_attend_tc, grid, dim3(kThreads), kSmemBytes, s, p);
+    cudaError_t e = launch_pdl(k_attend_tc, grid, dim3(kThreads), kSmemBytes, s, p.chained, p);
     if (e != cudaSuccess || p.nsplit == 1) return e;
     return launch_attend_combine(p, s);
 }

@@ -133,8 +133,7 @@ __global__ void __launch_bounds__(256) k_scores_simt(ScoreParams p) {
 template <int D, typename QT, typename KT>
 static cudaError_t launch_scores_t(const ScoreParams &p, cudaStream_t s) {
     const size_t smem = (size_t)p.H_i * D * 4 + (size_t)p.H_i * 4 + 64 * 4;
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        k_scores_simt<D, QT, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 128 * 4 + 1024);
+    const cudaError_t attr = smem_attr_once<k_scores_simt<D, QT, KT>>(128 * 128 * 4 + 1024);
     if (attr != cudaSuccess) return attr;
     const int64_t tiles = (p.n_max + 255) / 256;
     if (tiles == 0) return cudaSuccess;
@@ -279,8 +278,9 @@ cudaError_t launch_block_means(const MeansParams &p, int64_t nb_max, cudaStream_
     dim3 grid(gx, (unsigned)p.B);
     if ((int64_t)p.b * p.D_i <= kMeansStage) {
         if (p.keys_bf16)
-            return launch_pdl(k_block_means_staged<__nv_bfloat16>, grid, dim3(kMeansThreads), 0, s, p);
-        return launch_pdl(k_block_means_staged<float>, grid, dim3(kMeansThreads), 0, s, p);
+            return launch_pdl(k_block_means_staged<__nv_bfloat16>, grid, dim3(kMeansThreads), 0, s, p.chained,
+                              p);
+        return launch_pdl(k_block_means_staged<float>, grid, dim3(kMeansThreads), 0, s, p.chained, p);
     }
     const int threads = p.D_i;
     if (p.keys_bf16)

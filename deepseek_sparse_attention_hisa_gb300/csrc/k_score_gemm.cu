@@ -314,13 +314,12 @@ cudaError_t launch_score_gemm(const ScoreParams &s, cudaStream_t stream) {
     if (!encode_map_rows(&P.keys_map, s.rows, (uint64_t)s.keys_rows, kM) ||
         !encode_map_rows(&P.q_map, s.q, (uint64_t)s.B * s.L * kH, kN))
         return cudaErrorInvalidValue;
-    static const cudaError_t attr =
-        cudaFuncSetAttribute(k_score_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    const cudaError_t attr = smem_attr_once<k_score_gemm>((int)kSmem);
     if (attr != cudaSuccess) return attr;
     const int sms = sm_count_gemm();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = units < sms ? (int)units : sms;
-    return launch_pdl(k_score_gemm, dim3(grid), dim3(kThreads), kSmem, stream, P);
+    return launch_pdl(k_score_gemm, dim3(grid), dim3(kThreads), kSmem, stream, s.chained, P);
 }
 
 }  // namespace hisa

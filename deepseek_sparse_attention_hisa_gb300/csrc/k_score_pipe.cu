@@ -612,16 +612,16 @@ int sm_count() {
 template <int MODE, bool QBF16>
 cudaError_t launch_pipe_t(const ScoreTcParams &p, cudaStream_t s) {
     constexpr int cap = MODE == kCoarse ? kPipeMaxCoarse : kPipeMaxFine;
-    static const cudaError_t attr =
-        cudaFuncSetAttribute(k_score_pipe<MODE, QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(Layout<MODE>::fixed + 2 * cap * 4));
+    const cudaError_t attr =
+        smem_attr_once<k_score_pipe<MODE, QBF16>>((int)(Layout<MODE>::fixed + 2 * cap * 4));
     if (attr != cudaSuccess) return attr;
     const int rows = p.s.B * p.s.L;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = rows < sms ? rows : sms;
     const size_t smem = Layout<MODE>::fixed + 2 * (size_t)p.s.n_max * 4;
-    return launch_pdl(k_score_pipe<MODE, QBF16>, dim3(grid), dim3(pipe_threads<MODE>()), smem, s, p);
+    return launch_pdl(k_score_pipe<MODE, QBF16>, dim3(grid), dim3(pipe_threads<MODE>()), smem, s,
+                      p.s.chained, p);
 }
 
 }  // namespace

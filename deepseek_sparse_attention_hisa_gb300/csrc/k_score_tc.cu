@@ -443,9 +443,7 @@ int score_tc_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max,
 
 template <int MODE, bool QBF16>
 static cudaError_t launch_t(const ScoreTcParams &p, dim3 grid, cudaStream_t s) {
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        k_score_tc<MODE, QBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        (int)(kSmemFixed + kMaxSel * 4));
+    const cudaError_t attr = smem_attr_once<k_score_tc<MODE, QBF16>>((int)(kSmemFixed + kMaxSel * 4));
     if (attr != cudaSuccess) return attr;
     // the fused select keeps n scores in shared memory; split launches keep none
     const size_t smem = kSmemFixed + (p.tiles_per_cta > 0 ? 0 : (size_t)p.s.n_max * 4);

@@ -167,10 +167,8 @@ cudaError_t launch_select(const SelectParams &p, int64_t n_max, cudaStream_t s) 
     if (p.mode == kFlat && p.work && chunked_select_fits(p.ld, p.k) && n_max > kSmemSel) {
         const int64_t nchunk = (p.ld + kChunk - 1) / kChunk;
         const int cap = (int)chunked_candidates(p.ld, p.k);
-        static const cudaError_t a1 = cudaFuncSetAttribute(
-            k_select_chunks<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunk * 4);
-        static const cudaError_t a2 = cudaFuncSetAttribute(
-            k_select_merge<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMergeSmem);
+        const cudaError_t a1 = smem_attr_once<k_select_chunks<1024>>(kChunk * 4);
+        const cudaError_t a2 = smem_attr_once<k_select_merge<1024>>((int)kMergeSmem);
         if (a1 != cudaSuccess) return a1;
         if (a2 != cudaSuccess) return a2;
         k_select_chunks<1024><<<dim3(rows, (unsigned)nchunk), 1024, kChunk * 4, s>>>(p);
@@ -183,8 +181,7 @@ cudaError_t launch_select(const SelectParams &p, int64_t n_max, cudaStream_t s) 
     if (n_max <= 256) {
         k_select<256><<<rows, 256, smem, s>>>(q);
     } else {
-        static const cudaError_t a = cudaFuncSetAttribute(
-            k_select<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemSel * 4);
+        const cudaError_t a = smem_attr_once<k_select<1024>>(kSmemSel * 4);
         if (a != cudaSuccess) return a;
         k_select<1024><<<rows, 1024, smem, s>>>(q);
     }

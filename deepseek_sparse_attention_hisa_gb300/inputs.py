@@ -53,6 +53,9 @@ class Workload:
     local_prefix: int = 0        # cached local rows before t0 (prefill)
     plant_frac: float = 0.0
     with_attention: bool = True
+    kv_std: float | None = None  # local / pooled KV std (None: Dh^-1/2)
+    q_attn_std: float = 1.0      # attention q std
+    sink_mean: float = 0.0       # sinks ~ N(sink_mean, 1)
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -82,6 +85,15 @@ WORKLOADS = {
 }
 
 
+def peaked(wl: Workload) -> Workload:
+    """The same workload with attention inputs drawn so that a wrong combine is visible
+    at bf16 precision: KV ~ N(0, 1) (outputs of order one), q ~ N(0, 9) (logits of std 3,
+    so a few rows dominate each head's softmax) and sinks ~ N(9, 1), about the largest
+    logit of 640 rows, so each sink holds a sizeable share of its head's normaliser.
+    The indexer inputs are the same draws as the plain workload's."""
+    return wl.replace(kv_std=1.0, q_attn_std=3.0, sink_mean=9.0)
+
+
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round f32 to bf16 (nearest, ties to even); returns the uint16 bit patterns."""
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
@@ -89,7 +101,7 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
 
 
-def _normal(rng, shape, dtype: str, std: float = 1.0) -> np.ndarray:
+def _normal(rng, shape, dtype: str, std: float = 1.0, mean: float = 0.0) -> np.ndarray:
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16 if dtype == "bf16" else np.float32)
     s = np.float32(std)
@@ -98,6 +110,8 @@ def _normal(rng, shape, dtype: str, std: float = 1.0) -> np.ndarray:
         z = rng.standard_normal(hi - lo, dtype=np.float32)
         if std != 1.0:
             z *= s
+        if mean != 0.0:
+            z += np.float32(mean)
         out[lo:hi] = f32_to_bf16_bits(z) if dtype == "bf16" else z
     return out.reshape(shape)
 
@@ -147,8 +161,9 @@ def generate(wl: Workload | str, seed: int | None = None) -> dict:
     if wl.with_attention:
         W_rows = wl.window + (wl.L - 1) if wl.local_prefix == 0 else wl.local_prefix + wl.L
         W_rows = max(W_rows, 1)
-        out["q_attn"] = _normal(rng, (wl.B, wl.L, wl.H, wl.Dh), wl.kv_dtype)
-        out["local_kv"] = _normal(rng, (wl.B, W_rows, wl.Dh), wl.kv_dtype, std=wl.Dh ** -0.5)
+        kv_std = wl.Dh ** -0.5 if wl.kv_std is None else wl.kv_std
+        out["q_attn"] = _normal(rng, (wl.B, wl.L, wl.H, wl.Dh), wl.kv_dtype, std=wl.q_attn_std)
+        out["local_kv"] = _normal(rng, (wl.B, W_rows, wl.Dh), wl.kv_dtype, std=kv_std)
         if wl.local_prefix:
             pos0 = t0.astype(np.int64) - wl.local_prefix
         else:
@@ -156,8 +171,40 @@ def generate(wl: Workload | str, seed: int | None = None) -> dict:
             pos0 = t0.astype(np.int64) + (wl.L - 1) - (W_rows - 1)
         out["local_len"] = np.full(wl.B, W_rows, dtype=np.int32)
         out["local_pos0"] = pos0.astype(np.int32)
-        out["pooled_kv"] = _normal(rng, (total, wl.Dh), wl.kv_dtype, std=wl.Dh ** -0.5)
-        out["sinks"] = _normal(rng, (wl.H,), "f32")
+        out["pooled_kv"] = _normal(rng, (total, wl.Dh), wl.kv_dtype, std=kv_std)
+        out["sinks"] = _normal(rng, (wl.H,), "f32", mean=wl.sink_mean)
+    return out
+
+
+def compressor_inputs(seed: int, p_first, n_new, D: int = 128, r: int = 4, overlap: bool = True,
+                      key_dtype: str = "bf16", capacity=None) -> dict:
+    """Synthetic inputs of the indexer's compressor for B sequences ([HiSA issue]
+    "Configuration": compressor.{wkv, wgate, ape, norm}). The projections wkv(x), wgate(x)
+    stand for x ~ N(0, 1) through weights ~ N(0, 1 / hidden), so they are drawn directly as
+    N(0, 1) rows; ape ~ N(0, 1); norm weight ~ 1 + N(0, 0.1^2). Sequence b holds
+    (n_new[b] + 1) * r token rows (the window before its first new pooled row, then the new
+    rows' windows) and a pooled key cache of capacity[b] rows (default p_first + n_new),
+    whose rows below p_first[b] are drawn as earlier pooled keys ~ N(0, 1).
+    Draw order: kv, gate, ape, norm weight, earlier keys."""
+    rng = np.random.default_rng(seed)
+    p_first = np.asarray(p_first, dtype=np.int32)
+    n_new = np.asarray(n_new, dtype=np.int32)
+    B = len(p_first)
+    C = 2 * D if overlap else D
+    T = (n_new.astype(np.int64) + 1) * r
+    tok_off = np.zeros(B + 1, dtype=np.int64)
+    tok_off[1:] = np.cumsum(T)
+    cap = (p_first.astype(np.int64) + n_new) if capacity is None else np.asarray(capacity, np.int64)
+    key_off = np.zeros(B + 1, dtype=np.int64)
+    key_off[1:] = np.cumsum(cap)
+    out = dict(B=B, D=D, r=r, C=C, overlap=overlap, p_first=p_first, n_new=n_new,
+               tok_off=tok_off, key_off=key_off)
+    out["kv"] = _normal(rng, (int(tok_off[-1]), C), "f32")
+    out["gate"] = _normal(rng, (int(tok_off[-1]), C), "f32")
+    out["ape"] = _normal(rng, (r, C), "f32")
+    out["norm_w"] = _normal(rng, (D,), "f32", std=0.1, mean=1.0)
+    keys = _normal(rng, (int(key_off[-1]), D), key_dtype)
+    out["keys"] = keys
     return out
 
 
@@ -174,19 +221,26 @@ def generate_device(wl: Workload, device="cuda", seed: int | None = None) -> dic
     """Like generate(), but drawn on the device with torch's generator (for batches too
     large to draw on the host). Same shapes, distributions and layout; different random
     stream, so results are only comparable with the oracle on host copies of the draws.
-    Every sequence has wl.Np[0] pooled rows; returns torch tensors (bf16 as torch.bfloat16).
+    Every sequence has wl.Np[0] pooled rows, or, for a ragged workload (wl.Np None), the
+    per-sequence counts generate() draws (the same numpy draw, first from default_rng(seed));
+    returns torch tensors (bf16 as torch.bfloat16).
     """
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(wl.seed if seed is None else seed)
-    B, Np = wl.B, int(wl.Np[0])
-    npb = np.full(B, Np, dtype=np.int64)
+    B = wl.B
+    if wl.Np is None:
+        lo, hi = wl.Np_range
+        rng = np.random.default_rng(wl.seed if seed is None else seed)
+        npb = rng.integers(lo, hi, endpoint=True, size=B).astype(np.int64)
+    else:
+        npb = np.full(B, int(wl.Np[0]), dtype=np.int64)
     key_off = np.zeros(B + 1, dtype=np.int64)
     key_off[1:] = np.cumsum(npb)
     t0 = (wl.r * npb - 1).astype(np.int32) if wl.t0 is None else np.full(B, wl.t0, np.int32)
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16}
 
-    def normal(shape, dtype, std=1.0, rows_per_draw=None):
+    def normal(shape, dtype, std=1.0, rows_per_draw=None, mean=0.0):
         out = torch.empty(shape, dtype=tdt[dtype], device=device)
         flat = out.view(shape[0], -1)
         step = rows_per_draw or shape[0]
@@ -196,6 +250,8 @@ def generate_device(wl: Workload, device="cuda", seed: int | None = None) -> dic
                             dtype=torch.float32)
             if std != 1.0:
                 z *= std
+            if mean != 0.0:
+                z += mean
             flat[lo:hi] = z.to(tdt[dtype])
         return out
 
@@ -205,12 +261,17 @@ def generate_device(wl: Workload, device="cuda", seed: int | None = None) -> dic
     out["w"] = normal((B, wl.L, wl.H_i), "f32")
     out["keys"] = normal((total, wl.D_i), wl.key_dtype, rows_per_draw=1 << 20)
     if wl.with_attention:
-        W_rows = wl.window + (wl.L - 1)
-        out["q_attn"] = normal((B, wl.L, wl.H, wl.Dh), wl.kv_dtype)
-        out["local_kv"] = normal((B, W_rows, wl.Dh), wl.kv_dtype, std=wl.Dh ** -0.5)
+        W_rows = wl.window + (wl.L - 1) if wl.local_prefix == 0 else wl.local_prefix + wl.L
+        kv_std = wl.Dh ** -0.5 if wl.kv_std is None else wl.kv_std
+        out["q_attn"] = normal((B, wl.L, wl.H, wl.Dh), wl.kv_dtype, std=wl.q_attn_std)
+        out["local_kv"] = normal((B, W_rows, wl.Dh), wl.kv_dtype, std=kv_std)
         out["local_len"] = np.full(B, W_rows, dtype=np.int32)
-        out["local_pos0"] = (t0.astype(np.int64) + (wl.L - 1) - (W_rows - 1)).astype(np.int32)
-        out["pooled_kv"] = normal((total, wl.Dh), wl.kv_dtype, std=wl.Dh ** -0.5,
+        if wl.local_prefix:
+            pos0 = t0.astype(np.int64) - wl.local_prefix
+        else:
+            pos0 = t0.astype(np.int64) + (wl.L - 1) - (W_rows - 1)
+        out["local_pos0"] = pos0.astype(np.int32)
+        out["pooled_kv"] = normal((total, wl.Dh), wl.kv_dtype, std=kv_std,
                                   rows_per_draw=1 << 17)
-        out["sinks"] = normal((wl.H,), "f32")
+        out["sinks"] = normal((wl.H,), "f32", mean=wl.sink_mean)
     return out

@@ -85,6 +85,13 @@ class Problem:
             raise ValueError("descriptor rejected by hisa_workspace_bytes")
         self.ws_bytes = need
         self.ws = hb.alloc_workspace(need, dev)
+        # the same descriptors with HISA_FLAG_CHAINED: for calls that directly follow the
+        # previous libhisa call of the step on the stream
+        self.idesc_chained = hb.IndexDesc.from_buffer_copy(self.idesc)
+        self.idesc_chained.flags = hb.FLAG_CHAINED
+        if self.has_attention:
+            self.adesc_chained = hb.AttnDesc.from_buffer_copy(self.adesc)
+            self.adesc_chained.flags = hb.FLAG_CHAINED
 
     def io_clone(self):
         """A second set of the per-step buffers (query inputs, selections, output, workspace)
@@ -121,10 +128,11 @@ class Problem:
                                self.means_off, first_block, self.t0, self.top_blk, self.ws,
                                cscores, ld, stream)
 
-    def select_topk(self, fscores=None, top_blk=None, stream=None):
+    def select_topk(self, fscores=None, top_blk=None, stream=None, chained=False):
         tb = self.top_blk if top_blk is None else top_blk
-        hb.select_topk(self.idesc, self.q_idx, self.w, self.keys, self.key_off, self.t0, tb,
-                       self.I, self.ws, fscores, stream)
+        d = self.idesc_chained if chained else self.idesc
+        hb.select_topk(d, self.q_idx, self.w, self.keys, self.key_off, self.t0, tb, self.I,
+                       self.ws, fscores, stream)
 
     def flat_topk(self, I=None, stream=None):
         hb.flat_topk(self.idesc, self.q_idx, self.w, self.keys, self.key_off, self.t0,
@@ -134,21 +142,23 @@ class Problem:
         hb.index_scores(self.idesc, self.q_idx, self.w, self.keys, self.key_off, self.t0, scores,
                         scores.shape[1], self.ws, stream)
 
-    def attend(self, I="selected", out=None, stream=None):
+    def attend(self, I="selected", out=None, stream=None, chained=False):
         """I: 'selected' (self.I), None (dense branch over all pooled rows) or a tensor."""
         sel = self.I if isinstance(I, str) else I
-        hb.sparse_attend(self.adesc, self.q_attn, self.local_kv, self.local_len, self.local_pos0,
+        d = self.adesc_chained if chained else self.adesc
+        hb.sparse_attend(d, self.q_attn, self.local_kv, self.local_len, self.local_pos0,
                          self.pooled_kv, self.key_off, sel, self.sinks, self.t0,
                          self.out if out is None else out, self.ws, stream)
 
     def hisa_step(self, first_block=None, stream=None):
-        """The HiSA step: newest block means, coarse filter, fine top-k, sparse combine."""
+        """The HiSA step: newest block means, coarse filter, fine top-k, sparse combine; the
+        fine top-k and the combine are chained to the call before them."""
         if first_block is not None:
             self.block_means(first_block, stream)
         self.block_filter(stream=stream)
-        self.select_topk(stream=stream)
+        self.select_topk(stream=stream, chained=True)
         if self.has_attention:
-            self.attend(stream=stream)
+            self.attend(stream=stream, chained=True)
 
     def status(self, stream=None) -> int:
         return hb.device_status(self.ws, stream)

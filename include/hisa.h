@@ -13,14 +13,17 @@
  *    allocates, never frees, never synchronises the stream and keeps no state
  *    between calls; it is safe to call from several host threads on different
  *    streams with different workspaces.
- *  - Consecutive calls overlap: kernels are launched as programmatic dependents
- *    of the previous kernel on the stream. After hisa_block_filter(_append) or
- *    hisa_select_topk, the next call may start before that call has finished:
- *    hisa_select_topk then reads q, w, key_off and t0, and hisa_sparse_attend
- *    reads q, local_kv, local_len, local_pos0, kv_off, t0 and sinks early, and
- *    each waits before it reads the previous call's outputs (top_blk, I). So an
- *    input of a call must not be an output of the library call just before it
- *    on the same stream, other than top_blk / I as documented.
+ *  - Consecutive calls may overlap, on request: a call whose descriptor sets
+ *    HISA_FLAG_CHAINED launches its kernels as programmatic dependents of the
+ *    kernel before it on the stream, so it may start while that kernel finishes.
+ *    hisa_select_topk then reads q, w, key_off and t0, and hisa_sparse_attend reads
+ *    q, local_kv, local_len, local_pos0, kv_off, t0 and sinks before that kernel has
+ *    completed; each waits for it before reading top_blk / I and before writing any
+ *    output. Set the flag only when the kernel just before the call on the stream is
+ *    another libhisa call and none of those early-read inputs is written by it (the
+ *    usual chain: hisa_block_filter(_append) -> hisa_select_topk -> hisa_sparse_attend).
+ *    Without the flag (flags = 0) every kernel starts after the previous work on the
+ *    stream has completed, as with any ordinary launch.
  *  - Ragged batches: sequence b owns pooled rows [key_off[b], key_off[b+1]) of the
  *    packed key / KV arrays, so Np_b = key_off[b+1] - key_off[b] (int64, device).
  *  - Positions: t0[b] (int32, device) is the absolute token position of query
@@ -85,6 +88,9 @@ typedef enum { HISA_F32 = 0, HISA_BF16 = 1 } hisa_dtype;
 #define HISA_DEV_BAD_BLOCK   0x10u /* a top_blk entry outside [0, nb_b); that row is written as -1 */
 #define HISA_DEV_TIMEOUT     0x20u /* a kernel gave up on a bounded wait; its outputs are incomplete */
 
+/* Bits of hisa_index_desc.flags / hisa_attn_desc.flags (all others must be 0). */
+#define HISA_FLAG_CHAINED    0x1u /* may overlap the previous libhisa call on the stream (see above) */
+
 /* Operation ids for hisa_workspace_bytes. */
 #define HISA_OP_INDEX_SCORES  0
 #define HISA_OP_BLOCK_MEANS   1
@@ -92,6 +98,7 @@ typedef enum { HISA_F32 = 0, HISA_BF16 = 1 } hisa_dtype;
 #define HISA_OP_SELECT_TOPK   3
 #define HISA_OP_FLAT_TOPK     4
 #define HISA_OP_SPARSE_ATTEND 5
+#define HISA_OP_COMPRESS      6
 
 /* Indexer problem ([HiSA issue] "Configuration", "Flat selection", "HiSA decode path"). */
 typedef struct {
@@ -109,6 +116,7 @@ typedef struct {
                              write goes past it (0 for calls that take no means) */
     int32_t q_dtype;      /* hisa_dtype of q: HISA_F32 or HISA_BF16 */
     int32_t k_dtype;      /* hisa_dtype of the pooled indexer keys */
+    int32_t flags;        /* HISA_FLAG_* bits (0 = none) */
 } hisa_index_desc;
 
 /* Attention problem ([HiSA issue] "Consuming the selection: sparse combine"). */
@@ -125,10 +133,31 @@ typedef struct {
     float scale;          /* softmax scale; <= 0 selects Dh^-1/2 */
     int32_t q_dtype;      /* hisa_dtype of q; must equal kv_dtype */
     int32_t kv_dtype;     /* hisa_dtype of local_kv and pooled_kv */
+    int32_t flags;        /* HISA_FLAG_* bits (0 = none) */
 } hisa_attn_desc;
 
+/* The indexer's compressor ([HiSA issue] "The pooled stream and positions", "Configuration":
+ * compressor.{wkv, wgate, ape, norm}, compress_rope_theta, qk_rope_head_dim). */
+typedef struct {
+    int32_t B;            /* sequences (>= 1) */
+    int32_t D_i;          /* pooled key dim: 32, 64 or 128 */
+    int32_t r;            /* compress ratio: tokens per window (1..128) */
+    int32_t overlap;      /* 1: the overlap variant, projections 2*D_i wide (channels [0, D_i) pool
+                             the previous window, [D_i, 2*D_i) the row's own window); 0: plain, D_i wide */
+    int32_t rope_dims;    /* trailing dims rotated, even, 0..D_i (64) */
+    int32_t index_block;  /* b: block size of the block-mean cache (0: no means kept) */
+    int32_t n_new_max;    /* an upper bound of n_new[b] (0..1048576) */
+    int32_t k_dtype;      /* hisa_dtype of the pooled key cache */
+    float rope_theta;     /* RoPE base (> 1): compress_rope_theta = 160000 */
+    float eps;            /* RMSNorm epsilon (> 0) */
+    int64_t tok_rows;     /* rows allocated in kv and gate */
+    int64_t keys_rows;    /* rows allocated in keys; no key read or write goes past it */
+    int64_t means_rows;   /* rows allocated in means (0 when means is NULL) */
+    int32_t flags;        /* HISA_FLAG_* bits (0 = none) */
+} hisa_compress_desc;
+
 /* Bytes of device workspace `op` needs for `desc` (a hisa_index_desc* for ops 0-4,
- * a hisa_attn_desc* for op 5). Always >= 256 for a valid desc; 0 for an invalid one.
+ * a hisa_attn_desc* for op 5, a hisa_compress_desc* for op 6). Always >= 256 for a valid desc; 0 for an invalid one.
  * Pure host arithmetic: needs no GPU. */
 HISA_API size_t hisa_workspace_bytes(int32_t op, const void *desc);
 
@@ -241,6 +270,35 @@ HISA_API hisa_status hisa_flat_topk_noalloc(const hisa_index_desc *desc, const v
                                    const float *w, const void *keys, const int64_t *key_off,
                                    const int32_t *t0, int32_t *I, uint32_t *dev_status,
                                    hisa_stream_t stream);
+
+/* Indexer compressor ([HiSA issue] "The pooled stream and positions"): appends n_new[b]
+ * pooled rows p = p_first[b] .. p_first[b] + n_new[b] - 1 to sequence b's pooled key cache,
+ * each anchored at the token window [p r, p r + r - 1]: per output dim d, one softmax over
+ * the gate logits gate[t] + ape[t - window start] of the window's tokens (with the overlap
+ * variant also the previous window's, through their first D_i channels; row 0 has no
+ * previous window) weighs their kv values; then RMSNorm with norm_w and eps, then RoPE of
+ * the trailing rope_dims dims, pairs (2m, 2m+1), by the angle (p r) * rope_theta^(-2i /
+ * rope_dims) for the i-th rotated pair. Afterwards every block of index_block rows that
+ * the new rows complete gets its mean in `means`, with the bits hisa_block_means writes.
+ *   kv, gate   [tok_rows, C] f32: wkv(x) and wgate(x) of the tokens, C = 2*D_i (overlap) or
+ *              D_i. Sequence b's rows [tok_off[b], tok_off[b+1]) hold (n_new[b] + 1) * r
+ *              tokens: the window before row p_first[b] (ignored when p_first[b] == 0 or
+ *              without overlap), then the windows of the new rows, in token order.
+ *   tok_off    [B+1] int64;  p_first, n_new [B] int32 (n_new <= n_new_max; 0 = nothing)
+ *   ape        [r, C] f32;   norm_w [D_i] f32
+ *   keys       [keys_rows, D_i] k_dtype in/out: pooled row p of sequence b is row
+ *              key_off[b] + p; rows below p_first[b] are read for block means, and
+ *              key_off[b] + p_first[b] + n_new[b] must not pass key_off[b+1].
+ *   means      [means_rows, D_i] f32 out or NULL; block beta of sequence b at
+ *              means_off[b] + beta (means_off [B+1] int64 must leave room for every complete
+ *              block). NULL, or index_block == 0, keeps no means.
+ * Offsets or counts that do not fit set HISA_DEV_BAD_OFFSETS; that sequence is skipped. */
+HISA_API hisa_status hisa_compress_append(const hisa_compress_desc *desc, const float *kv,
+                                 const float *gate, const int64_t *tok_off,
+                                 const int32_t *p_first, const int32_t *n_new, const float *ape,
+                                 const float *norm_w, void *keys, const int64_t *key_off,
+                                 float *means, const int64_t *means_off, void *ws,
+                                 size_t ws_bytes, hisa_stream_t stream);
 
 /* Sparse combine ([HiSA issue] "Consuming the selection: sparse combine"): one softmax
  * over the visible local rows, the gathered pooled rows P = pooled_kv[I] and the

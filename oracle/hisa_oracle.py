@@ -6,8 +6,8 @@ library never uses it, and this module imports nothing from the CUDA side.
 
 Every function follows the page "feat(deepseek-v4): implement HiSA
 hierarchical sparse attention" (cited below as [HiSA issue], with its section)
-in the page's order and notation: q, w, pooled, rep, cs/cscore, top_blk, pos,
-cand, fs/fscore, sel, I, valid_len, NEG. Arithmetic is numpy float64; bf16
+in the page's order and notation: q, w, pooled, rep, cscore, top_blk, pos,
+fscore, I, valid_len, NEG. Arithmetic is numpy float64; bf16
 inputs arrive as uint16 bit patterns and are widened exactly. Top-k uses a full
 sort instead of argpartition.
 
@@ -58,6 +58,76 @@ def visible_len(t: int, r: int, Np: int) -> int:
 
 
 # ----------------------------------------------------------------------------
+# the indexer's compressor  ([HiSA issue] "The pooled stream and positions",
+# "Configuration": compressor.{wkv, wgate, ape, norm}, compress_rope_theta,
+# qk_rope_head_dim)
+# ----------------------------------------------------------------------------
+ROPE_THETA = 160000.0
+RMS_EPS = 1e-6
+
+
+def rms_norm(x, weight, eps: float = RMS_EPS) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * weight over the last axis."""
+    x = to_f64(x)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * to_f64(weight)
+
+
+def rope_interleaved(x, pos, theta: float = ROPE_THETA, rope_dims: int = 64) -> np.ndarray:
+    """Rotate the last rope_dims dims of x (pairs (2m, 2m+1)) by the angles pos * f_i,
+    f_i = theta^(-2i / rope_dims) for the i-th rotated pair; the leading dims pass
+    through. x: (..., D); pos: an integer or an array broadcastable to x[..., 0]."""
+    x = to_f64(x).copy()
+    D = x.shape[-1]
+    first = (D - rope_dims) // 2                 # index of the first rotated pair
+    pos = np.asarray(pos, dtype=np.float64)[..., None]
+    for i in range(rope_dims // 2):
+        m = first + i
+        ang = pos[..., 0] * theta ** (-2.0 * i / rope_dims)
+        c, s = np.cos(ang), np.sin(ang)
+        a, b = x[..., 2 * m].copy(), x[..., 2 * m + 1].copy()
+        x[..., 2 * m] = a * c - b * s
+        x[..., 2 * m + 1] = a * s + b * c
+    return x
+
+
+def compress_rows(kv, gate, ape, norm_w, p_rows, r: int, tok0: int = 0, overlap: bool = True,
+                  theta: float = ROPE_THETA, rope_dims: int = 64, eps: float = RMS_EPS):
+    """Pooled indexer keys p in p_rows from the projected token rows of one sequence.
+
+    kv, gate: (T, 2 D) = wkv(x), wgate(x) of tokens tok0 .. tok0 + T - 1 (absolute
+    positions). ape: (r, 2 D), added to the gate logit of the token at offset i of its
+    window. Pooled row p is anchored at the window [p r, p r + r - 1]; with the overlap
+    variant it also draws on the previous window [(p - 1) r, p r - 1]: channels D .. 2D - 1
+    of the current window's tokens and channels 0 .. D - 1 of the previous window's
+    tokens, all 2r of them weighted by one softmax over their gate logits per output dim
+    (p = 0 has no previous window: r entries). Without overlap (2 D = the head dim) a
+    softmax over the current window's r tokens per dim. Then RMSNorm with norm_w and the
+    interleaved RoPE of the last rope_dims dims at position p r. Returns (len(p_rows), D).
+    """
+    kv, gate, ape = to_f64(kv), to_f64(gate), to_f64(ape)
+    C = kv.shape[1]
+    D = C // 2 if overlap else C
+    out = np.zeros((len(p_rows), D))
+    for n, p in enumerate(p_rows):
+        vals, logits = [], []
+        if overlap and p > 0:
+            for i in range(r):
+                t = (p - 1) * r + i - tok0
+                vals.append(kv[t, :D])
+                logits.append(gate[t, :D] + ape[i, :D])
+        for i in range(r):
+            t = p * r + i - tok0
+            vals.append(kv[t, D:] if overlap else kv[t])
+            logits.append(gate[t, D:] + ape[i, D:] if overlap else gate[t] + ape[i])
+        vals, logits = np.array(vals), np.array(logits)          # (entries, D)
+        wts = np.exp(logits - logits.max(axis=0))
+        wts /= wts.sum(axis=0)
+        out[n] = (wts * vals).sum(axis=0)
+    out = rms_norm(out, norm_w, eps)
+    return rope_interleaved(out, np.asarray(p_rows) * r, theta, rope_dims)
+
+
+# ----------------------------------------------------------------------------
 # top-k  ([HiSA issue] "Conventions": argpartition returns an unordered set)
 # ----------------------------------------------------------------------------
 def top_k(score: np.ndarray, k: int, ids: np.ndarray | None = None) -> np.ndarray:
@@ -92,18 +162,6 @@ def combined_scores(q: np.ndarray, w: np.ndarray, rows: np.ndarray) -> np.ndarra
     H_i, D_i = q.shape
     s = np.maximum(q @ rows.T, 0.0)            # (H_i, n): relu(sum_d q[h,d] * row[p,d])
     return (w * head_scale(H_i, D_i)) @ s      # sum over h
-
-
-def error_scale(q: np.ndarray, w: np.ndarray, rows: np.ndarray) -> np.ndarray:
-    """A[p] = sum_h |w_h * scale| * sum_d |q_hd * rows_pd|: the magnitude of every
-    product that enters score[p], which is what an f32 evaluation of the two nested
-    sums is rounded against (a head's dot product can cancel to near zero while its
-    terms stay large). Used for tolerances only."""
-    q = to_f64(q)
-    w = to_f64(w)
-    rows = to_f64(rows)
-    H_i, D_i = q.shape
-    return np.abs(w * head_scale(H_i, D_i)) @ (np.abs(q) @ np.abs(rows).T)
 
 
 # ----------------------------------------------------------------------------
@@ -147,35 +205,34 @@ def block_means(pooled, b: int) -> np.ndarray:
 
 
 def hisa_coarse(q, w, rep, Kb: int, b: int, valid_len: int | None = None):
-    """Coarse stage for one query row: cscore over block means and the top Kb blocks.
+    """Coarse stage for one query row: block-level scores and the Kb best blocks.
 
-    With valid_len (batched path) a block is eligible iff its first row is
-    visible: cscore = NEG when beta * b >= valid_len.
-    Returns (cscore (nb,), top_blk (Kb,)).
+    Each block is scored through its mean row exactly as a pooled row is scored.
+    With valid_len (batched path) a block whose first pooled row is not visible
+    cannot be kept: its score is NEG. Returns (cscore (nb,), top_blk (Kb,)).
     """
     cscore = combined_scores(q, w, rep)
     if valid_len is not None:
-        first_row = np.arange(cscore.shape[0]) * b
-        cscore = np.where(first_row >= valid_len, NEG, cscore)
+        for beta in range(cscore.shape[0]):
+            if beta * b >= valid_len:
+                cscore[beta] = NEG
     return cscore, top_k(cscore, Kb)
 
 
 def hisa_fine(q, w, pooled, top_blk, b: int, k: int, valid_len: int | None = None):
-    """Fine stage for one query row: candidate table, exact rescoring, top k.
+    """Fine stage for one query row: every pooled row of the kept blocks is scored
+    again exactly, and the k best rows are kept.
 
-    pos[c] = top_blk[c // b] * b + c % b; cand = pooled[pos]; with valid_len the
-    candidates at pos >= valid_len are NEG. Returns (pos (C,), fscore (C,), I (k,)).
+    The candidates are the b rows of each kept block, block after block in the
+    order given. With valid_len, candidates at or past valid_len score NEG.
+    Returns (pos (C,) candidate pooled ids, fscore (C,), I (k,) selected ids).
     """
-    top_blk = np.asarray(top_blk, dtype=np.int64)
-    C = top_blk.shape[0] * b
-    c = np.arange(C)
-    pos = top_blk[c // b] * b + (c % b)
-    cand = np.asarray(pooled)[pos]
-    fscore = combined_scores(q, w, cand)
+    blocks = [int(beta) for beta in np.asarray(top_blk).ravel()]
+    pos = np.array([beta * b + i for beta in blocks for i in range(b)], dtype=np.int64)
+    fscore = combined_scores(q, w, np.asarray(pooled)[pos]) if pos.size else np.zeros(0)
     if valid_len is not None:
-        fscore = np.where(pos >= valid_len, NEG, fscore)
-    sel_ids = top_k(fscore, k, ids=pos)  # sel mapped through pos: I = pos[sel]
-    return pos, fscore, sel_ids
+        fscore[pos >= valid_len] = NEG
+    return pos, fscore, top_k(fscore, k, ids=pos)
 
 
 def hisa_select_decode(q, w, pooled, b: int, keep: int, index_topk: int, rep=None) -> dict:
@@ -266,13 +323,17 @@ def _logaddexp(a: np.ndarray, b: np.ndarray) -> np.ndarray:
 
 def sparse_combine(q_rows, local_kv, local_pos0: int, pooled_kv, I, sinks, t0: int, r: int,
                    window: int, scale: float | None = None, causal: bool | None = None,
-                   return_lse: bool = False):
+                   return_lse: bool = False, magnitude: bool = False):
     """One split softmax over the local stream, the gathered pooled rows and the sink.
 
     q_rows: (L, H, Dh), already roped. local_kv: (W, Dh), row i at absolute
     position local_pos0 + i. pooled_kv: (Np, Dh); K = V in both streams.
     I: (L, k) pooled ids or None for the dense branch (all Np rows). sinks: (H,).
     Returns out (L, H, Dh) [and the normaliser n (L, H)].
+
+    magnitude=True returns instead E = sum_j weight_j * |v_j| (the same softmax
+    weights applied to the absolute values): the scale against which a rounding
+    of the weights perturbs each output element (used for tolerances only).
     """
     q_rows = to_f64(q_rows)
     local_kv = to_f64(local_kv)
@@ -313,7 +374,10 @@ def sparse_combine(q_rows, local_kv, local_pos0: int, pooled_kv, I, sinks, t0: i
             w_pooled = np.exp(pooled_scores - n[:, None])
         w_local = np.where(np.isfinite(local_scores), w_local, 0.0)
         w_pooled = np.where(np.isfinite(pooled_scores), w_pooled, 0.0)
-        out[j] = w_local @ local_kv + w_pooled @ P                 # the sink adds no value
+        if magnitude:
+            out[j] = w_local @ np.abs(local_kv) + w_pooled @ np.abs(P)
+        else:
+            out[j] = w_local @ local_kv + w_pooled @ P             # the sink adds no value
         lse[j] = n
     return (out, lse) if return_lse else out
 

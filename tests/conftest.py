@@ -8,3 +8,14 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libhisa.so")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The worst error ratios of every parity check run (oracle/parity.py STATS)."""
+    try:
+        from oracle import parity
+    except Exception:
+        return
+    if parity.STATS:
+        terminalreporter.write_sep("-", "parity figures (worst per test)")
+        terminalreporter.write_line(parity.format_stats())

@@ -80,12 +80,18 @@ def test_struct_layout_matches_c():
 #include <stddef.h>
 #include "hisa.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(hisa_index_desc), offsetof(hisa_index_desc, Np_max),
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(hisa_index_desc), offsetof(hisa_index_desc, Np_max),
          offsetof(hisa_index_desc, keys_rows), offsetof(hisa_index_desc, means_rows),
-         offsetof(hisa_index_desc, q_dtype), offsetof(hisa_index_desc, k_dtype));
-  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(hisa_attn_desc), offsetof(hisa_attn_desc, Np_max),
+         offsetof(hisa_index_desc, q_dtype), offsetof(hisa_index_desc, k_dtype),
+         offsetof(hisa_index_desc, flags));
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(hisa_attn_desc), offsetof(hisa_attn_desc, Np_max),
          offsetof(hisa_attn_desc, kv_rows), offsetof(hisa_attn_desc, scale),
-         offsetof(hisa_attn_desc, q_dtype), offsetof(hisa_attn_desc, kv_dtype));
+         offsetof(hisa_attn_desc, q_dtype), offsetof(hisa_attn_desc, kv_dtype),
+         offsetof(hisa_attn_desc, flags));
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(hisa_compress_desc),
+         offsetof(hisa_compress_desc, rope_theta), offsetof(hisa_compress_desc, eps),
+         offsetof(hisa_compress_desc, tok_rows), offsetof(hisa_compress_desc, keys_rows),
+         offsetof(hisa_compress_desc, means_rows), offsetof(hisa_compress_desc, flags));
   return 0;
 }
 """
@@ -97,11 +103,16 @@ int main(void) {
         lines = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
     i = [int(x) for x in lines[0].split()]
     a = [int(x) for x in lines[1].split()]
+    c = [int(x) for x in lines[2].split()]
+    C = hb.CompressDesc
+    assert c == [ctypes.sizeof(C), C.rope_theta.offset, C.eps.offset, C.tok_rows.offset,
+                 C.keys_rows.offset, C.means_rows.offset, C.flags.offset]
     assert i == [ctypes.sizeof(hb.IndexDesc), hb.IndexDesc.Np_max.offset,
                  hb.IndexDesc.keys_rows.offset, hb.IndexDesc.means_rows.offset,
-                 hb.IndexDesc.q_dtype.offset, hb.IndexDesc.k_dtype.offset]
+                 hb.IndexDesc.q_dtype.offset, hb.IndexDesc.k_dtype.offset, hb.IndexDesc.flags.offset]
     assert a == [ctypes.sizeof(hb.AttnDesc), hb.AttnDesc.Np_max.offset, hb.AttnDesc.kv_rows.offset,
-                 hb.AttnDesc.scale.offset, hb.AttnDesc.q_dtype.offset, hb.AttnDesc.kv_dtype.offset]
+                 hb.AttnDesc.scale.offset, hb.AttnDesc.q_dtype.offset, hb.AttnDesc.kv_dtype.offset,
+                 hb.AttnDesc.flags.offset]
 
 
 def v4_index_desc(**kw):
@@ -173,9 +184,53 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.hisa_sparse_attend(ctypes.byref(a), *args) == hb.HISA_EDTYPE
     a = v4_attn_desc(k=0)
     assert lib.hisa_sparse_attend(ctypes.byref(a), *args) == hb.HISA_EINVAL
+    # flag bits other than HISA_FLAG_CHAINED
+    a = v4_attn_desc(flags=0x2)
+    assert lib.hisa_sparse_attend(ctypes.byref(a), *args) == hb.HISA_EINVAL
+    assert hb.workspace_bytes(hb.OP_SPARSE_ATTEND, v4_attn_desc(flags=hb.FLAG_CHAINED)) >= 256
+    g = v4_index_desc(flags=0x4)
+    assert lib.hisa_flat_topk(ctypes.byref(g), fake, fake, fake, fake, fake, fake, fake, 1 << 30,
+                              None) == hb.HISA_EINVAL
+    assert hb.workspace_bytes(hb.OP_FLAT_TOPK, v4_index_desc(flags=0x4)) == 0
     # status helpers
     assert lib.hisa_device_status(None, None, None) == hb.HISA_EINVAL
     assert lib.hisa_workspace_init(None, 0, None) == hb.HISA_EWORKSPACE
+
+
+def v4_compress_desc(**kw):
+    d = dict(B=2, D_i=128, r=4, overlap=1, rope_dims=64, index_block=64, n_new_max=16,
+             k_dtype=hb.HISA_BF16, rope_theta=160000.0, eps=1e-6, tok_rows=1 << 20,
+             keys_rows=1 << 20, means_rows=1 << 14)
+    d.update(kw)
+    return hb.CompressDesc(**d)
+
+
+def test_compress_host_validation(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    args = [fake] * 11 + [fake, 1 << 30, None]     # kv .. means_off, ws; ws_bytes; stream
+    assert hb.workspace_bytes(hb.OP_COMPRESS, v4_compress_desc()) == 256
+    for bad, code in ((dict(D_i=96), hb.HISA_EDTYPE), (dict(r=0), hb.HISA_EINVAL),
+                      (dict(rope_dims=65), hb.HISA_EINVAL), (dict(rope_dims=256), hb.HISA_EINVAL),
+                      (dict(overlap=2), hb.HISA_EINVAL), (dict(eps=0.0), hb.HISA_EINVAL),
+                      (dict(rope_theta=1.0), hb.HISA_EINVAL), (dict(n_new_max=-1), hb.HISA_EINVAL),
+                      (dict(flags=0x8), hb.HISA_EINVAL), (dict(k_dtype=7), hb.HISA_EDTYPE)):
+        d = v4_compress_desc(**bad)
+        assert lib.hisa_compress_append(ctypes.byref(d), *args) == code, bad
+        assert hb.workspace_bytes(hb.OP_COMPRESS, d) == 0, bad
+    d = v4_compress_desc()
+    assert lib.hisa_compress_append(ctypes.byref(d), None, *args[1:]) == hb.HISA_EINVAL
+    # means without their offsets
+    a2 = list(args)
+    a2[10] = None
+    assert lib.hisa_compress_append(ctypes.byref(d), *a2) == hb.HISA_EINVAL
+    # misaligned f32 input
+    a3 = list(args)
+    a3[0] = P((1 << 20) + 2)
+    assert lib.hisa_compress_append(ctypes.byref(d), *a3) == hb.HISA_EINVAL
+    a4 = list(args)
+    a4[11] = None
+    assert lib.hisa_compress_append(ctypes.byref(d), *a4) == hb.HISA_EWORKSPACE
 
 
 def test_status_strings(lib):
