@@ -79,6 +79,14 @@ hisa_status check_compress_desc(const hisa_compress_desc *d) {
 
 int64_t n_rows(const hisa_index_desc *d) { return (int64_t)d->B * d->L; }
 
+// The coarse stage of many bf16 query rows (batched prefill) runs as a dense contraction
+// over the block means split into bf16 planes (launch_coarse_gemm), then a select; fewer
+// or f32 rows take the per-row pipeline. Host arithmetic only (sizes the workspace).
+bool coarse_gemm_ok(const hisa_index_desc *d) {
+    return d->L >= 4 && n_rows(d) >= 256 && d->q_dtype == HISA_BF16 && d->means_rows > 0 &&
+           score_gemm_supported(d->H_i, d->D_i, 1, 1, d->B, d->L);
+}
+
 // Number of split-K ranges for the combine: enough CTAs to cover the GPU twice, never
 // fewer rows per split than one chunk. `list_len` bounds the attended rows per query.
 int pick_nsplit(int64_t queries, int64_t list_len, int64_t *rows_per_split) {
@@ -156,12 +164,13 @@ int device_sms() {
     return counts[dev];
 }
 
-// Few coarse / fine rows (a small batch, a single query, a long-context query): one CTA
-// per row would leave most SMs idle, so when the rows fill less than half of the SMs each
-// row's tiles are split over CTAs and a separate select follows.
+// A few long coarse / fine rows (a single long-context query): one CTA per row would leave
+// most SMs idle, so each row's tiles are split over CTAs and a separate select follows.
+// (Splitting shorter rows, or more of them, measured slower than one CTA per row: the
+// separate select and the scores' round trip cost more than the idle SMs.)
 bool split_rows(const hisa_index_desc *d, int mode, int64_t n) {
     const int sms = device_sms();
-    return sms > 0 && n >= 256 && n_rows(d) * 2 <= sms &&
+    return sms > 0 && n >= 2048 && n_rows(d) * 8 <= sms &&
            score_tc_split_ok(mode, d->H_i, d->D_i, mode == kFine ? d->k_dtype == HISA_BF16 : 0,
                              d->index_block);
 }
@@ -239,7 +248,8 @@ size_t hisa_workspace_bytes(int32_t op, const void *desc) {
         case HISA_OP_BLOCK_FILTER: {
             if (check_hisa_gate(d) != HISA_OK) return 0;
             const int64_t nb_max = d->Np_max / d->index_block;
-            return kStatusBytes + round_up((size_t)n_rows(d) * nb_max * sizeof(float));
+            return kStatusBytes + round_up((size_t)n_rows(d) * nb_max * sizeof(float)) +
+                   (coarse_gemm_ok(d) ? round_up(coarse_gemm_planes_bytes(d->means_rows)) : 0);
         }
         case HISA_OP_SELECT_TOPK: {
             if (check_hisa_gate(d) != HISA_OK) return 0;
@@ -325,15 +335,23 @@ hisa_status hisa_block_filter(const hisa_index_desc *d, const void *q, const flo
     if ((st = check_ws(ws, ws_bytes, hisa_workspace_bytes(HISA_OP_BLOCK_FILTER, d))) != HISA_OK)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool split = split_rows(d, kCoarse, nb_max);
-    const bool tc = !split && score_tc_supported(kCoarse, d->H_i, d->D_i, 0, nb_max, d->index_block);
+    const bool gemm = coarse_gemm_ok(d) && nb_max > 0;
+    const bool split = !gemm && split_rows(d, kCoarse, nb_max);
+    const bool tc = !gemm && !split && score_tc_supported(kCoarse, d->H_i, d->D_i, 0, nb_max, d->index_block);
     float *buf = cscores ? cscores : (tc ? nullptr : scratch_of(ws));
     const int64_t ld = cscores ? ld_cscores : (nb_max > 0 ? nb_max : 1);
     ScoreParams p = score_params(d, kCoarse, q, w, means, 0, key_off, t0, buf, ld, ws);
     p.means_off = means_off;
     p.n_max = nb_max;
     bool fused = false;
-    cudaError_t e = run_scores(p, top_blk, d->index_keep, &fused, s, split);
+    cudaError_t e;
+    if (gemm) {
+        void *planes = reinterpret_cast<char *>(ws) + kStatusBytes +
+                       round_up((size_t)n_rows(d) * nb_max * sizeof(float));
+        e = launch_coarse_gemm(p, planes, s);
+    } else {
+        e = run_scores(p, top_blk, d->index_keep, &fused, s, split);
+    }
     if (e != cudaSuccess) return HISA_ECUDA;
     if (fused) return HISA_OK;
     SelectParams sp{};

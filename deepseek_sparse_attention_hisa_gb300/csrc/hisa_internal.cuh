@@ -266,6 +266,11 @@ cudaError_t launch_score_pipe(const ScoreTcParams &p, cudaStream_t s);
 int score_pipe_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b, int keep);
 // Dense scoring of many query rows per sequence (batched prefill): flat scores to p.out.
 cudaError_t launch_score_gemm(const ScoreParams &p, cudaStream_t s);
+// Coarse scores of many bf16 query rows (batched prefill) as the same contraction over the
+// f32 block means (p.rows) split into three exact bf16 planes held in `planes`
+// (coarse_gemm_planes_bytes(p.means_rows) bytes); scores to p.out.
+cudaError_t launch_coarse_gemm(const ScoreParams &p, void *planes, cudaStream_t s);
+size_t coarse_gemm_planes_bytes(int64_t means_rows);
 // The indexer compressor: new pooled rows and the block means they complete.
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t s);
 int score_gemm_supported(int H_i, int D_i, int q_bf16, int rows_bf16, int B, int L);

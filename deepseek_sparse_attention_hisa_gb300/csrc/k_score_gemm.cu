@@ -16,6 +16,13 @@
 // four-slot ring), warps 2-9 form the epilogue (warp w reads TMEM lanes 32 (w % 4) ..
 // + 31, for rows 2 ((w - 2) / 4) and 2 ((w - 2) / 4) + 1). Key tiles past the visible
 // prefix of all four rows are not multiplied; their scores are written as NEG.
+//
+// The same kernel scores the coarse stage of many rows ([HiSA issue] "HiSA batched path":
+// cscore over the block means, NEG for a block whose first row is not visible) with the
+// f32 block means as the "keys": k_split_planes first splits each mean exactly into three
+// bf16 planes (x = x1 + x2 + x3, truncation), and every 128-block tile is three key tiles
+// (one per plane) whose products with the bf16 q accumulate in the same TMEM columns, so the
+// scores are f32 scoring of the f32 means.
 // Every wait is bounded; a timeout raises HISA_DEV_TIMEOUT, and the CTA drains and exits.
 #include "hisa_internal.cuh"
 #include "tc_ptx.cuh"
@@ -48,7 +55,9 @@ struct Misc {
 };
 
 struct GemmParams {
-    CUtensorMap keys_map;       // [keys_rows, 128] bf16, box 64 dims x 128 rows
+    CUtensorMap keys_map;       // [keys_rows, 128] bf16, box 64 dims x 128 rows (coarse: the
+                                // planes [3 * means_rows, 128], plane p of mean m at row
+                                // p * means_rows + m)
     CUtensorMap q_map;          // [B * L * 64, 128] bf16, box 64 dims x 256 rows
     ScoreParams s;
     int units_per_seq;          // ceil(L / 4)
@@ -76,28 +85,67 @@ __device__ __forceinline__ bool group_all(int id, int n, bool v) {
     return r != 0u;
 }
 
-// What every role derives for a unit from the offsets alone.
+// What every role derives for a unit from the offsets alone. Flat: the scored rows are the
+// sequence's pooled rows; coarse: its nb = floor(Np / b) block means.
 struct Unit {
     int b, j0, rows;            // sequence, first row, rows of the unit in the sequence (<= 4)
-    int64_t k0, Np;             // first pooled row, pooled rows
+    int64_t k0, Np;             // first scored row (pooled row / block-mean row), scored rows
+    int64_t Np_seq;             // pooled rows of the sequence
     int T, Tv;                  // key tiles, tiles that reach into the visible prefix
     bool ok;
 };
 
+// Scored rows visible to the query row at position t: pooled rows p < V(t) (flat), blocks
+// whose first row beta * b < V(t) (coarse).
+template <int NP>
+__device__ __forceinline__ int64_t visible_rows(const ScoreParams &p, int64_t t, int64_t Np, int64_t n) {
+    const int64_t V = p.causal ? visible_len(t, p.r, Np) : Np;
+    if (NP == 1) return V < n ? V : n;
+    const int64_t vb = (V + p.b - 1) / p.b;
+    return vb < n ? vb : n;
+}
+
+template <int NP>
 __device__ __forceinline__ Unit unit_of(const ScoreParams &p, int units_per_seq, int u) {
     Unit x;
     x.b = u / units_per_seq;
     x.j0 = (u - x.b * units_per_seq) * kRowsPerUnit;
     x.rows = p.L - x.j0 < kRowsPerUnit ? p.L - x.j0 : kRowsPerUnit;
     x.ok = seq_ok(p.key_off, x.b, p.Np_max, p.keys_rows);
-    x.k0 = x.ok ? p.key_off[x.b] : 0;
-    x.Np = x.ok ? p.key_off[x.b + 1] - x.k0 : 0;
+    x.Np_seq = x.ok ? p.key_off[x.b + 1] - p.key_off[x.b] : 0;
+    if (NP == 1) {
+        x.k0 = x.ok ? p.key_off[x.b] : 0;
+        x.Np = x.Np_seq;
+    } else {
+        const int64_t nb = x.Np_seq / p.b;
+        x.ok = x.ok && means_ok(p.means_off, x.b, nb, p.means_rows);
+        x.k0 = x.ok ? p.means_off[x.b] : 0;
+        x.Np = x.ok ? nb : 0;
+    }
     x.T = (int)((x.Np + kM - 1) / kM);
-    const int64_t Vl = p.causal ? visible_len((int64_t)p.t0[x.b] + x.j0 + x.rows - 1, p.r, x.Np) : x.Np;
+    const int64_t Vl = visible_rows<NP>(p, (int64_t)(x.ok ? p.t0[x.b] : 0) + x.j0 + x.rows - 1,
+                                        x.Np_seq, x.Np);
     x.Tv = (int)((Vl + kM - 1) / kM);
     return x;
 }
 
+// Three exact bf16 planes of each f32 block mean (truncation: x1 = the top 16 bits of x,
+// x2 = the top 16 bits of x - x1, x3 = x - x1 - x2, which has at most 8 significant bits).
+__global__ void k_split_planes(const float *means, int64_t n, __nv_bfloat16 *planes, int64_t plane_stride) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float x = means[i];
+        const float x1 = __uint_as_float(__float_as_uint(x) & 0xffff0000u);
+        const float r1 = x - x1;
+        const float x2 = __uint_as_float(__float_as_uint(r1) & 0xffff0000u);
+        const float x3 = r1 - x2;
+        planes[i] = __float2bfloat16_rz(x1);
+        planes[plane_stride + i] = __float2bfloat16_rz(x2);
+        planes[2 * plane_stride + i] = __float2bfloat16_rz(x3);
+    }
+}
+
+template <int NP>
 __global__ void __launch_bounds__(kThreads, 1) k_score_gemm(const __grid_constant__ GemmParams P) {
     const ScoreParams &p = P.s;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -142,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_gemm(const __grid_constan
             uint32_t g = 0;                                      // key tiles issued
             int i = 0;                                           // valid units so far
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const Unit x = unit_of(p, P.units_per_seq, u);
+                const Unit x = unit_of<NP>(p, P.units_per_seq, u);
                 if (!x.ok) {
                     if (x.j0 == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
                     continue;
@@ -154,11 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_gemm(const __grid_constan
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch)
                     tma_load_2d(sbase + kOffQ + ch * (kN * 128), &P.q_map, ch * 64, qy, &bars[kBarQFull]);
-                for (int t = 0; t < x.Tv; ++t, ++g) {
+                for (int t = 0; t < x.Tv * NP && ok; ++t, ++g) {   // coarse: plane t % 3 of tile t / 3
                     const uint32_t s = g % kSlots, use = g / kSlots;
                     if (use >= 1 && !wait_bar(&bars[kBarEmpty + s], (use - 1) & 1, abort)) { fail(); break; }
                     mbar_arrive_expect_tx(&bars[kBarFull + s], kKeyTile);
-                    const int32_t y = (int32_t)(x.k0 + (int64_t)t * kM);
+                    const int32_t y = (int32_t)((int64_t)(t % NP) * p.means_rows + x.k0 +
+                                                (int64_t)(t / NP) * kM);
 #pragma unroll
                     for (int ch = 0; ch < 2; ++ch)
                         tma_load_2d(sbase + kOffKeys + s * kKeyTile + ch * (kM * 128), &P.keys_map,
@@ -177,28 +226,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_gemm(const __grid_constan
         const uint64_t qd = smem_desc_sw128(sbase + kOffQ, 16, 1024);
         uint32_t g = 0;
         int i = 0;
+        uint32_t gs = 0;                                 // key slots consumed
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const Unit x = unit_of(p, P.units_per_seq, u);
+            const Unit x = unit_of<NP>(p, P.units_per_seq, u);
             if (!x.ok) continue;
             if (!wait_bar_warp(&bars[kBarQFull], i & 1, abort)) { fail(); break; }
             fence_after_sync();
             for (int t = 0; t < x.Tv; ++t, ++g) {
-                const uint32_t s = g % kSlots, ab = g & 1;
-                if ((g >= 2 && !wait_bar_warp(&bars[kBarAccEmpty + ab], ((g >> 1) - 1) & 1, abort)) ||
-                    !wait_bar_warp(&bars[kBarFull + s], (g / kSlots) & 1, abort)) {
+                const uint32_t ab = g & 1;
+                if (g >= 2 && !wait_bar_warp(&bars[kBarAccEmpty + ab], ((g >> 1) - 1) & 1, abort)) {
                     fail();
                     break;
                 }
-                fence_after_sync();
-                const uint64_t kd = smem_desc_sw128(sbase + kOffKeys + s * kKeyTile, 16, 1024);
                 const uint32_t d = tmem + ab * 256;
+                bool good = true;
+                for (int pl = 0; pl < NP; ++pl, ++gs) {          // the tile's planes, one slot each
+                    const uint32_t s = gs % kSlots;
+                    if (!wait_bar_warp(&bars[kBarFull + s], (gs / kSlots) & 1, abort)) { good = false; break; }
+                    fence_after_sync();
+                    const uint64_t kd = smem_desc_sw128(sbase + kOffKeys + s * kKeyTile, 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t ko = ks >> 2, kb = (ks & 3) * 32;
-                    mma_bf16_warp(d, desc_add(kd, ko * (kM * 128) + kb), desc_add(qd, ko * (kN * 128) + kb),
-                                  idesc, ks > 0 ? 1u : 0u);
+                    for (int ks = 0; ks < kD / 16; ++ks) {
+                        const uint32_t ko = ks >> 2, kb = (ks & 3) * 32;
+                        mma_bf16_warp(d, desc_add(kd, ko * (kM * 128) + kb), desc_add(qd, ko * (kN * 128) + kb),
+                                      idesc, (ks > 0 || pl > 0) ? 1u : 0u);
+                    }
+                    mma_commit_warp(&bars[kBarEmpty + s]);
                 }
-                mma_commit_warp(&bars[kBarEmpty + s]);
+                if (!good) { fail(); break; }
                 mma_commit_warp(&bars[kBarAccFull + ab]);
             }
             if (!ok) break;
@@ -216,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_gemm(const __grid_constan
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
             // every epilogue thread votes here, so that a timeout ends the loop for all of them
             if (!group_all(kBarEpi, kEpiThreads, ok)) { fail(); break; }
-            const Unit x = unit_of(p, P.units_per_seq, u);
+            const Unit x = unit_of<NP>(p, P.units_per_seq, u);
             if (!x.ok) continue;
             // weights of the unit's rows (w * H_i^-1/2 * D_i^-1/2), once the last unit is done
             {
@@ -231,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_gemm(const __grid_constan
             for (int rr = 0; rr < 2; ++rr) {
                 const int r = 2 * half + rr;
                 const int j = x.j0 + r;
-                V[rr] = r < x.rows ? (p.causal ? visible_len((int64_t)p.t0[x.b] + j, p.r, x.Np) : x.Np) : 0;
+                V[rr] = r < x.rows ? visible_rows<NP>(p, (int64_t)p.t0[x.b] + j, x.Np_seq, x.Np) : 0;
                 orow[rr] = r < x.rows ? p.out + ((int64_t)x.b * p.L + j) * p.ld_out : nullptr;
             }
             for (int t = 0; t < x.T; ++t) {
@@ -305,21 +360,43 @@ int score_gemm_supported(int H_i, int D_i, int q_bf16, int rows_bf16, int B, int
            (int64_t)B * L * kH < ((int64_t)1 << 31);
 }
 
-cudaError_t launch_score_gemm(const ScoreParams &s, cudaStream_t stream) {
+template <int NP>
+cudaError_t launch_gemm_t(const ScoreParams &s, const void *key_rows, uint64_t n_key_rows,
+                          cudaStream_t stream) {
     GemmParams P{};
     P.s = s;
     P.units_per_seq = (s.L + kRowsPerUnit - 1) / kRowsPerUnit;
     const int64_t units = (int64_t)s.B * P.units_per_seq;
-    if (units == 0 || s.keys_rows == 0) return cudaSuccess;
-    if (!encode_map_rows(&P.keys_map, s.rows, (uint64_t)s.keys_rows, kM) ||
+    if (units == 0 || n_key_rows == 0) return cudaSuccess;
+    if (!encode_map_rows(&P.keys_map, key_rows, n_key_rows, kM) ||
         !encode_map_rows(&P.q_map, s.q, (uint64_t)s.B * s.L * kH, kN))
         return cudaErrorInvalidValue;
-    const cudaError_t attr = smem_attr_once<k_score_gemm>((int)kSmem);
+    const cudaError_t attr = smem_attr_once<k_score_gemm<NP>>((int)kSmem);
     if (attr != cudaSuccess) return attr;
     const int sms = sm_count_gemm();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = units < sms ? (int)units : sms;
-    return launch_pdl(k_score_gemm, dim3(grid), dim3(kThreads), kSmem, stream, s.chained, P);
+    return launch_pdl(k_score_gemm<NP>, dim3(grid), dim3(kThreads), kSmem, stream, s.chained, P);
+}
+
+cudaError_t launch_score_gemm(const ScoreParams &s, cudaStream_t stream) {
+    if (s.keys_rows == 0) return cudaSuccess;
+    return launch_gemm_t<1>(s, s.rows, (uint64_t)s.keys_rows, stream);
+}
+
+size_t coarse_gemm_planes_bytes(int64_t means_rows) { return (size_t)means_rows * kD * 2 * 3; }
+
+cudaError_t launch_coarse_gemm(const ScoreParams &s, void *planes, cudaStream_t stream) {
+    if (s.means_rows == 0) return cudaSuccess;
+    const int64_t n = s.means_rows * kD;
+    const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    // the planes are this call's own scratch: nothing before the call writes them, and the
+    // means are read after the previous kernel (the block-mean append) has completed
+    cudaError_t e = launch_pdl(k_split_planes, dim3((unsigned)blocks), dim3(256), 0, stream, 0,
+                               static_cast<const float *>(s.rows), n,
+                               static_cast<__nv_bfloat16 *>(planes), n);
+    if (e != cudaSuccess) return e;
+    return launch_gemm_t<3>(s, planes, (uint64_t)(3 * s.means_rows), stream);
 }
 
 }  // namespace hisa

@@ -675,3 +675,21 @@ def test_inputs_written_by_the_kernel_just_before_a_call():
         for b in range(2):
             P.check_fine(mixed, b, 0, tb[b], I[b], None, 64, 512)
             P.check_attend(mixed, b, 0, out[b], I[b])
+
+
+def test_prefill_coarse_contraction_ragged_rows():
+    """The coarse stage of many bf16 query rows runs as one dense contraction over the block
+    means split into three bf16 planes: three sequences of 100 rows each (block counts 32, 78
+    and 17, none a multiple of the 128-block tile), rows whose visible prefix ends inside a
+    block, and rows that see fewer than keep eligible blocks. Coarse scores element by
+    element (f32 bound included) and the kept sets against the oracle, then the fine stage."""
+    L = 100
+    wl = inputs.small_workload(name="coarse_rows", seed=77, B=3, L=L, H_i=64, D_i=128,
+                               index_block=64, index_keep=16, index_topk=512, q_idx_dtype="bf16",
+                               key_dtype="bf16", Np=(2048, 5000, 1100), t0=0, with_attention=False)
+    data = inputs.generate(wl)
+    data["t0"][:] = np.array([4 * 2048 - 4 * L - 50, 4 * 5000 - 7000, 3780], dtype=np.int32)
+    prob = Problem(data)
+    res = run_hisa(prob)
+    rows = [(b, j) for b in range(3) for j in (0, 1, 2, 17, 50, 63, 64, 98, 99)]
+    check_rows(data, prob, res, rows)
