@@ -372,6 +372,10 @@ def run_gpu(args, wl, R):
     nb = int(prob.nb[0])
     newest = torch.as_tensor(np.full(R, nb - 1, dtype=np.int32), device=dev)
     prob.block_means()                               # cache of completed blocks
+    # a second, disjoint batch of R sequences: the headline alternates the two, so that
+    # a step's inputs were last touched two steps (2 x ~430 MB) earlier
+    prob_b = Problem(inputs.generate_device(bwl, device=dev, seed=1100 + rank), device=dev)
+    prob_b.block_means()
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=dev)
@@ -402,6 +406,17 @@ def run_gpu(args, wl, R):
     with torch.cuda.graph(g_step, stream=stream):
         for name in stages:
             calls[name](stream)
+    # headline graph: a step of batch A then a step of batch B, chained kernel to kernel
+    calls_b = calls_for(prob_b)
+    with torch.cuda.stream(stream):
+        for name in stages:
+            calls_b[name](stream)
+    stream.synchronize()
+    g_rot = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_rot, stream=stream):
+        for cl in (calls, calls_b):
+            for name in stages:
+                cl[name](stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     scrub = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     sink = torch.empty((), dtype=torch.float32, device=dev)
@@ -429,15 +444,16 @@ def run_gpu(args, wl, R):
             g_step.replay()
             flush_l2()
             step()
+        for _ in range((args.warmup + 1) // 2):
+            g_rot.replay()
     stream.synchronize()
-    assert prob.status(stream) == 0, "device status flags set during warm-up"
+    assert prob.status(stream) == 0 and prob_b.status(stream) == 0, \
+        "device status flags set during warm-up"
 
     K = args.steps
-    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K)]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
-    wo_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(K)]
+    # ---- headline: K steps back to back, batches A and B alternating (no flush: the step
+    # inputs, ~430 MB per batch, are over 3x the L2; each batch is reused every other step)
+    rot_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -445,7 +461,33 @@ def run_gpu(args, wl, R):
         clk.mark_start()
         t_wall = time.perf_counter()
         with torch.cuda.stream(stream):
-            for i in range(K):                      # headline: whole-step graph
+            rot_ev[0].record(stream)
+            for _ in range(K // 2):
+                g_rot.replay()
+            if K % 2:
+                g_step.replay()
+            rot_ev[1].record(stream)
+        stream.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        clk.mark_stop()
+    torch.cuda.synchronize()
+    rot_total_ms = max_over_ranks(rot_ev[0].elapsed_time(rot_ev[1]), dev)
+    assert prob.status(stream) == 0 and prob_b.status(stream) == 0, \
+        "device status flags set during the timed region"
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    wo_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(K)]
+    # ---- the same step with the L2 flushed before each one (timed one by one), per stage,
+    # and after a write-only flush
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk_f:
+        clk_f.mark_start()
+        with torch.cuda.stream(stream):
+            for i in range(K):                      # whole-step graph
                 flush_l2()                          # L2 flush outside the step's events
                 step_ev[i][0].record(stream)
                 g_step.replay()
@@ -459,16 +501,15 @@ def run_gpu(args, wl, R):
                 g_step.replay()
                 wo_ev[i][1].record(stream)
         stream.synchronize()
-        t_wall = time.perf_counter() - t_wall
-        clk.mark_stop()
+        clk_f.mark_stop()
     torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     wo_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in wo_ev), dev) / K
     stage_ms = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]
                 for j, name in enumerate(stages)}
-    total_ms = max_over_ranks(sum(step_ms), dev)
-    ms_per_step = total_ms / K
-    value = job_value(world, R, K, total_ms)
+    flushed_ms = max_over_ranks(sum(step_ms), dev) / K
+    ms_per_step = rot_total_ms / K
+    value = job_value(world, R, K, rot_total_ms)
 
     # e2e: the same step through the public API from pinned host buffers, with the
     # per-step query inputs copied in and the results (out, I) copied back.
@@ -512,9 +553,15 @@ def run_gpu(args, wl, R):
                                f"(Np={args.Np} each, H_i=64x128, b=64, keep=16, k=512, "
                                f"H=64x512 bf16, W=128)",
                    "R": R, "Np": int(args.Np),
-                   "l2": "L2 flush between steps: 256 MiB written, then 256 MiB read (no step "
-                         "input and no dirty flush line in L2 when a step starts); "
-                         f"{step_bytes * R / 1e6:.0f} MB touched per step"},
+                   "l2": "inputs larger than L2: K steps back to back alternating two disjoint "
+                         f"batches of R sequences ({step_bytes * R / 1e6:.0f} MB touched per step, "
+                         f"{2 * step_bytes * R / 1e6:.0f} MB between two uses of a batch, L2 129 MB); "
+                         "'flushed' has the same step timed one by one after an L2 flush"},
+        "flushed": {"ms_per_step": flushed_ms, "value": job_value(world, R, 1, flushed_ms),
+                    "step_hbm_gbs": step_bytes * R / (flushed_ms / 1e3) / 1e9,
+                    "how": "before each step (outside its events): 256 MiB written, then 256 MiB "
+                           "read, so no step input and no dirty flush line is in L2",
+                    "clocks": clk_f.summary()},
         "ms_per_step_after_write_only_flush": wo_ms,
         "step_hbm_gbs": step_bytes * R / (ms_per_step / 1e3) / 1e9,
         "step_bytes_per_query": step_bytes,
@@ -522,7 +569,8 @@ def run_gpu(args, wl, R):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic},
-        "gpu_launches": 3 * K * launches_per_step(prob),   # whole-step, per-stage, write-only passes
+        # headline, flushed whole-step, per-stage and write-only passes
+        "gpu_launches": 4 * K * launches_per_step(prob),
         "e2e": {"value": job_value(world, R, 1, e2e_ms), "unit": UNIT,
                 "serial_value": job_value(world, R, 1, e2e_serial_ms),
                 "how": "two buffer sets: step i's inputs copied in and step i-1's results copied "

@@ -656,6 +656,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
     if (!ok) flag(p.status, HISA_DEV_TIMEOUT);
     fence_before_sync();
     __syncthreads();
+    // this CTA is done: the next kernel may take over the SM once it exits (that kernel waits
+    // for this grid before it reads what this grid writes)
+    grid_dep_trigger();
     if (warp == kMmaWarp) {
         fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);

@@ -108,11 +108,11 @@ constexpr int kPipeMaxFine = 48 * 64;
 static_assert(kPipeMaxFine <= kSmallMax && kPipeMaxCoarse <= kSmallMax, "select capacity");
 
 // 227 KiB of shared memory per CTA: the layout, two score rows at capacity and the static
-// select state (kept blocks and SelectShared of the whole CTA)
+// select state (kept blocks and the select warps' SelectShared)
 template <int MODE>
 constexpr bool fits() {
     constexpr int cap = MODE == kCoarse ? kPipeMaxCoarse : kPipeMaxFine;
-    return Layout<MODE>::fixed + 2 * cap * 4 + sizeof(SelectShared<pipe_threads<MODE>()>) + 256 <=
+    return Layout<MODE>::fixed + 2 * cap * 4 + sizeof(SelectShared<kGroup>) + 256 <=
            227 * 1024;
 }
 static_assert(fits<kCoarse>() && fits<kFine>(), "shared memory");
@@ -122,6 +122,19 @@ static_assert(fits<kCoarse>() && fits<kFine>(), "shared memory");
 
 namespace hisa {
 namespace {
+
+// Candidate column -> absolute pooled id through the kept blocks (fine), or itself (coarse):
+// named types, so that every select of a stage shares one instantiation of the select code.
+struct FineIds {
+    const int *blk;
+    __device__ __forceinline__ int32_t operator()(int64_t c) const {
+        return (int32_t)(blk[(int)c >> 6] * 64 + ((int)c & 63));
+    }
+};
+struct SameIds {
+    __device__ __forceinline__ int32_t operator()(int64_t c) const { return (int32_t)c; }
+};
+
 
 // Registers: 14 (fine) or 22 (coarse) warps spread over the SM's four 16K-register
 // sub-partitions, so at most 128 or 88 registers per thread.
@@ -133,13 +146,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     using Lay = Layout<MODE>;
     const ScoreParams &p = P.s;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    constexpr int kAll = pipe_threads<MODE>();
-    // the select warps' state, and the whole CTA's for the last query (never both at once)
-    __shared__ union {
-        SelectShared<kGroup> group;
-        SelectShared<kAll> all;
-    } sel_u;
-    SelectShared<kGroup> &sel_sh = sel_u.group;
+    __shared__ SelectShared<kGroup> sel_sh;             // the select warps' state
     __shared__ int s_blk_raw[64];                       // kept blocks as read (fine)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -154,6 +161,23 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rows = p.B * p.L;
     const int nql = (int)blockIdx.x < rows ? (rows - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+
+    // The first query's q, weights and offsets into L2 while the barriers and TMEM are set
+    // up (a prefetch only warms L2, which every write reaches first, so it is safe whatever
+    // the previous kernel writes).
+    if (warp >= kWarpBld && warp < kWarpBld + 4 && nql > 0) {
+        const int bt = tid - kWarpBld * 32;
+        const int row = (int)blockIdx.x, bq = row / p.L;
+        const char *qrow = static_cast<const char *>(p.q) + (int64_t)row * kH * kD * (QBF16 ? 2 : 4);
+        for (int o = bt * 128; o < kH * kD * (QBF16 ? 2 : 4); o += kGroup * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + o));
+        if (bt < 2) asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(p.w + (int64_t)row * kH) + 128 * bt));
+        if (bt == 2) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.key_off + bq));
+        if (bt == 3) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.t0 + bq));
+        if (MODE == kCoarse && bt == 4) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.means_off + bq));
+        if (MODE == kCoarse && bt == 5 && P.first_block)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(P.first_block + bq));
+    }
 
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) {
@@ -479,9 +503,11 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
         }
     } else if (warp >= kWarpSel && warp < kWarpSel + 4) {
         // ---------------- select: top-k of a finished query, beside the next one's stream ----
-        // (fine: the last query is selected by the whole CTA below, once every role is done)
+        // The last query too: the select's code is then already in the SM's instruction cache
+        // (a first run of a code path after the caches were flushed stalls on instruction
+        // fetch; a CTA-wide select of the last query, a separate code path, took 4.7 us).
         const int st = tid - kWarpSel * 32;
-        for (int i = 0; i < nql - (MODE == kFine ? 1 : 0); ++i) {
+        for (int i = 0; i < nql; ++i) {
             const int qb = i & 1;
             const int row = (int)blockIdx.x + i * (int)gridDim.x;
             const bool w = wait_bar(&bars[kBarScFull + qb], (i >> 1) & 1, abort);
@@ -491,16 +517,12 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             int32_t *out = P.sel + (int64_t)row * P.k_sel;
             const int64_t kout = M.state ? 0 : (M.n < P.k_sel ? M.n : P.k_sel);
             if (kout > 0) {
-                if (MODE == kFine) {
-                    const int *blk = M.blk;
-                    small_topk<kGroup, kBarSel, kWarpSel * 32>(
-                        sc, M.n, (int)kout, out,
-                        [blk](int64_t c) { return (int32_t)(blk[(int)c >> 6] * 64 + ((int)c & 63)); },
-                        sel_sh, p.status);
-                } else {
-                    small_topk<kGroup, kBarSel, kWarpSel * 32>(
-                        sc, M.n, (int)kout, out, [](int64_t c) { return (int32_t)c; }, sel_sh, p.status);
-                }
+                if (MODE == kFine)
+                    small_topk<kGroup, kBarSel, kWarpSel * 32>(sc, M.n, (int)kout, out, FineIds{M.blk}, sel_sh,
+                                                              p.status);
+                else
+                    small_topk<kGroup, kBarSel, kWarpSel * 32>(sc, M.n, (int)kout, out, SameIds{}, sel_sh,
+                                                              p.status);
             }
             for (int64_t e = kout + st; e < P.k_sel; e += kGroup) out[e] = -1;
             named_sync(kBarSel, kGroup);
@@ -551,38 +573,12 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     if (!ok) flag(p.status, HISA_DEV_TIMEOUT);
     fence_before_sync();
     __syncthreads();
-    // every role of this CTA is done streaming: the next kernel may take over the SM once
-    // this CTA exits (it waits for this grid before it reads what this grid writes)
+    // every role of this CTA is done: the next kernel may take over the SM once this CTA
+    // exits (it waits for this grid before it reads what this grid writes)
     grid_dep_trigger();
     if (warp == kWarpMma) {
         fence_after_sync();
         tmem_dealloc(tmem, 512);
-    }
-    // ---------------- fine: the last query's top-k on every warp of the CTA ----------------
-    // Every role has left its loop, so the last query's scores are complete (or a wait
-    // gave up, and the row is written as -1). The coarse top-Kb is short and stays with
-    // the select warps, where it overlaps the other roles' tail.
-    if (MODE == kFine && nql > 0) {
-        const int i = nql - 1, qb = i & 1;
-        const int row = (int)blockIdx.x + i * (int)gridDim.x;
-        const QMeta &M = meta[qb];
-        const float *sc = scb + qb * n_cap;
-        int32_t *out = P.sel + (int64_t)row * P.k_sel;
-        const bool done = *abort == 0;
-        const int64_t kout = (M.state || !done) ? 0 : (M.n < P.k_sel ? M.n : P.k_sel);
-        if (kout > 0) {
-            if (MODE == kFine) {
-                const int *blk = M.blk;
-                small_topk<kAll, 0, 0>(
-                    sc, M.n, (int)kout, out,
-                    [blk](int64_t c) { return (int32_t)(blk[(int)c >> 6] * 64 + ((int)c & 63)); },
-                    sel_u.all, p.status);
-            } else {
-                small_topk<kAll, 0, 0>(sc, M.n, (int)kout, out, [](int64_t c) { return (int32_t)c; },
-                                       sel_u.all, p.status);
-            }
-        }
-        for (int64_t e = kout + tid; e < P.k_sel; e += kAll) out[e] = -1;
     }
 }
 
@@ -620,8 +616,11 @@ cudaError_t launch_pipe_t(const ScoreTcParams &p, cudaStream_t s) {
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = rows < sms ? rows : sms;
     const size_t smem = Layout<MODE>::fixed + 2 * (size_t)p.s.n_max * 4;
+    // the coarse form waits for the previous grid before its first global access (before it
+    // only warms L2 by prefetches), so it may always start while that grid ends
+    const int chained = MODE == kCoarse ? 1 : p.s.chained;
     return launch_pdl(k_score_pipe<MODE, QBF16>, dim3(grid), dim3(pipe_threads<MODE>()), smem, s,
-                      p.s.chained, p);
+                      chained, p);
 }
 
 }  // namespace
