@@ -228,6 +228,58 @@ def compress_append(desc, kv, gate, tok_off, p_first, n_new, ape, norm_w, keys, 
 
 
 # ----------------------------------------------------------------------------
+# page-locked host memory as a device-accessible output
+# ----------------------------------------------------------------------------
+_cudart = None
+
+
+def _runtime():
+    """The CUDA runtime library (the one torch loads, else the toolkit's)."""
+    global _cudart
+    if _cudart is None:
+        import glob
+        import torch
+        base = os.path.dirname(os.path.dirname(torch.__file__))
+        cands = glob.glob(os.path.join(base, "nvidia", "cu*", "lib", "libcudart.so*")) + \
+            glob.glob("/usr/local/cuda/lib64/libcudart.so*")
+        for c in cands:
+            try:
+                _cudart = ctypes.CDLL(c)
+                break
+            except OSError:
+                continue
+        if _cudart is None:
+            raise RuntimeError("no CUDA runtime library found")
+    return _cudart
+
+
+def device_pointer_of_pinned(t) -> int:
+    """The device address of a page-locked host tensor (torch's pin_memory), for a call that
+    should read or write host memory directly (on GB300 over NVLink-C2C). Under unified
+    addressing it is the host address itself; raises if the runtime does not map it."""
+    dptr = ctypes.c_void_p()
+    rc = _runtime().cudaHostGetDevicePointer(ctypes.byref(dptr), ctypes.c_void_p(t.data_ptr()),
+                                             ctypes.c_uint(0))
+    if rc != 0 or not dptr.value:
+        raise RuntimeError(f"cudaHostGetDevicePointer failed ({rc})")
+    return int(dptr.value)
+
+
+class DevicePointer:
+    """A raw device address passed where a tensor is expected (data_ptr() only)."""
+
+    def __init__(self, addr: int, numel: int = 0):
+        self.addr = int(addr)
+        self._numel = numel
+
+    def data_ptr(self) -> int:
+        return self.addr
+
+    def numel(self) -> int:
+        return self._numel
+
+
+# ----------------------------------------------------------------------------
 # host arrays -> device tensors (uint16 arrays are bf16 bit patterns)
 # ----------------------------------------------------------------------------
 def to_device(a, device="cuda"):

@@ -87,12 +87,14 @@ bool coarse_gemm_ok(const hisa_index_desc *d) {
            score_gemm_supported(d->H_i, d->D_i, 1, 1, d->B, d->L);
 }
 
-// Number of split-K ranges for the combine: enough CTAs to cover the GPU twice, never
-// fewer rows per split than one chunk. `list_len` bounds the attended rows per query.
+// Number of split-K ranges for the combine: about one item per SM (a split item re-reads its
+// row's q and writes a partial as large as the row's output, which the merge reads back, so
+// more splits than SMs cost more than they spread), never fewer rows per split than one chunk.
+// `list_len` bounds the attended rows per query. Host arithmetic only (sizes the workspace).
 int pick_nsplit(int64_t queries, int64_t list_len, int64_t *rows_per_split) {
     const int chunk = attend_chunk_rows();
     const int64_t chunks = (list_len + chunk - 1) / chunk;
-    int64_t ns = (kTargetCtas + queries - 1) / queries;
+    int64_t ns = kSmTarget / queries;
     if (ns > chunks) ns = chunks;
     if (ns < 1) ns = 1;
     if (ns > 64) ns = 64;
@@ -167,12 +169,27 @@ int device_sms() {
 // A few long coarse / fine rows (a single long-context query): one CTA per row would leave
 // most SMs idle, so each row's tiles are split over CTAs and a separate select follows.
 // (Splitting shorter rows, or more of them, measured slower than one CTA per row: the
-// separate select and the scores' round trip cost more than the idle SMs.)
+// separate select and the scores' round trip cost more than the idle SMs.) Coarse rows
+// longer than the persistent pipeline takes (over 4096 blocks, 1M+ tokens) are split
+// whatever their number.
 bool split_rows(const hisa_index_desc *d, int mode, int64_t n) {
     const int sms = device_sms();
-    return sms > 0 && n >= 2048 && n_rows(d) * 8 <= sms &&
+    const bool few_long = n >= 2048 && n_rows(d) * 8 <= sms;
+    const bool past_pipe = mode == kCoarse && n > (int64_t)kCoarseChunk * kCoarseMaxChunks;
+    return sms > 0 && (few_long || past_pipe) &&
            score_tc_split_ok(mode, d->H_i, d->D_i, mode == kFine ? d->k_dtype == HISA_BF16 : 0,
                              d->index_block);
+}
+
+// Coarse rows of more than kCoarseChunk blocks run in chunks whose (id, score) selections
+// go to `scratch` (the workspace's score area, which holds far more than the pairs).
+void set_coarse_chunks(ScoreTcParams *t, void *scratch) {
+    t->chunks = 1;
+    if (t->s.mode != kCoarse || t->s.n_max <= kCoarseChunk || !scratch) return;
+    const int64_t rows = (int64_t)t->s.B * t->s.L;
+    t->chunks = (int)((t->s.n_max + kCoarseChunk - 1) / kCoarseChunk);
+    t->chunk_ids = reinterpret_cast<int32_t *>(scratch);
+    t->chunk_sc = reinterpret_cast<float *>(t->chunk_ids + rows * t->chunks * t->k_sel);
 }
 
 // Runs one scoring pass: for the V4 indexer shape the persistent tcgen05 pipeline (coarse
@@ -180,7 +197,7 @@ bool split_rows(const hisa_index_desc *d, int mode, int64_t n) {
 // `sel` the tensor-core coarse / fine kernels also select (returns true in *fused); with
 // `split` the rows' tiles are spread over CTAs and the scores go to p.out.
 cudaError_t run_scores(const ScoreParams &p, int32_t *sel, int k_sel, bool *fused,
-                       cudaStream_t s, bool split = false) {
+                       cudaStream_t s, bool split = false, void *scratch = nullptr) {
     *fused = false;
     if (split) {
         ScoreTcParams t{};
@@ -194,6 +211,7 @@ cudaError_t run_scores(const ScoreParams &p, int32_t *sel, int k_sel, bool *fuse
         t.s = p;
         t.sel = sel;
         t.k_sel = k_sel;
+        set_coarse_chunks(&t, scratch);
         *fused = true;
         return launch_score_pipe(t, s);
     }
@@ -350,7 +368,7 @@ hisa_status hisa_block_filter(const hisa_index_desc *d, const void *q, const flo
                        round_up((size_t)n_rows(d) * nb_max * sizeof(float));
         e = launch_coarse_gemm(p, planes, s);
     } else {
-        e = run_scores(p, top_blk, d->index_keep, &fused, s, split);
+        e = run_scores(p, top_blk, d->index_keep, &fused, s, split, scratch_of(ws));
     }
     if (e != cudaSuccess) return HISA_ECUDA;
     if (fused) return HISA_OK;
@@ -398,6 +416,7 @@ hisa_status hisa_block_filter_append(const hisa_index_desc *d, const void *q, co
     t.k_sel = d->index_keep;
     t.append_keys = keys;
     t.first_block = first_block;
+    set_coarse_chunks(&t, scratch_of(ws));
     return from_cuda(launch_score_pipe(t, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -67,6 +67,7 @@ cudaError_t smem_attr_once(int bytes) {
 constexpr float kNeg = -1e30f;            // selection mask value ([HiSA issue] "Flat selection")
 constexpr size_t kStatusBytes = 256;      // status word region at the head of the workspace
 constexpr int kTargetCtas = 304;          // 2 CTAs per SM on a 152-SM GB300
+constexpr int kSmTarget = 152;            // one CTA per SM on a 152-SM GB300
 constexpr int kMaxTopk = 2048;
 
 enum ScoreMode : int { kFlat = 0, kCoarse = 1, kFine = 2 };
@@ -233,7 +234,15 @@ struct ScoreTcParams {
     int32_t *sel;
     int k_sel;
     int tiles_per_cta;        // flat: 128-row tiles per CTA (grid.y covers the row)
+    // coarse rows of more than kCoarseChunk blocks: each query row is scored as `chunks`
+    // chunks of kCoarseChunk blocks, each chunk's top-k_sel (id, score) pairs go to
+    // chunk_ids / chunk_sc [rows * chunks, k_sel], and a merge writes sel
+    int chunks;
+    int32_t *chunk_ids;
+    float *chunk_sc;
 };
+constexpr int kCoarseChunk = 1024;        // block means per chunk of a long coarse row
+constexpr int kCoarseMaxChunks = 4;
 
 // Encodes a 2-D bf16 tensor map over [rows, cols] (row-major) with a box of box_cols x
 // box_rows and the 128-byte swizzle. Returns false if the driver has no encoder or

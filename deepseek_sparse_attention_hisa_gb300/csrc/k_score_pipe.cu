@@ -52,9 +52,14 @@ constexpr uint32_t kOffQ = 0;                             // up to 3 planes, sta
 // two q buffers, so that the next query's planes are written while this one streams
 template <int MODE>
 constexpr int q_bufs() { return 2; }
-template <int MODE>
-constexpr uint32_t off_reg() { return q_bufs<MODE>() * 3 * kQPlane; }   // streaming region
-constexpr int kFineSlots = 3;
+// bytes of one q buffer: coarse keeps room for three planes, fine for its NQ planes (1 for
+// bf16 q, 3 for f32 q), and the fine ring takes the rest: 5 key tiles with bf16 q, 3 with f32
+template <int MODE, int NQ>
+constexpr uint32_t q_span() { return MODE == kFine ? NQ * kQPlane : 3 * kQPlane; }
+template <int MODE, int NQ>
+constexpr uint32_t off_reg() { return q_bufs<MODE>() * q_span<MODE, NQ>(); }   // streaming region
+template <int NQ>
+constexpr int fine_slots() { return NQ == 1 ? 5 : 3; }
 constexpr uint32_t kTileBytes = kM * kD * 2;              // fine: one [128 x 128] bf16 key tile
 constexpr uint32_t kRawBytes = kM * 32 * 4;               // coarse: f32 means, 128 rows x 32 dims
 constexpr int kRawSlots = 7;                              // coarse raw boxes in flight
@@ -64,15 +69,15 @@ constexpr int kASlots = 8;
 constexpr uint32_t kAColBase = 128, kABoxCols = 48;
 static_assert(kAColBase + kASlots * kABoxCols <= 512, "coarse TMEM");
 // coarse: kRawSlots raw f32 boxes; fine: the key tile ring
-template <int MODE>
+template <int MODE, int NQ>
 constexpr uint32_t region_bytes() {
-    return MODE == kCoarse ? kRawSlots * kRawBytes : kFineSlots * kTileBytes;
+    return MODE == kCoarse ? kRawSlots * kRawBytes : fine_slots<NQ>() * kTileBytes;
 }
 // TMEM columns between the two accumulators
 template <int MODE>
 constexpr uint32_t acc_stride() { return MODE == kCoarse ? 64 : 256; }
 constexpr uint32_t kOffReg = 2 * 3 * kQPlane;             // coarse streaming region
-static_assert(off_reg<kCoarse>() == kOffReg, "coarse layout");
+static_assert(off_reg<kCoarse, 1>() == kOffReg && off_reg<kCoarse, 3>() == kOffReg, "coarse layout");
 
 struct QMeta {            // one query row, double-buffered
     int row;              // b * L + j
@@ -89,13 +94,13 @@ struct QMeta {            // one query row, double-buffered
 // barriers
 constexpr int kBarMetaFull = 0, kBarSlotFree = 2, kBarQFull = 4, kBarQEmpty = 6,
               kBarAccFull = 8, kBarAccEmpty = 10, kBarScFull = 12, kBarDrain = 14,
-              kBarFull = 15,                // fine: kFineSlots; coarse: kASlots TMEM boxes, then kRawSlots raw
+              kBarFull = 15,                // fine: its key slots; coarse: kASlots TMEM boxes, then kRawSlots raw
               kBarEmpty = kBarFull + kASlots + kRawSlots, kBarMeansReady = kBarEmpty + kASlots + kRawSlots,
               kNumBars = kBarMeansReady + 2;
 
-template <int MODE>
+template <int MODE, int NQ>
 struct Layout {
-    static constexpr uint32_t meta = off_reg<MODE>() + region_bytes<MODE>();
+    static constexpr uint32_t meta = off_reg<MODE, NQ>() + region_bytes<MODE, NQ>();
     static constexpr uint32_t bars = meta + 2 * sizeof(QMeta);
     static constexpr uint32_t misc = bars + kNumBars * 8;
     static constexpr uint32_t sc = (misc + 64 + 15) & ~15u;   // 2 x n_cap floats
@@ -109,13 +114,15 @@ static_assert(kPipeMaxFine <= kSmallMax && kPipeMaxCoarse <= kSmallMax, "select 
 
 // 227 KiB of shared memory per CTA: the layout, two score rows at capacity and the static
 // select state (kept blocks and the select warps' SelectShared)
-template <int MODE>
+template <int MODE, int NQ>
 constexpr bool fits() {
     constexpr int cap = MODE == kCoarse ? kPipeMaxCoarse : kPipeMaxFine;
-    return Layout<MODE>::fixed + 2 * cap * 4 + sizeof(SelectShared<kGroup>) + 256 <=
+    return Layout<MODE, NQ>::fixed + 2 * cap * 4 + sizeof(SelectShared<kGroup>) + 256 <=
            227 * 1024;
 }
-static_assert(fits<kCoarse>() && fits<kFine>(), "shared memory");
+static_assert(fits<kCoarse, 1>() && fits<kCoarse, 3>() && fits<kFine, 1>() && fits<kFine, 3>(),
+              "shared memory");
+static_assert(fine_slots<1>() <= kASlots + kRawSlots && fine_slots<3>() <= kASlots + kRawSlots, "barriers");
 
 }  // namespace
 }  // namespace hisa
@@ -131,8 +138,9 @@ struct FineIds {
         return (int32_t)(blk[(int)c >> 6] * 64 + ((int)c & 63));
     }
 };
-struct SameIds {
-    __device__ __forceinline__ int32_t operator()(int64_t c) const { return (int32_t)c; }
+struct OffsetIds {                        // coarse: block id = chunk start + column
+    int off;
+    __device__ __forceinline__ int32_t operator()(int64_t c) const { return (int32_t)(off + c); }
 };
 
 
@@ -143,7 +151,8 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     k_score_pipe(const __grid_constant__ ScoreTcParams P) {
     constexpr int NQ = QBF16 ? 1 : 3;                       // q planes
     constexpr int kQB = q_bufs<MODE>();
-    using Lay = Layout<MODE>;
+    using Lay = Layout<MODE, NQ>;
+    constexpr int kFineSlots = fine_slots<NQ>();
     const ScoreParams &p = P.s;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ SelectShared<kGroup> sel_sh;             // the select warps' state
@@ -159,7 +168,9 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     const int n_cap = (int)p.n_max;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rows = p.B * p.L;
+    // coarse rows longer than kCoarseChunk blocks run as P.chunks virtual rows each
+    const int nch = MODE == kCoarse && P.chunks > 1 ? P.chunks : 1;
+    const int rows = p.B * p.L * nch;
     const int nql = (int)blockIdx.x < rows ? (rows - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
     // The first query's q, weights and offsets into L2 while the barriers and TMEM are set
@@ -167,7 +178,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     // the previous kernel writes).
     if (warp >= kWarpBld && warp < kWarpBld + 4 && nql > 0) {
         const int bt = tid - kWarpBld * 32;
-        const int row = (int)blockIdx.x, bq = row / p.L;
+        const int row = (int)blockIdx.x / nch, bq = row / p.L;
         const char *qrow = static_cast<const char *>(p.q) + (int64_t)row * kH * kD * (QBF16 ? 2 : 4);
         for (int o = bt * 128; o < kH * kD * (QBF16 ? 2 : 4); o += kGroup * 128)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + o));
@@ -217,7 +228,8 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
         const int bt = tid - kWarpBld * 32;
         for (int i = 0; i < nql; ++i) {
             const int qb = i & 1;
-            const int row = (int)blockIdx.x + i * (int)gridDim.x;
+            const int vrow = (int)blockIdx.x + i * (int)gridDim.x;
+            const int row = vrow / nch, chunk = vrow - row * nch;
             const int bq = row / p.L, j = row - bq * p.L;
             // this row's weights, offsets and position first (the row's checks and the loader's
             // first copies wait on them), then q, then the kept blocks: the loads overlap the
@@ -269,11 +281,18 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                     st = 1;
                     flag(p.status, HISA_DEV_GATE);
                 } else if (MODE == kCoarse) {
-                    n = Np / p.b;
-                    base = m0;
-                    if (!means_ok_v(m0, m1, n, p.means_rows) || n > n_cap) {
+                    const int64_t nb = Np / p.b;
+                    const int64_t c0 = (int64_t)chunk * kCoarseChunk;
+                    n = nb - c0 < kCoarseChunk ? nb - c0 : kCoarseChunk;   // this chunk's blocks
+                    base = m0 + c0;
+                    if (!means_ok_v(m0, m1, nb, p.means_rows) || n > n_cap ||
+                        nb > (int64_t)nch * kCoarseChunk) {
                         st = 1;
+                        n = 0;
                         flag(p.status, HISA_DEV_BAD_OFFSETS);
+                    } else if (n <= 0) {
+                        st = 2;                           // a chunk past this row's blocks
+                        n = 0;
                     }
                 } else {
                     n = (int64_t)p.keep * 64;
@@ -286,7 +305,9 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 M.state = st;
                 M.n = (int)n;
                 M.T = (int)((n + kM - 1) / kM);
-                M.t_new = fb < n ? (int)(fb / kM) : M.T;
+                // the chunk's first new block (chunk-local), if it holds any
+                const int64_t fbl = fb - (int64_t)chunk * kCoarseChunk;
+                M.t_new = fbl < n ? (int)((fbl > 0 ? fbl : 0) / kM) : M.T;
                 M.base = base;
                 M.V = p.causal ? visible_len(t_row, p.r, Np) : Np;
                 mbar_arrive(&bars[kBarMetaFull + qb]);
@@ -294,7 +315,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 w2 = i < kQB || wait_bar(&bars[kBarQEmpty + i % kQB], (i / kQB - 1) & 1, abort);
             }
             if (!group_all(kBarBld, kGroup, w2)) { fail(); break; }
-            const uint32_t qoff = kOffQ + (uint32_t)(i % kQB) * (3 * kQPlane);
+            const uint32_t qoff = kOffQ + (uint32_t)(i % kQB) * q_span<MODE, NQ>();
             qr.store(smem + qoff, bt);
             fence_async_smem();
             mbar_arrive(&bars[kBarQFull + i % kQB]);
@@ -302,7 +323,10 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 // block means of the newly completed blocks [first_block, nb)
                 const QMeta &M = meta[qb];
                 if (!M.state) {
-                    append_block_means(reinterpret_cast<const uint4 *>(P.append_keys), k0, fb, M.n,
+                    // this chunk's new blocks, chunk-local: keys from block c0, means from base
+                    const int64_t c0 = (int64_t)chunk * kCoarseChunk;
+                    const int64_t fbl = fb - c0 > 0 ? fb - c0 : 0;
+                    append_block_means(reinterpret_cast<const uint4 *>(P.append_keys), k0 + c0 * 64, fbl, M.n,
                                        const_cast<float *>(reinterpret_cast<const float *>(p.rows)), M.base, bt);
                     fence_async_global();               // the loader reads them by TMA
                 }
@@ -326,7 +350,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                         break;
                     }
                     const int nblk = p.keep - 2 * t < 2 ? p.keep - 2 * t : 2;
-                    const uint32_t slot = sbase + off_reg<MODE>() + s * kTileBytes;
+                    const uint32_t slot = sbase + off_reg<MODE, NQ>() + s * kTileBytes;
                     mbar_arrive_expect_tx(&bars[kBarFull + s], (uint32_t)nblk * 16384u);
                     for (int hb = 0; hb < nblk; ++hb) {
                         const int32_t y = (int32_t)(M.base + (int64_t)M.blk[2 * t + hb] * 64);
@@ -392,7 +416,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 break;
             }
             fence_after_sync();
-            const uint64_t qd = smem_desc_sw128(sbase + kOffQ + (uint32_t)(i % kQB) * (3 * kQPlane), 16, 1024);
+            const uint64_t qd = smem_desc_sw128(sbase + kOffQ + (uint32_t)(i % kQB) * q_span<MODE, NQ>(), 16, 1024);
             const QMeta &M = meta[qb];
             const int T = M.state ? 0 : M.T;
             for (int t = 0; t < T; ++t, ++g) {
@@ -410,7 +434,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                         break;
                     }
                     fence_after_sync();
-                    const uint64_t rd = smem_desc_sw128(sbase + off_reg<MODE>() + s * kTileBytes, 16, 1024);
+                    const uint64_t rd = smem_desc_sw128(sbase + off_reg<MODE, NQ>() + s * kTileBytes, 16, 1024);
 #pragma unroll
                     for (int ks = 0; ks < kD / 16; ++ks) {
                         const uint32_t ko = ks >> 2, kb = (ks & 3) * 32;
@@ -456,7 +480,8 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
         uint32_t g = 0;
         for (int i = 0; i < nql && ok; ++i) {
             const int qb = i & 1;
-            const int row = (int)blockIdx.x + i * (int)gridDim.x;
+            const int vrow = (int)blockIdx.x + i * (int)gridDim.x;
+            const int row = vrow / nch, c0 = (vrow - row * nch) * kCoarseChunk;
             if (!wait_bar(&bars[kBarMetaFull + qb], (i >> 1) & 1, abort) ||
                 (i >= 2 && !wait_bar(&bars[kBarSlotFree + qb], ((i >> 1) - 1) & 1, abort))) {
                 fail();
@@ -491,11 +516,11 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
                 const int cidx = t * kM + r;
                 if (cidx < M.n) {
                     // coarse: a block is eligible iff its first row is visible
-                    const int64_t pos = MODE == kCoarse ? (int64_t)cidx * p.b
+                    const int64_t pos = MODE == kCoarse ? (int64_t)(c0 + cidx) * p.b
                                                         : (int64_t)M.blk[cidx >> 6] * 64 + (cidx & 63);
                     const float score = pos < M.V ? acc : kNeg;
                     sc[cidx] = score;
-                    if (p.out) p.out[(int64_t)row * p.ld_out + cidx] = score;
+                    if (p.out) p.out[(int64_t)row * p.ld_out + c0 + cidx] = score;
                 }
             }
             if (!ok) break;
@@ -509,23 +534,28 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
         const int st = tid - kWarpSel * 32;
         for (int i = 0; i < nql; ++i) {
             const int qb = i & 1;
-            const int row = (int)blockIdx.x + i * (int)gridDim.x;
+            const int vrow = (int)blockIdx.x + i * (int)gridDim.x;
+            const int row = vrow / nch, c0 = (vrow - row * nch) * kCoarseChunk;
             const bool w = wait_bar(&bars[kBarScFull + qb], (i >> 1) & 1, abort);
             if (!group_all(kBarSel, kGroup, w)) { fail(); break; }
             const QMeta &M = meta[qb];
             const float *sc = scb + qb * n_cap;
-            int32_t *out = P.sel + (int64_t)row * P.k_sel;
+            int32_t *out = nch > 1 ? P.chunk_ids + (int64_t)vrow * P.k_sel : P.sel + (int64_t)row * P.k_sel;
             const int64_t kout = M.state ? 0 : (M.n < P.k_sel ? M.n : P.k_sel);
             if (kout > 0) {
                 if (MODE == kFine)
                     small_topk<kGroup, kBarSel, kWarpSel * 32>(sc, M.n, (int)kout, out, FineIds{M.blk}, sel_sh,
                                                               p.status);
                 else
-                    small_topk<kGroup, kBarSel, kWarpSel * 32>(sc, M.n, (int)kout, out, SameIds{}, sel_sh,
+                    small_topk<kGroup, kBarSel, kWarpSel * 32>(sc, M.n, (int)kout, out, OffsetIds{c0}, sel_sh,
                                                               p.status);
             }
             for (int64_t e = kout + st; e < P.k_sel; e += kGroup) out[e] = -1;
             named_sync(kBarSel, kGroup);
+            if (MODE == kCoarse && nch > 1) {            // the chunk's selected scores, for the merge
+                if (st < kout) P.chunk_sc[(int64_t)vrow * P.k_sel + st] = sc[out[st] - c0];
+                named_sync(kBarSel, kGroup);              // all reads of sc done before it is freed
+            }
             if (st == 0) mbar_arrive(&bars[kBarSlotFree + qb]);
         }
     }
@@ -586,7 +616,7 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
 
 int score_pipe_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_max, int b, int keep) {
     if (H_i != kH || D_i != kD || n_max < 1) return 0;
-    if (mode == kCoarse) return !rows_bf16 && n_max <= kPipeMaxCoarse;
+    if (mode == kCoarse) return !rows_bf16 && keep <= 64 && n_max <= (int64_t)kCoarseChunk * kCoarseMaxChunks;
     if (mode == kFine) return rows_bf16 && b == 64 && keep >= 1 && keep <= 48 && n_max <= kPipeMaxFine;
     return 0;
 }
@@ -609,13 +639,14 @@ template <int MODE, bool QBF16>
 cudaError_t launch_pipe_t(const ScoreTcParams &p, cudaStream_t s) {
     constexpr int cap = MODE == kCoarse ? kPipeMaxCoarse : kPipeMaxFine;
     const cudaError_t attr =
-        smem_attr_once<k_score_pipe<MODE, QBF16>>((int)(Layout<MODE>::fixed + 2 * cap * 4));
+        smem_attr_once<k_score_pipe<MODE, QBF16>>((int)(Layout<MODE, QBF16 ? 1 : 3>::fixed + 2 * cap * 4));
+    if (p.s.n_max > cap) return cudaErrorInvalidValue;
     if (attr != cudaSuccess) return attr;
-    const int rows = p.s.B * p.s.L;
+    const int rows = p.s.B * p.s.L * (MODE == kCoarse && p.chunks > 1 ? p.chunks : 1);
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = rows < sms ? rows : sms;
-    const size_t smem = Layout<MODE>::fixed + 2 * (size_t)p.s.n_max * 4;
+    const size_t smem = Layout<MODE, QBF16 ? 1 : 3>::fixed + 2 * (size_t)p.s.n_max * 4;
     // the coarse form waits for the previous grid before its first global access (before it
     // only warms L2 by prefetches), so it may always start while that grid ends
     const int chained = MODE == kCoarse ? 1 : p.s.chained;
@@ -625,9 +656,65 @@ cudaError_t launch_pipe_t(const ScoreTcParams &p, cudaStream_t s) {
 
 }  // namespace
 
+cudaError_t launch_score_pipe_rows(const ScoreTcParams &p, cudaStream_t s);
+
+namespace {
+
+// The top keep blocks of each long coarse row from its chunks' top keep (id, score) pairs:
+// by (score desc, id asc), -0.0 equal to +0.0, ids < 0 (chunks past the row, invalid rows)
+// skipped; written in ascending id order, -1 past the candidates. One thread per candidate.
+__global__ void __launch_bounds__(kCoarseMaxChunks * 64) k_coarse_merge(const int32_t *ids, const float *sc,
+                                                                        int chunks, int keep, int32_t *top_blk) {
+    __shared__ uint32_t s_key[kCoarseMaxChunks * 64];
+    __shared__ int32_t s_id[kCoarseMaxChunks * 64];
+    __shared__ int s_sel[kCoarseMaxChunks * 64];
+    __shared__ int s_count;
+    const int row = blockIdx.x, t = threadIdx.x, m = chunks * keep;
+    const int32_t id = t < m ? ids[(int64_t)row * m + t] : -1;
+    const uint32_t key = id >= 0 ? order_key(sc[(int64_t)row * m + t]) : 0u;
+    s_key[t] = key;
+    s_id[t] = id;
+    if (t == 0) s_count = 0;
+    __syncthreads();
+    int rank = 0;
+    if (id >= 0)
+        for (int u = 0; u < m; ++u)
+            rank += (s_id[u] >= 0 && (s_key[u] > key || (s_key[u] == key && s_id[u] < id))) ? 1 : 0;
+    const int sel = id >= 0 && rank < keep;
+    s_sel[t] = sel;
+    if (sel) atomicAdd(&s_count, 1);
+    __syncthreads();
+    if (sel) {
+        int pos = 0;
+        for (int u = 0; u < m; ++u) pos += (s_sel[u] && s_id[u] < id) ? 1 : 0;
+        top_blk[(int64_t)row * keep + pos] = id;
+    }
+    for (int e = s_count + t; e < keep; e += blockDim.x) top_blk[(int64_t)row * keep + e] = -1;
+}
+
+}  // namespace
+
 cudaError_t launch_score_pipe(const ScoreTcParams &p_in, cudaStream_t s) {
     ScoreTcParams p = p_in;
     if (p.s.B * p.s.L == 0) return cudaSuccess;
+    if (p.s.mode == kCoarse && p.chunks > 1) {
+        // chunks of kCoarseChunk blocks, then the merge of their selections
+        if (p.chunks > kCoarseMaxChunks || !p.chunk_ids || !p.chunk_sc || p.k_sel > 64)
+            return cudaErrorInvalidValue;
+        int32_t *sel = p.sel;
+        p.s.n_max = kCoarseChunk;
+        cudaError_t e = launch_score_pipe_rows(p, s);
+        if (e != cudaSuccess) return e;
+        k_coarse_merge<<<(unsigned)(p.s.B * p.s.L), kCoarseMaxChunks * 64, 0, s>>>(
+            p.chunk_ids, p.chunk_sc, p.chunks, p.k_sel, sel);
+        return cudaGetLastError();
+    }
+    p.chunks = 1;
+    return launch_score_pipe_rows(p, s);
+}
+
+cudaError_t launch_score_pipe_rows(const ScoreTcParams &p_in, cudaStream_t s) {
+    ScoreTcParams p = p_in;
     if (p.s.mode == kFine &&
         !encode_bf16_map(&p.keys_map, p.s.rows, (uint64_t)p.s.keys_rows, kD, 64, 64))
         return cudaErrorInvalidValue;

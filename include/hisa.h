@@ -312,7 +312,9 @@ HISA_API hisa_status hisa_compress_append(const hisa_compress_desc *desc, const 
  *   I          [B, L, k] int32 pooled ids (-1 = skip), or NULL for the dense branch over
  *              all Np_b rows. With L > 1 ids >= V(t0+j) are masked.
  *   sinks      [H] f32;  t0 [B] int32
- *   out        [B, L, H, Dh] f32 out
+ *   out        [B, L, H, Dh] f32 out (any device-accessible address: device memory, or the
+ *              device address of page-locked host memory, which the kernels then write
+ *              directly over the host link)
  * Np_b == 0 gives local-only attention (branch 1 of the three-way branch). */
 HISA_API hisa_status hisa_sparse_attend(const hisa_attn_desc *desc, const void *q, const void *local_kv,
                                const int32_t *local_len, const int32_t *local_pos0,

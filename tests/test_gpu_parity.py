@@ -693,3 +693,58 @@ def test_prefill_coarse_contraction_ragged_rows():
     res = run_hisa(prob)
     rows = [(b, j) for b in range(3) for j in (0, 1, 2, 17, 50, 63, 64, 98, 99)]
     check_rows(data, prob, res, rows)
+
+
+def test_combine_writes_to_page_locked_host_memory():
+    """The combine's output may be page-locked host memory (its device address): the kernels
+    then write the results straight to the host (over NVLink-C2C on GB300). The host copy
+    equals, bit for bit, the output written to device memory; the split path (few rows,
+    partials in the workspace, then the merge kernel) and the single-pass path both."""
+    data = v4_small("peaked", B=3, Np=(2048, 3000, 1500), seed=17)
+    prob = Problem(data)
+    rng = np.random.default_rng(3)
+    I = np.stack([rng.choice(int(n), 512, replace=False) for n in (2048, 3000, 1500)]).astype(np.int32)
+    It = torch.as_tensor(I, device="cuda")
+    prob.attend(I=It)
+    torch.cuda.synchronize()
+    ref = prob.out.cpu()
+    host_out = torch.full(tuple(prob.out.shape), 5.0, dtype=torch.float32).pin_memory()
+    dptr = hb.device_pointer_of_pinned(host_out)
+    prob.attend(I=It, out=hb.DevicePointer(dptr, host_out.numel()))
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    assert torch.equal(host_out, ref)
+    for b in range(3):
+        P.check_attend(data, b, 0, host_out[b].numpy(), I[b])
+
+
+def test_many_long_coarse_rows_in_chunks():
+    """Coarse rows of more than 1024 blocks (Np over 65536 pooled rows) with more rows than a
+    few: the coarse pipeline scores each row as chunks of 1024 blocks (the newest blocks' means
+    appended by the chunk that holds them), each chunk selects its top blocks with their scores,
+    and a merge picks the row's top blocks; a 262144-row sequence takes four chunks, two short
+    sequences leave their second chunk empty. The fine stage follows as usual."""
+    B = 24
+    rng = np.random.default_rng(91)
+    Np = [int(x) for x in rng.integers(65600, 70000, size=B)]
+    Np[3], Np[11], Np[19] = 5000, 1100, 262144
+    Np = tuple(Np)
+    wl = inputs.small_workload(name="past_pipe", seed=91, B=B, H_i=64, D_i=128, index_block=64,
+                               index_keep=16, index_topk=512, q_idx_dtype="f32", key_dtype="bf16",
+                               Np=Np, with_attention=False)
+    data = inputs.generate(wl)
+    prob = Problem(data)
+    nb = np.asarray(Np) // 64
+    cs = torch.full((B, int(nb.max())), 7.0, device="cuda")
+    fs = torch.full((B, 1024), 7.0, device="cuda")
+    prob.block_means(first_block=np.zeros(B, np.int32))
+    prob.block_filter_append(first_block=torch.as_tensor((nb - 2).astype(np.int32), device="cuda"),
+                             cscores=cs)
+    prob.select_topk(fscores=fs)
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    tb, I, cs, fs = np_(prob.top_blk), np_(prob.I), np_(cs), np_(fs)
+    P.check_block_means(data, np_(prob.means), np_(prob.means_off), 64)
+    for b in (0, 3, 7, 11, 19, 23):
+        P.check_coarse(data, b, 0, tb[b], cs[b], 64, 16)
+        P.check_fine(data, b, 0, tb[b], I[b], fs[b], 64, 512)
