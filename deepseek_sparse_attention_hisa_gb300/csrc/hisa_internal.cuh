@@ -19,12 +19,13 @@ namespace hisa {
 // stream runs. grid_dep_wait() waits until the previous grid has completed and its writes
 // are visible (without the attribute it returns at once: the kernel started after the
 // previous work completed). Most kernels execute it before their first global-memory
-// access. Two kinds of kernel let their successor start early, once all of their CTAs have
-// finished streaming (grid_dep_trigger): the coarse / fine scoring pipeline, whose fine
-// form reads q, w and the offsets before it waits and only the kept blocks (the coarse
-// output) after; and the combine, which waits before its first selected id (the fine
-// output) and first output write, after its first item's q and local rows are on their
-// way. The flag's contract (include/hisa.h) is that no such early-read input is written
+// access. The scoring pipeline and the combine let their successor launch before they
+// complete (grid_dep_trigger): the coarse form and the combine once every role of a CTA is
+// done, the fine form right after its own wait (never before it, so that a successor never
+// runs beside the kernel two back). The fine form reads q, w and the offsets before it
+// waits and only the kept blocks (the coarse output) after; the combine waits before its
+// first selected id (the fine output) and first output write, after its first item's q and
+// local rows are on their way. The flag's contract (include/hisa.h) is that no such early-read input is written
 // by the kernel just before the call.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

@@ -247,7 +247,13 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             const int64_t t_row = p.causal ? (int64_t)p.t0[bq] + j : 0;
             QRegs<QBF16, MODE == kCoarse> qr;
             qr.load(p.q, row, bt);
-            if (MODE == kFine && i == 0) grid_dep_wait();
+            if (MODE == kFine && i == 0) {
+                grid_dep_wait();
+                // the fine form lets a chained successor (the combine) launch now: its CTAs
+                // take each SM as this kernel's CTA there exits and load their first item's
+                // q and local rows while the last selections finish
+                grid_dep_trigger();
+            }
             int bv = 0;
             if (MODE == kFine && bt < p.keep) bv = __ldg(p.top_blk + (int64_t)row * p.keep + bt);
             // meta slot qb is free once query i - 2 is selected
@@ -603,9 +609,10 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
     if (!ok) flag(p.status, HISA_DEV_TIMEOUT);
     fence_before_sync();
     __syncthreads();
-    // every role of this CTA is done: the next kernel may take over the SM once this CTA
-    // exits (it waits for this grid before it reads what this grid writes)
-    grid_dep_trigger();
+    // coarse: every role of this CTA is done, the successor may take the SM once it exits.
+    // (Triggered right after its wait instead, the fine grid launched while the coarse one
+    // ran, and both pipeline kernels then streamed more slowly, as measured.)
+    if (MODE == kCoarse) grid_dep_trigger();
     if (warp == kWarpMma) {
         fence_after_sync();
         tmem_dealloc(tmem, 512);

@@ -748,3 +748,36 @@ def test_many_long_coarse_rows_in_chunks():
     for b in (0, 3, 7, 11, 19, 23):
         P.check_coarse(data, b, 0, tb[b], cs[b], 64, 16)
         P.check_fine(data, b, 0, tb[b], I[b], fs[b], 64, 512)
+
+
+@pytest.mark.parametrize("Np", [(41034, 5000, 65536), (30000,)], ids=["B3", "B1"])
+def test_few_sequences_append_filter_select(Np):
+    """A batch of a few sequences (one scoring CTA per row, most SMs idle): a 1024-block
+    row, a ragged 641-block row, a short row and a single query, with the newest two blocks'
+    means appended by the coarse call itself; block means, coarse and fine against the oracle,
+    and a repeated coarse call on the same workspace gives the same kept blocks."""
+    B = len(Np)
+    wl = inputs.small_workload(name="few_sequences", seed=93, B=B, H_i=64, D_i=128,
+                               index_block=64, index_keep=16, index_topk=512, q_idx_dtype="f32",
+                               key_dtype="bf16", Np=Np, with_attention=False)
+    data = inputs.generate(wl)
+    prob = Problem(data)
+    nb = np.asarray(Np) // 64
+    cs = torch.full((B, int(nb.max())), 7.0, device="cuda")
+    fs = torch.full((B, 1024), 7.0, device="cuda")
+    prob.block_means(first_block=np.zeros(B, np.int32))
+    prob.block_filter_append(first_block=torch.as_tensor((nb - 2).astype(np.int32), device="cuda"),
+                             cscores=cs)
+    prob.select_topk(fscores=fs)
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    tb, I, cs, fs = np_(prob.top_blk), np_(prob.I), np_(cs), np_(fs)
+    P.check_block_means(data, np_(prob.means), np_(prob.means_off), 64)
+    for b in range(B):
+        P.check_coarse(data, b, 0, tb[b], cs[b], 64, 16)
+        P.check_fine(data, b, 0, tb[b], I[b], fs[b], 64, 512)
+    prob.top_blk.fill_(-7)
+    prob.block_filter()
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    assert np.array_equal(np_(prob.top_blk), tb)
