@@ -154,18 +154,6 @@ ScoreParams score_params(const hisa_index_desc *d, int mode, const void *q, cons
     return p;
 }
 
-int device_sms() {
-    static int counts[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (counts[dev] == 0) {
-        int c = 0;
-        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        counts[dev] = c;
-    }
-    return counts[dev];
-}
-
 // A few long coarse / fine rows (a single long-context query): one CTA per row would leave
 // most SMs idle, so each row's tiles are split over CTAs and a separate select follows.
 // (Splitting shorter rows, or more of them, measured slower than one CTA per row: the
@@ -173,7 +161,7 @@ int device_sms() {
 // longer than the persistent pipeline takes (over 4096 blocks, 1M+ tokens) are split
 // whatever their number.
 bool split_rows(const hisa_index_desc *d, int mode, int64_t n) {
-    const int sms = device_sms();
+    const int sms = device_sm_count();
     const bool few_long = n >= 2048 && n_rows(d) * 8 <= sms;
     const bool past_pipe = mode == kCoarse && n > (int64_t)kCoarseChunk * kCoarseMaxChunks;
     return sms > 0 && (few_long || past_pipe) &&
@@ -231,6 +219,18 @@ cudaError_t run_scores(const ScoreParams &p, int32_t *sel, int k_sel, bool *fuse
 }
 
 }  // namespace
+
+int hisa::device_sm_count() {
+    static std::atomic<int> counts[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int c = counts[dev].load(std::memory_order_relaxed);
+    if (c == 0) {
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev].store(c, std::memory_order_relaxed);
+    }
+    return c;
+}
 
 extern "C" {
 

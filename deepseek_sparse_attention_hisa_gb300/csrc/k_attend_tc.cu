@@ -673,11 +673,8 @@ cudaError_t launch_attend_tc(const AttnParams &p, cudaStream_t s) {
     const cudaError_t attr = smem_attr_once<k_attend_tc>((int)kSmemBytes);
     if (attr != cudaSuccess) return attr;
     // persistent: one CTA per SM walks the items (query row, split)
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-    int nsm = 0;
-    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return cudaErrorInvalidDevice;
+    const int nsm = device_sm_count();
+    if (nsm <= 0) return cudaErrorInvalidDevice;
     const int64_t items = (int64_t)p.B * p.L * p.nsplit;
     if (items == 0) return cudaSuccess;
     dim3 grid((unsigned)(items < nsm ? items : nsm));

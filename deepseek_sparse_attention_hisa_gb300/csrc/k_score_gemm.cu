@@ -341,18 +341,6 @@ bool encode_map_rows(CUtensorMap *map, const void *base, uint64_t rows, uint32_t
     return encode_bf16_map(map, base, rows, kD, 64, box_rows);
 }
 
-int sm_count_gemm() {
-    static int counts[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (counts[dev] == 0) {
-        int c = 0;
-        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        counts[dev] = c;
-    }
-    return counts[dev];
-}
-
 }  // namespace
 
 int score_gemm_supported(int H_i, int D_i, int q_bf16, int rows_bf16, int B, int L) {
@@ -373,7 +361,7 @@ cudaError_t launch_gemm_t(const ScoreParams &s, const void *key_rows, uint64_t n
         return cudaErrorInvalidValue;
     const cudaError_t attr = smem_attr_once<k_score_gemm<NP>>((int)kSmem);
     if (attr != cudaSuccess) return attr;
-    const int sms = sm_count_gemm();
+    const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = units < sms ? (int)units : sms;
     return launch_pdl(k_score_gemm<NP>, dim3(grid), dim3(kThreads), kSmem, stream, s.chained, P);

@@ -630,18 +630,6 @@ int score_pipe_supported(int mode, int H_i, int D_i, int rows_bf16, int64_t n_ma
 
 namespace {
 
-int sm_count() {
-    static int counts[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (counts[dev] == 0) {
-        int c = 0;
-        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        counts[dev] = c;
-    }
-    return counts[dev];
-}
-
 template <int MODE, bool QBF16>
 cudaError_t launch_pipe_t(const ScoreTcParams &p, cudaStream_t s) {
     constexpr int cap = MODE == kCoarse ? kPipeMaxCoarse : kPipeMaxFine;
@@ -650,7 +638,7 @@ cudaError_t launch_pipe_t(const ScoreTcParams &p, cudaStream_t s) {
     if (p.s.n_max > cap) return cudaErrorInvalidValue;
     if (attr != cudaSuccess) return attr;
     const int rows = p.s.B * p.s.L * (MODE == kCoarse && p.chunks > 1 ? p.chunks : 1);
-    const int sms = sm_count();
+    const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int grid = rows < sms ? rows : sms;
     const size_t smem = Layout<MODE, QBF16 ? 1 : 3>::fixed + 2 * (size_t)p.s.n_max * 4;
