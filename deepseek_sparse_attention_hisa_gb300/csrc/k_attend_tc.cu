@@ -391,6 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 }
                 if (!ok) break;
                 mma_commit_warp(&bars[kBarQFree]);
+                // the CTA's last item has all its S products: a successor may launch during
+                // its last PV products and epilogue (it waits for this grid)
+                if (id + (int)gridDim.x >= items) grid_dep_trigger();
             } else {
                 // O^T += V^T . P^T of every tile; O^T starts from zero once the previous item's
                 // epilogue has read it, and is handed to the epilogue after the last tile

@@ -544,6 +544,9 @@ __global__ void __launch_bounds__(pipe_threads<MODE>(), 1)
             const int row = vrow / nch, c0 = (vrow - row * nch) * kCoarseChunk;
             const bool w = wait_bar(&bars[kBarScFull + qb], (i >> 1) & 1, abort);
             if (!group_all(kBarSel, kGroup, w)) { fail(); break; }
+            // coarse: the CTA's last scores are in, so its successor may launch during this
+            // top-Kb (it waits for this grid before reading what it writes)
+            if (MODE == kCoarse && i == nql - 1) grid_dep_trigger();
             const QMeta &M = meta[qb];
             const float *sc = scb + qb * n_cap;
             int32_t *out = nch > 1 ? P.chunk_ids + (int64_t)vrow * P.k_sel : P.sel + (int64_t)row * P.k_sel;
