@@ -556,6 +556,13 @@ def run_gpu(args, wl, R):
     assert prob.status(stream) == 0, "device status flags set during the timed region"
     e2e_ms = e2e_pipelined(prob, host_in, host_out, calls_for, K, dev)
     e2e_direct_ms = e2e_pipelined(prob, host_in, host_out, calls_for, K, dev, direct_out=True)
+    # the same, with the combine's output rounded to bf16 (hisa_attn_desc.out_dtype): half the
+    # bytes copied back; reported beside the f32 figures, never as the value
+    prob16 = prob.with_out("bf16")
+    host_out16 = {"out": torch.empty_like(prob16.out, device="cpu").pin_memory(),
+                  "I": host_out["I"]}
+    d2h16 = sum(t.numel() * t.element_size() for t in host_out16.values())
+    e2e_b16_ms = e2e_pipelined(prob16, host_in, host_out16, calls_for, K, dev)
 
     per_stage_bytes, step_bytes = stage_bytes(wl, nb)
     peak, peak_src = peaks()
@@ -600,12 +607,16 @@ def run_gpu(args, wl, R):
                 "copied_out_value": job_value(world, R, 1, e2e_ms),
                 "direct_out_value": job_value(world, R, 1, e2e_direct_ms),
                 "serial_value": job_value(world, R, 1, e2e_serial_ms),
+                "bf16_out_value": job_value(world, R, 1, e2e_b16_ms),
+                "bf16_out_d2h_bytes_per_step": d2h16,
                 "how": "two buffer sets: step i's inputs copied in and step i-1's results copied "
                        "out on their own streams while step i computes; every step's copies are "
                        "in the timed region. value = the better of copied_out_value (out and I "
                        "copied back by cudaMemcpy) and direct_out_value (the combine writes out "
                        "straight into page-locked host memory, I copied back); serial_value: copy "
-                       "in, step, copy out, one after the other, L2 flushed before each",
+                       "in, step, copy out, one after the other, L2 flushed before each; "
+                       "bf16_out_value: as copied_out_value with out rounded to bf16 by the "
+                       "combine (out_dtype = HISA_BF16), not part of value",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "wall_s": t_wall,

@@ -46,7 +46,7 @@ class AttnDesc(ctypes.Structure):
                 ("Dh", ctypes.c_int32), ("window", ctypes.c_int32), ("W_max", ctypes.c_int32),
                 ("r", ctypes.c_int32), ("k", ctypes.c_int32), ("Np_max", ctypes.c_int64),
                 ("kv_rows", ctypes.c_int64), ("scale", ctypes.c_float), ("q_dtype", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
+                ("kv_dtype", ctypes.c_int32), ("flags", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
 
 
 class CompressDesc(ctypes.Structure):

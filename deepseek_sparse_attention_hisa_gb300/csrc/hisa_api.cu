@@ -53,7 +53,8 @@ hisa_status check_attn_desc(const hisa_attn_desc *d) {
     if (d->kv_rows < 0 || d->kv_rows > 0x7fffffffLL) return HISA_EINVAL;
     if ((int64_t)d->B * d->L > 0x7fffffffLL) return HISA_EINVAL;
     if (d->flags & ~(int32_t)HISA_FLAG_CHAINED) return HISA_EINVAL;
-    if (!dtype_ok(d->q_dtype) || !dtype_ok(d->kv_dtype) || d->q_dtype != d->kv_dtype)
+    if (!dtype_ok(d->q_dtype) || !dtype_ok(d->kv_dtype) || d->q_dtype != d->kv_dtype ||
+        !dtype_ok(d->out_dtype))
         return HISA_EDTYPE;
     if (!attend_simt_supported(d->H, d->Dh)) return HISA_EDTYPE;
     return HISA_OK;
@@ -514,7 +515,7 @@ hisa_status hisa_compress_append(const hisa_compress_desc *d, const float *kv, c
 hisa_status hisa_sparse_attend(const hisa_attn_desc *d, const void *q, const void *local_kv,
                                const int32_t *local_len, const int32_t *local_pos0,
                                const void *pooled_kv, const int64_t *kv_off, const int32_t *I,
-                               const float *sinks, const int32_t *t0, float *out, void *ws,
+                               const float *sinks, const int32_t *t0, void *out, void *ws,
                                size_t ws_bytes, hisa_stream_t stream) {
     hisa_status st = check_attn_desc(d);
     if (st != HISA_OK) return st;
@@ -537,6 +538,7 @@ hisa_status hisa_sparse_attend(const hisa_attn_desc *d, const void *q, const voi
     p.q = q; p.local_kv = local_kv; p.local_len = local_len; p.local_pos0 = local_pos0;
     p.pooled_kv = pooled_kv; p.kv_off = kv_off; p.I = I; p.sinks = sinks; p.t0 = t0;
     p.out = out;
+    p.out_bf16 = d->out_dtype == HISA_BF16;
     p.part = scratch_of(ws);
     int64_t per = 0;
     p.nsplit = pick_nsplit((int64_t)d->B * d->L, attn_list_len(d, dense), &per);

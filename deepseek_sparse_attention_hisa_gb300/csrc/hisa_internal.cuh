@@ -193,7 +193,8 @@ struct AttnParams {
     const int32_t *I;         // [B*L, k] or nullptr
     const float *sinks;       // [H]
     const int32_t *t0;
-    float *out;               // [B*L, H, Dh]
+    void *out;                // [B*L, H, Dh] f32, or bf16 when out_bf16
+    int out_bf16;
     float *part;              // split partials [B*L, nsplit, H, Dh + 2]
     int nsplit;
     int rows_per_split;       // multiple of the chunk size

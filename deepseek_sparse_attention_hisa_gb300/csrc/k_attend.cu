@@ -213,9 +213,21 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend_simt(AttnParams p) {
             const float wm = (mh == -INFINITY) ? 0.f : expf(mh - M);
             const float denom = sl[h] * wm + expf(sink - M);
             const float f = wm / denom;
-            float4 *dst = reinterpret_cast<float4 *>(p.out + ((int64_t)row * H + h) * DH + dg * 8);
-            dst[0] = make_float4(acc[it][0] * f, acc[it][1] * f, acc[it][2] * f, acc[it][3] * f);
-            dst[1] = make_float4(acc[it][4] * f, acc[it][5] * f, acc[it][6] * f, acc[it][7] * f);
+            const int64_t at = ((int64_t)row * H + h) * DH + dg * 8;
+            if (p.out_bf16) {
+                uint4 v;
+                uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[it][2 * e] * f, acc[it][2 * e + 1] * f);
+                    w[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + at) = v;
+            } else {
+                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + at);
+                dst[0] = make_float4(acc[it][0] * f, acc[it][1] * f, acc[it][2] * f, acc[it][3] * f);
+                dst[1] = make_float4(acc[it][4] * f, acc[it][5] * f, acc[it][6] * f, acc[it][7] * f);
+            }
         } else {
             float *base = p.part + (((int64_t)row * p.nsplit + split) * H + h) * (DH + 2);
             if (dg == 0) { base[0] = sm[h]; base[1] = sl[h]; }
@@ -247,7 +259,11 @@ __global__ void k_attend_combine(AttnParams p) {
             const float m = base[s * stride];
             if (m != -INFINITY) o += base[s * stride + 2 + d] * expf(m - M);
         }
-        p.out[((int64_t)row * H + h) * DH + d] = o / denom;
+        const int64_t at = ((int64_t)row * H + h) * DH + d;
+        if (p.out_bf16)
+            static_cast<__nv_bfloat16 *>(p.out)[at] = __float2bfloat16_rn(o / denom);
+        else
+            static_cast<float *>(p.out)[at] = o / denom;
     }
 }
 

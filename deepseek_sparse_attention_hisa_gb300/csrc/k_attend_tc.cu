@@ -612,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
             if (n == 0) grid_dep_wait();                // before the first output write
             const bool have_o = x.T > 0;
             if (p.nsplit == 1) {
-                float *out = p.out + (int64_t)x.row * kH * kDH;
+                const int64_t out0 = (int64_t)x.row * kH * kDH;
                 for (int mt = 0; mt < 4; ++mt) {
                     const int d = mt * 128 + quad * 32 + lane;
                     for (int c = 0; c < 64; c += 16) {
@@ -624,8 +624,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
 #pragma unroll
                             for (int q = 0; q < 16; ++q) o[q] = 0.f;
                         }
+                        if (p.out_bf16) {
+                            __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + out0;
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) out[(c + q) * kDH + d] = o[q] * misc->factor[c + q];
+                            for (int q = 0; q < 16; ++q)
+                                out[(c + q) * kDH + d] = __float2bfloat16_rn(o[q] * misc->factor[c + q]);
+                        } else {
+                            float *out = static_cast<float *>(p.out) + out0;
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) out[(c + q) * kDH + d] = o[q] * misc->factor[c + q];
+                        }
                     }
                 }
             } else {

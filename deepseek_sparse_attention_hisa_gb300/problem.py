@@ -28,7 +28,7 @@ class Problem:
     `data` is the dict returned by inputs.generate (numpy arrays; uint16 = bf16 bits).
     """
 
-    def __init__(self, data: dict, device="cuda", index_keep: int | None = None):
+    def __init__(self, data: dict, device="cuda", index_keep: int | None = None, out_dtype="f32"):
         import torch
         wl = data["wl"]
         self.wl = wl
@@ -78,8 +78,10 @@ class Problem:
                 B=wl.B, L=wl.L, H=wl.H, Dh=wl.Dh, window=wl.window,
                 W_max=int(data["local_kv"].shape[1]), r=wl.r, k=self.k, Np_max=self.Np_max,
                 kv_rows=int(self.pooled_kv.shape[0]), scale=0.0, q_dtype=hb.dtype_code(self.q_attn),
-                kv_dtype=hb.dtype_code(self.pooled_kv))
-            self.out = torch.empty((rows, wl.H, wl.Dh), dtype=torch.float32, device=dev)
+                kv_dtype=hb.dtype_code(self.pooled_kv),
+                out_dtype=hb.HISA_BF16 if out_dtype == "bf16" else hb.HISA_F32)
+            self.out = torch.empty((rows, wl.H, wl.Dh), device=dev,
+                                   dtype=torch.bfloat16 if out_dtype == "bf16" else torch.float32)
             need = max(need, hb.workspace_bytes(hb.OP_SPARSE_ATTEND, self.adesc))
         if need == 0:
             raise ValueError("descriptor rejected by hisa_workspace_bytes")
@@ -92,6 +94,21 @@ class Problem:
         if self.has_attention:
             self.adesc_chained = hb.AttnDesc.from_buffer_copy(self.adesc)
             self.adesc_chained.flags = hb.FLAG_CHAINED
+
+    def with_out(self, out_dtype: str):
+        """The same problem (inputs, caches, selections, workspace) with the combine writing
+        an output of another dtype ("f32" or "bf16") into a buffer of its own."""
+        import copy
+        import torch
+        c = copy.copy(self)
+        code = hb.HISA_BF16 if out_dtype == "bf16" else hb.HISA_F32
+        c.adesc = hb.AttnDesc.from_buffer_copy(self.adesc)
+        c.adesc.out_dtype = code
+        c.adesc_chained = hb.AttnDesc.from_buffer_copy(self.adesc_chained)
+        c.adesc_chained.out_dtype = code
+        c.out = torch.empty(self.out.shape, device=self.out.device,
+                            dtype=torch.bfloat16 if out_dtype == "bf16" else torch.float32)
+        return c
 
     def io_clone(self):
         """A second set of the per-step buffers (query inputs, selections, output, workspace)

@@ -136,6 +136,8 @@ typedef struct {
     int32_t q_dtype;      /* hisa_dtype of q; must equal kv_dtype */
     int32_t kv_dtype;     /* hisa_dtype of local_kv and pooled_kv */
     int32_t flags;        /* HISA_FLAG_* bits (0 = none) */
+    int32_t out_dtype;    /* hisa_dtype of out: HISA_F32 (0, the default) or HISA_BF16, the
+                             f32 result rounded to nearest even once, after the combine */
 } hisa_attn_desc;
 
 /* The indexer's compressor ([HiSA issue] "The pooled stream and positions", "Configuration":
@@ -312,14 +314,14 @@ HISA_API hisa_status hisa_compress_append(const hisa_compress_desc *desc, const 
  *   I          [B, L, k] int32 pooled ids (-1 = skip), or NULL for the dense branch over
  *              all Np_b rows. With L > 1 ids >= V(t0+j) are masked.
  *   sinks      [H] f32;  t0 [B] int32
- *   out        [B, L, H, Dh] f32 out (any device-accessible address: device memory, or the
- *              device address of page-locked host memory, which the kernels then write
- *              directly over the host link)
+ *   out        [B, L, H, Dh] out, f32 or bf16 as desc->out_dtype says (any device-accessible
+ *              address, 16-byte aligned: device memory, or the device address of page-locked
+ *              host memory, which the kernels then write directly over the host link)
  * Np_b == 0 gives local-only attention (branch 1 of the three-way branch). */
 HISA_API hisa_status hisa_sparse_attend(const hisa_attn_desc *desc, const void *q, const void *local_kv,
                                const int32_t *local_len, const int32_t *local_pos0,
                                const void *pooled_kv, const int64_t *kv_off, const int32_t *I,
-                               const float *sinks, const int32_t *t0, float *out, void *ws,
+                               const float *sinks, const int32_t *t0, void *out, void *ws,
                                size_t ws_bytes, hisa_stream_t stream);
 
 #ifdef __cplusplus

@@ -84,10 +84,10 @@ int main(void) {
          offsetof(hisa_index_desc, keys_rows), offsetof(hisa_index_desc, means_rows),
          offsetof(hisa_index_desc, q_dtype), offsetof(hisa_index_desc, k_dtype),
          offsetof(hisa_index_desc, flags));
-  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(hisa_attn_desc), offsetof(hisa_attn_desc, Np_max),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(hisa_attn_desc), offsetof(hisa_attn_desc, Np_max),
          offsetof(hisa_attn_desc, kv_rows), offsetof(hisa_attn_desc, scale),
          offsetof(hisa_attn_desc, q_dtype), offsetof(hisa_attn_desc, kv_dtype),
-         offsetof(hisa_attn_desc, flags));
+         offsetof(hisa_attn_desc, flags), offsetof(hisa_attn_desc, out_dtype));
   printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(hisa_compress_desc),
          offsetof(hisa_compress_desc, rope_theta), offsetof(hisa_compress_desc, eps),
          offsetof(hisa_compress_desc, tok_rows), offsetof(hisa_compress_desc, keys_rows),
@@ -112,7 +112,7 @@ int main(void) {
                  hb.IndexDesc.q_dtype.offset, hb.IndexDesc.k_dtype.offset, hb.IndexDesc.flags.offset]
     assert a == [ctypes.sizeof(hb.AttnDesc), hb.AttnDesc.Np_max.offset, hb.AttnDesc.kv_rows.offset,
                  hb.AttnDesc.scale.offset, hb.AttnDesc.q_dtype.offset, hb.AttnDesc.kv_dtype.offset,
-                 hb.AttnDesc.flags.offset]
+                 hb.AttnDesc.flags.offset, hb.AttnDesc.out_dtype.offset]
 
 
 def v4_index_desc(**kw):
@@ -187,6 +187,10 @@ def test_host_validation_rejects_before_launch(lib):
     # flag bits other than HISA_FLAG_CHAINED
     a = v4_attn_desc(flags=0x2)
     assert lib.hisa_sparse_attend(ctypes.byref(a), *args) == hb.HISA_EINVAL
+    # output dtype: f32 (0) or bf16 (1)
+    a = v4_attn_desc(out_dtype=2)
+    assert lib.hisa_sparse_attend(ctypes.byref(a), *args) == hb.HISA_EDTYPE
+    assert hb.workspace_bytes(hb.OP_SPARSE_ATTEND, v4_attn_desc(out_dtype=hb.HISA_BF16)) >= 256
     assert hb.workspace_bytes(hb.OP_SPARSE_ATTEND, v4_attn_desc(flags=hb.FLAG_CHAINED)) >= 256
     g = v4_index_desc(flags=0x4)
     assert lib.hisa_flat_topk(ctypes.byref(g), fake, fake, fake, fake, fake, fake, fake, 1 << 30,

@@ -781,3 +781,38 @@ def test_few_sequences_append_filter_select(Np):
     torch.cuda.synchronize()
     assert prob.status() == 0
     assert np.array_equal(np_(prob.top_blk), tb)
+
+
+@pytest.mark.parametrize("case", ["tc_rows", "tc_split", "simt"])
+def test_bf16_output_is_the_f32_output_rounded_once(case):
+    """hisa_attn_desc.out_dtype = HISA_BF16: the combine's f32 result rounded to nearest even
+    once (bit for bit the f32 output of the same call rounded), within the widened bound of
+    the oracle. tc_rows: 160 V4-shape rows, one item per row (the tensor-core epilogue);
+    tc_split: 3 rows split over CTAs (the merge kernel writes out); simt: f32 KV on the CUDA
+    cores."""
+    if case == "simt":
+        data = small(B=2, Np=(300, 700), seed=17, kv_dtype="f32", key_dtype="f32")
+        k = 32
+    else:
+        B = 160 if case == "tc_rows" else 3
+        rng = np.random.default_rng(18)
+        Np = tuple(int(x) for x in rng.integers(600, 1500, size=B))
+        data = v4_small("peaked", B=B, Np=Np, seed=18)
+        k = 512
+    B = data["wl"].B
+    f32 = Problem(data)
+    b16 = Problem(data, out_dtype="bf16")
+    rng = np.random.default_rng(19)
+    I = np.stack([rng.choice(int(n), min(k, int(n)), replace=False).tolist() + [-1] * (k - min(k, int(n)))
+                  for n in data["Np"]]).astype(np.int32)
+    It = torch.as_tensor(I, device="cuda")
+    f32.attend(I=It)
+    b16.attend(I=It)
+    torch.cuda.synchronize()
+    assert f32.status() == 0 and b16.status() == 0
+    assert b16.out.dtype == torch.bfloat16
+    want = f32.out.to(torch.bfloat16)                     # round to nearest even
+    assert torch.equal(b16.out.view(torch.int16), want.view(torch.int16))
+    got = b16.out.view(torch.int16).cpu().numpy().view(np.uint16)
+    for b in sorted({0, 1, B - 1}):
+        P.check_attend(data, b, 0, got[b], I[b], out_bf16=True)

@@ -268,3 +268,28 @@ def test_score_scale_skips_heads_that_relu_zeroes():
     q = np.array([[1.0, 0.0], [-1.0, 0.0]])
     A = P.score_scale(q, w, rows)
     assert A[0] == pytest.approx(2.0 * c) and A[1] == pytest.approx(2.0 * c)
+
+
+@pytest.mark.parametrize("kv", ["f32", "bf16"])
+def test_bf16_output_rounding_is_accepted_and_mistakes_are_not(kv):
+    """A bf16 output (hisa_attn_desc.out_dtype) is the result rounded to nearest once: the
+    oracle's own output rounded so passes the widened check. With f32 KV the plain f32 check
+    (eps = 2^-13) rejects that rounding, so the widening is what admits it; zeros and a sign
+    flip of one head stay rejected."""
+    data = inputs.generate(inputs.peaked(inputs.WORKLOADS["v4flash_decode"]) if kv == "bf16"
+                           else inputs.small_workload(seed=5, kv_dtype="f32"))
+    Np = int(data["Np"][0])
+    k = int(data["wl"].index_topk)
+    I = np.arange(min(k, Np))
+    o = P.combine_row(data, 0, 0, I)
+    E = P.combine_row(data, 0, 0, I, magnitude=True)
+    r = inputs.f32_to_bf16_bits(o.astype(np.float32))
+    err, _, n_bad = P.attention_violations(r, o, E, kv, out_bf16=True)
+    assert n_bad == 0 and err <= P.ATTN_TOL[kv] + P.OUT_BF16_U * np.abs(o).max()
+    if kv == "f32":
+        _, _, n_plain = P.attention_violations(O.to_f64(r), o, E, kv)
+        assert n_plain > 0
+    for bad in (np.zeros_like(o), np.where(np.arange(o.shape[0])[:, None] == 3, -o, o)):
+        b16 = inputs.f32_to_bf16_bits(bad.astype(np.float32))
+        _, _, nb = P.attention_violations(b16, o, E, kv, out_bf16=True)
+        assert nb > 0
