@@ -173,3 +173,23 @@ def test_rows_past_the_cache_are_flagged_not_written():
     keys2, _, _, st2 = run(data2, keys_rows=14)
     assert st2 & hb.DEV_BAD_OFFSETS
     np.testing.assert_array_equal(host(keys2), data2["keys"])
+
+
+@pytest.mark.parametrize("B", [100, 200])
+def test_many_sequences_appending_a_row_or_two(B):
+    """Decode and two-token appends for many sequences at once: one or two new pooled rows
+    each, some completing a block (from 62, 63 or 127 cached rows), some inside one. With
+    up to two touched blocks per sequence the call runs 2 B CTAs: 200 take the compressor's
+    four-row-lane form (two CTAs per SM), 400 its one-lane form."""
+    rng = np.random.default_rng(200 + B)
+    p_first = rng.choice([62, 63, 127, 30, 95], size=B)
+    n_new = rng.integers(1, 3, size=B)
+    data = inputs.compressor_inputs(300 + B, p_first=p_first.tolist(), n_new=n_new.tolist(),
+                                    capacity=[192] * B)
+    keys, m, moff, st = run(data)
+    assert st == 0
+    check_rows(data, keys)
+    done = check_means(data, keys, m, moff)
+    want = sum(1 for p, n in zip(p_first, n_new) for beta in range(3)
+               if beta * 64 + 63 >= p and (beta + 1) * 64 <= p + n)
+    assert done == want and done > 0
