@@ -640,6 +640,7 @@ def run_gpu(args, wl, R):
         line["verify_L4"] = run_verify(dev, stream)
         line["compressor_append"] = run_compress(dev, stream, R)
         line["r_sweep"] = run_r_sweep(dev, stream)
+        line["per_step_means"] = run_per_step_means(dev, stream, R)
     if not args.no_np_sweep and world == 1:
         line["decode_np_sweep"] = run_np_sweep(dev, stream, R)
     if world > 1:
@@ -767,6 +768,47 @@ def decode_leg(wl, dev, stream, flush, n, seed, what):
            "bytes_per_step": nbytes, "hbm_gbs": nbytes / (mean / 1e3) / 1e9,
            "frac": nbytes / (mean / 1e3) / 1e9 / peak, "peak_source": src}
     del prob, data, g
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_per_step_means(dev, stream, R, n=10):
+    """The decode step with every block mean recomputed from the keys each step
+    (hisa_block_means over all blocks, then the coarse filter, fine top-k and combine)
+    instead of the cached means with the newest block appended: the reading of the
+    pages' step that keeps no cache. Reported beside the headline, never as it; its
+    bytes add every sequence's Np keys (8 MiB at Np = 32768)."""
+    import torch
+
+    from deepseek_sparse_attention_hisa_gb300.problem import Problem
+    wl = inputs.WORKLOADS["v4flash_decode"].replace(B=R, Np=(32768,))
+    data = inputs.generate_device(wl, device=dev, seed=7000)
+    prob = Problem(data, device=dev)
+    def step(s):
+        prob.block_means(stream=s)                       # every block of every sequence
+        prob.block_filter(stream=s)
+        prob.select_topk(stream=s, chained=True)
+        prob.attend(stream=s, chained=True)
+    g = capture(step, stream)
+    flush = L2Flush(dev)
+    mean, med = timed_graph(g, stream, flush, n)
+    gm = capture(lambda s: prob.block_means(stream=s), stream)
+    means_ms, _ = timed_graph(gm, stream, flush, n)
+    assert prob.status(stream) == 0
+    nb = int(prob.nb[0])
+    keys = int(wl.Np[0]) * wl.D_i * 2
+    # step_bytes_rows counts the newest block's keys and mean; here all keys are read and
+    # all nb means written (and read back by the coarse filter)
+    per_seq = step_bytes_rows(wl, nb, 1) - (wl.index_block * wl.D_i * 2 + wl.D_i * 4) + keys + nb * wl.D_i * 4
+    nbytes = R * per_seq
+    peak, src = peaks()
+    out = {"workload": f"v4flash_decode, R = {R} queries per step, Np = 32768, block means recomputed each step",
+           "us_per_step": mean * 1e3, "us_median": med * 1e3, "rows_per_s": R / (mean / 1e3),
+           "bytes_per_step": nbytes, "hbm_gbs": nbytes / (mean / 1e3) / 1e9,
+           "frac": nbytes / (mean / 1e3) / 1e9 / peak, "peak_source": src,
+           "block_means_us": means_ms * 1e3,
+           "block_means_frac": R * (keys + nb * wl.D_i * 4) / (means_ms / 1e3) / 1e9 / peak}
+    del prob, data, g, gm
     torch.cuda.empty_cache()
     return out
 

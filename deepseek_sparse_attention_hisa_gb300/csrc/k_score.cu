@@ -233,13 +233,31 @@ __global__ void __launch_bounds__(kMeansThreads) k_block_means_staged(MeansParam
     const int n = p.b * p.D_i;                          // keys of one block
     const KT *keys = reinterpret_cast<const KT *>(p.keys);
     const float inv_div = (float)p.b;
-    for (int64_t beta = fb + blockIdx.x; beta < nb; beta += gridDim.x) {
+    // a block that one round of loads covers (bf16 64 x 128): the next block's loads are
+    // issued before this one is summed, so a CTA keeps a block in flight throughout
+    const bool one_round = n / kPer <= 4 * kMeansThreads;
+    uint4 nxt[4];
+    auto load_block = [&](int64_t beta, uint4 *u) {
         const uint4 *src = reinterpret_cast<const uint4 *>(keys + (k0 + beta * p.b) * p.D_i);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int vv = (int)threadIdx.x + m * kMeansThreads;
+            if (vv < n / kPer) u[m] = __ldg(src + vv);
+        }
+    };
+    if (one_round && fb + blockIdx.x < nb) load_block(fb + blockIdx.x, nxt);
+    for (int64_t beta = fb + blockIdx.x; beta < nb; beta += gridDim.x) {
         for (int v = threadIdx.x; v < n / kPer; v += 4 * kMeansThreads) {
             uint4 u[4];
+            if (one_round) {
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
-                if (v + m * kMeansThreads < n / kPer) u[m] = __ldg(src + v + m * kMeansThreads);
+                for (int m = 0; m < 4; ++m) u[m] = nxt[m];
+            } else {
+                const uint4 *src = reinterpret_cast<const uint4 *>(keys + (k0 + beta * p.b) * p.D_i);
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    if (v + m * kMeansThreads < n / kPer) u[m] = __ldg(src + v + m * kMeansThreads);
+            }
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int vv = v + m * kMeansThreads;
@@ -250,6 +268,7 @@ __global__ void __launch_bounds__(kMeansThreads) k_block_means_staged(MeansParam
                 }
             }
         }
+        if (one_round && beta + gridDim.x < nb) load_block(beta + gridDim.x, nxt);
         __syncthreads();
         for (int d = threadIdx.x; d < p.D_i; d += kMeansThreads) {
             // partial sums over the rows i = k (mod 8), each in row order, then the fixed
@@ -268,14 +287,78 @@ __global__ void __launch_bounds__(kMeansThreads) k_block_means_staged(MeansParam
     }
 }
 
+// bf16 keys, D_i and b multiples of 8, b <= 64: the same sums without staging. Thread
+// (k, g) of a D_i-thread CTA loads rows k, k + 8, ... of the block, dims 8 g .. 8 g + 7, one
+// 16-byte load per row (a warp reads two whole adjacent rows per load), and adds them in row
+// order into the block's partial sums k of those dims; only the eight partial sums per dim
+// pass through shared memory, to the same pairwise tree.
+__global__ void __launch_bounds__(128, 8) k_block_means_rows(MeansParams p) {
+    __shared__ float part[8][128];
+    grid_dep_wait();
+    const int bq = blockIdx.y;
+    const int64_t k0 = p.key_off[bq];
+    const int64_t Np = p.key_off[bq + 1] - k0;
+    if (!seq_ok(p.key_off, bq, p.Np_max, p.keys_rows)) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
+        return;
+    }
+    const int64_t nb = Np / p.b;
+    const int64_t m0 = p.means_off[bq];
+    if (!means_ok(p.means_off, bq, nb, p.means_rows)) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
+        return;
+    }
+    int64_t fb = p.first_block ? (int64_t)p.first_block[bq] : 0;
+    if (fb < 0) fb = 0;
+    const int groups = p.D_i / 8, t = (int)threadIdx.x;
+    const int k = t / groups, g = t - k * groups;           // residue class, dim group
+    const int per = p.b / 8;                                  // rows of a class in a block
+    const __nv_bfloat16 *keys = static_cast<const __nv_bfloat16 *>(p.keys);
+    for (int64_t beta = fb + blockIdx.x; beta < nb; beta += gridDim.x) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(keys + (k0 + beta * p.b + k) * p.D_i + g * 8);
+        const int64_t step = p.D_i;                           // uint4s from row i to row i + 8
+        uint4 u[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < per) u[j] = __ldg(src + j * step);
+        float ps[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ps[e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < per) {
+                const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(&u[j]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ps[e] += __bfloat162float(x[e]);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part[k][g * 8 + e] = ps[e];
+        __syncthreads();
+        if (t < p.D_i) {
+            const float s = ((part[0][t] + part[1][t]) + (part[2][t] + part[3][t])) +
+                            ((part[4][t] + part[5][t]) + (part[6][t] + part[7][t]));
+            p.means[(m0 + beta) * p.D_i + t] = s / (float)p.b;
+        }
+        __syncthreads();
+    }
+}
+
 cudaError_t launch_block_means(const MeansParams &p, int64_t nb_max, cudaStream_t s) {
     if (nb_max <= 0) return cudaSuccess;
-    // Blocks [first_block, nb) are walked grid-stride; size the grid from the batch so
-    // an incremental update (few new blocks per sequence) launches few idle CTAs.
-    int64_t per_seq = (kTargetCtas + p.B - 1) / p.B;
+    // Blocks [first_block, nb) are walked grid-stride. An incremental update (first_block
+    // given: few new blocks per sequence) sizes the grid from the batch, so that few CTAs
+    // idle; a full build (no first_block) takes six CTAs per SM (as many as fit at once
+    // with 32 KiB of staging each: one wave), each keeping a 64-row block in flight, which
+    // the DRAM latency needs (two per SM ran at ~2.3 TB/s).
+    const bool rows = p.keys_bf16 && p.D_i % 8 == 0 && p.D_i <= 128 && p.b % 8 == 0 && p.b <= 64;
+    // the register form runs eight 128-thread CTAs per SM, each with a block in flight
+    const int64_t target = p.first_block ? kTargetCtas : (rows ? 8 : 6) * (int64_t)kSmTarget;
+    int64_t per_seq = (target + p.B - 1) / p.B;
     if (per_seq > nb_max) per_seq = nb_max;
     const unsigned gx = (unsigned)(per_seq < 1 ? 1 : per_seq);
     dim3 grid(gx, (unsigned)p.B);
+    if (rows) return launch_pdl(k_block_means_rows, grid, dim3(p.D_i), 0, s, p.chained, p);
     if ((int64_t)p.b * p.D_i <= kMeansStage) {
         if (p.keys_bf16)
             return launch_pdl(k_block_means_staged<__nv_bfloat16>, grid, dim3(kMeansThreads), 0, s, p.chained,

@@ -19,6 +19,8 @@ def _i64(a, device):
 
 def _i32(a, device):
     import torch
+    if isinstance(a, torch.Tensor):                  # no copy when it already is (graph capture)
+        return a.to(device=device, dtype=torch.int32)
     return torch.as_tensor(np.asarray(a, dtype=np.int32), device=device)
 
 
