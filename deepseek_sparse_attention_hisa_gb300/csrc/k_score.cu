@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(256) k_scores_simt(ScoreParams p) {
     float *sq = smem;                      // [H_i][D] f32
     float *sw = sq + p.H_i * D;            // [H_i] scaled weights
     int *sblk = reinterpret_cast<int *>(sw + p.H_i);  // [keep] kept blocks, ascending
+    int *sraw = sblk + 64;                             // [keep] kept blocks as read
 
     const int row = blockIdx.x;            // b * L + j
     const int bq = row / p.L;
@@ -76,13 +77,18 @@ __global__ void __launch_bounds__(256) k_scores_simt(ScoreParams p) {
     for (int e = threadIdx.x; e < p.H_i * D; e += blockDim.x) sq[e] = to_f32(qrow[e]);
     for (int h = threadIdx.x; h < p.H_i; h += blockDim.x)
         sw[h] = p.w[(int64_t)row * p.H_i + h] * p.head_scale;
-    if (p.mode == kFine && threadIdx.x == 0) {
-        const int32_t *tb = p.top_blk + (int64_t)row * p.keep;
-        for (int s = 0; s < p.keep; ++s) {  // insertion sort: candidates in ascending pos
-            int v = tb[s], u = s;
-            while (u > 0 && sblk[u - 1] > v) { sblk[u] = sblk[u - 1]; --u; }
-            sblk[u] = v;
+    if (p.mode == kFine && (int)threadIdx.x < p.keep)
+        sraw[threadIdx.x] = p.top_blk[(int64_t)row * p.keep + threadIdx.x];
+    __syncthreads();
+    if (p.mode == kFine && (int)threadIdx.x < p.keep) {
+        // candidates in ascending pos: thread s places kept block s by its rank, ties by index
+        const int v = sraw[threadIdx.x];
+        int rank = 0;
+        for (int u = 0; u < p.keep; ++u) {
+            const int o = sraw[u];
+            rank += (o < v || (o == v && u < (int)threadIdx.x)) ? 1 : 0;
         }
+        sblk[rank] = v;
     }
     __syncthreads();
 
@@ -132,7 +138,7 @@ __global__ void __launch_bounds__(256) k_scores_simt(ScoreParams p) {
 
 template <int D, typename QT, typename KT>
 static cudaError_t launch_scores_t(const ScoreParams &p, cudaStream_t s) {
-    const size_t smem = (size_t)p.H_i * D * 4 + (size_t)p.H_i * 4 + 64 * 4;
+    const size_t smem = (size_t)p.H_i * D * 4 + (size_t)p.H_i * 4 + 2 * 64 * 4;
     const cudaError_t attr = smem_attr_once<k_scores_simt<D, QT, KT>>(128 * 128 * 4 + 1024);
     if (attr != cudaSuccess) return attr;
     const int64_t tiles = (p.n_max + 255) / 256;

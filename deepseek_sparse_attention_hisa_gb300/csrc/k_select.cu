@@ -14,7 +14,7 @@ constexpr size_t kMergeSmem = 200 * 1024;                 // candidate scores + 
 template <int NT>
 __global__ void __launch_bounds__(NT) k_select(SelectParams p) {
     __shared__ SelectShared<NT> sh;
-    __shared__ int s_blk[64];
+    __shared__ int s_raw[64], s_blk[64];
     __shared__ int s_bad;
 
     const int row = blockIdx.x;
@@ -37,19 +37,23 @@ __global__ void __launch_bounds__(NT) k_select(SelectParams p) {
         n = (p.mode == kCoarse) ? Np / p.b : (int64_t)p.keep * p.b;
     }
     if (ok && p.mode == kFine) {
-        if (tid == 0) {
-            const int32_t *tb = p.top_blk + (int64_t)row * p.keep;
-            int bad = 0;
-            for (int s = 0; s < p.keep; ++s) {  // insertion sort: candidates in ascending pos
-                int v = tb[s], u = s;
-                if (v < 0 || (int64_t)v >= Np / p.b) bad = 1;
-                while (u > 0 && s_blk[u - 1] > v) { s_blk[u] = s_blk[u - 1]; --u; }
-                s_blk[u] = v;
+        // the kept blocks in ascending order (candidates in ascending pos): all are loaded at
+        // once, then thread s places block s by its rank, ties by index
+        if (tid < p.keep) s_raw[tid] = p.top_blk[(int64_t)row * p.keep + tid];
+        if (tid == 0) s_bad = 0;
+        __syncthreads();
+        if (tid < p.keep) {
+            const int v = s_raw[tid];
+            int rank = 0;
+            for (int u = 0; u < p.keep; ++u) {
+                const int o = s_raw[u];
+                rank += (o < v || (o == v && u < tid)) ? 1 : 0;
             }
-            s_bad = bad;
-            if (bad) flag(p.status, HISA_DEV_BAD_BLOCK);
+            s_blk[rank] = v;
+            if (v < 0 || (int64_t)v >= Np / p.b) s_bad = 1;
         }
         __syncthreads();
+        if (tid == 0 && s_bad) flag(p.status, HISA_DEV_BAD_BLOCK);
         ok = !s_bad;
     }
     if (!ok) {
@@ -130,23 +134,25 @@ __global__ void __launch_bounds__(NT) k_select_merge(SelectParams p, int cap) {
     }
     const int64_t kout = n < (int64_t)p.k ? n : (int64_t)p.k;
     const float *w = p.work + (int64_t)row * p.ld;
-    int m = 0;
-    for (int64_t c = 0; c * kChunk < n; ++c) {
-        int64_t len = n - c * kChunk;
-        len = len > kChunk ? kChunk : len;
+    // every chunk but the last is longer than 2k (k <= 2048 < kChunk / 2) and holds k
+    // candidates, so candidate i of the row (chunk order) is entry i % k of chunk i / k,
+    // or of the last chunk past them: all loads go out at once
+    const int64_t nchunk = (n + kChunk - 1) / kChunk;
+    const int64_t last = n - (nchunk - 1) * kChunk;               // length of the last chunk
+    const bool last_reduced = last > 2 * (int64_t)p.k;
+    const int m = n > 0 ? (int)((nchunk - 1) * p.k + (last_reduced ? p.k : last)) : 0;
+#pragma unroll 4
+    for (int i = tid; i < m; i += NT) {
+        int64_t c = i / p.k;
+        if (c > nchunk - 1) c = nchunk - 1;
+        const int e = (int)(i - c * p.k);
         const float *wc = w + c * kChunk;
-        if (len > 2 * (int64_t)p.k) {
-            for (int e = tid; e < p.k; e += NT) {
-                s_sc[m + e] = wc[2 * e];
-                s_id[m + e] = __float_as_int(wc[2 * e + 1]);
-            }
-            m += p.k;
+        if (c < nchunk - 1 || last_reduced) {
+            s_sc[i] = wc[2 * e];
+            s_id[i] = __float_as_int(wc[2 * e + 1]);
         } else {
-            for (int e = tid; e < (int)len; e += NT) {
-                s_sc[m + e] = wc[e];
-                s_id[m + e] = (int32_t)(c * kChunk + e);
-            }
-            m += (int)len;
+            s_sc[i] = wc[e];
+            s_id[i] = (int32_t)(c * kChunk + e);
         }
     }
     __syncthreads();
