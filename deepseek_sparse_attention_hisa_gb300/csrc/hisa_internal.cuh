@@ -46,12 +46,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// cudaFuncSetAttribute(Kernel, MaxDynamicSharedMemorySize, bytes), made once per device
-// (the attribute belongs to the device's context) and its result cached per device.
-// Concurrent first calls may both set it, which is harmless.
 // SMs of the current device (cached per device; 0 if the runtime cannot tell).
 int device_sm_count();
 
+// cudaFuncSetAttribute(Kernel, MaxDynamicSharedMemorySize, bytes), made once per device
+// (the attribute belongs to the device's context) and its result cached per device.
+// Concurrent first calls may both set it, which is harmless.
 template <auto Kernel>
 cudaError_t smem_attr_once(int bytes) {
     static std::atomic<int> state[64];      // 0: not yet set; else 1 + the cudaError_t

@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend_simt(AttnParams p) {
 // n = sum_s l_s e^{m_s - M} + e^{sink - M}, out = sum_s acc_s e^{m_s - M} / n.
 template <int DH>
 __global__ void k_attend_combine(AttnParams p) {
+    grid_dep_wait();                                 // the partials are the previous grid's
     const int row = blockIdx.x, h = blockIdx.y;
     const int H = p.H;
     const float sink = p.sinks[h];
@@ -270,12 +271,13 @@ __global__ void k_attend_combine(AttnParams p) {
 cudaError_t launch_attend_combine(const AttnParams &p, cudaStream_t s) {
     dim3 g2((unsigned)(p.B * p.L), (unsigned)p.H);
     switch (p.Dh) {
-        case 64: k_attend_combine<64><<<g2, 64, 0, s>>>(p); break;
-        case 128: k_attend_combine<128><<<g2, 128, 0, s>>>(p); break;
-        case 512: k_attend_combine<512><<<g2, 256, 0, s>>>(p); break;
+        // waits before its first global access, so it may always be launched as a
+        // programmatic dependent of the kernel that writes the partials
+        case 64: return launch_pdl(k_attend_combine<64>, g2, dim3(64), 0, s, 1, p);
+        case 128: return launch_pdl(k_attend_combine<128>, g2, dim3(128), 0, s, 1, p);
+        case 512: return launch_pdl(k_attend_combine<512>, g2, dim3(256), 0, s, 1, p);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 template <int H, int DH, typename T>

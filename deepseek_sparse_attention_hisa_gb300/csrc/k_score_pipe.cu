@@ -665,6 +665,7 @@ __global__ void __launch_bounds__(kCoarseMaxChunks * 64) k_coarse_merge(const in
                                                                         int chunks, int keep, int32_t *top_blk) {
     __shared__ uint32_t s_key[kCoarseMaxChunks * 64];
     __shared__ int32_t s_id[kCoarseMaxChunks * 64];
+    grid_dep_wait();                                 // the pairs are the previous grid's
     __shared__ int s_sel[kCoarseMaxChunks * 64];
     __shared__ int s_count;
     const int row = blockIdx.x, t = threadIdx.x, m = chunks * keep;
@@ -703,9 +704,10 @@ cudaError_t launch_score_pipe(const ScoreTcParams &p_in, cudaStream_t s) {
         p.s.n_max = kCoarseChunk;
         cudaError_t e = launch_score_pipe_rows(p, s);
         if (e != cudaSuccess) return e;
-        k_coarse_merge<<<(unsigned)(p.s.B * p.s.L), kCoarseMaxChunks * 64, 0, s>>>(
-            p.chunk_ids, p.chunk_sc, p.chunks, p.k_sel, sel);
-        return cudaGetLastError();
+        // the merge waits before its first global access: a programmatic dependent
+        return launch_pdl(k_coarse_merge, dim3((unsigned)(p.s.B * p.s.L)), dim3(kCoarseMaxChunks * 64), 0, s, 1,
+                          static_cast<const int32_t *>(p.chunk_ids), static_cast<const float *>(p.chunk_sc),
+                          p.chunks, p.k_sel, sel);
     }
     p.chunks = 1;
     return launch_score_pipe_rows(p, s);

@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(NT) k_select(SelectParams p) {
     __shared__ SelectShared<NT> sh;
     __shared__ int s_raw[64], s_blk[64];
     __shared__ int s_bad;
+    grid_dep_wait();                                 // the scores are the previous grid's
 
     const int row = blockIdx.x;
     const int bq = row / p.L;
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(NT) k_select_chunks(SelectParams p) {
     __shared__ SelectShared<NT> sh;
     __shared__ int32_t s_col[kMaxTopk];
     extern __shared__ __align__(16) float s_sc[];
+    grid_dep_wait();
     const int row = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
     const int bq = row / p.L;
     if (!seq_ok(p.key_off, bq, p.Np_max, p.keys_rows)) return;   // the merge flags it
@@ -123,6 +125,7 @@ __global__ void __launch_bounds__(NT) k_select_merge(SelectParams p, int cap) {
     __shared__ SelectShared<NT> sh;
     extern __shared__ __align__(16) float s_sc[];
     int32_t *s_id = reinterpret_cast<int32_t *>(s_sc + cap);
+    grid_dep_wait();
     const int row = blockIdx.x, tid = threadIdx.x;
     const int bq = row / p.L;
     int32_t *out = p.out + (int64_t)row * p.k;
@@ -177,21 +180,21 @@ cudaError_t launch_select(const SelectParams &p, int64_t n_max, cudaStream_t s) 
         const cudaError_t a2 = smem_attr_once<k_select_merge<1024>>((int)kMergeSmem);
         if (a1 != cudaSuccess) return a1;
         if (a2 != cudaSuccess) return a2;
-        k_select_chunks<1024><<<dim3(rows, (unsigned)nchunk), 1024, kChunk * 4, s>>>(p);
-        k_select_merge<1024><<<rows, 1024, (size_t)cap * 8, s>>>(p, cap);
-        return cudaGetLastError();
+        // every select kernel waits before its first global access, so each may be launched
+        // as a programmatic dependent of the kernel before it (the scoring kernel, or the
+        // first level)
+        cudaError_t e = launch_pdl(k_select_chunks<1024>, dim3(rows, (unsigned)nchunk), dim3(1024),
+                                   (size_t)kChunk * 4, s, 1, p);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(k_select_merge<1024>, dim3(rows), dim3(1024), (size_t)cap * 8, s, 1, p, cap);
     }
     SelectParams q = p;
     q.smem_n = n_max <= kSmemSel ? (int)n_max : 0;
     const size_t smem = (size_t)q.smem_n * 4;
-    if (n_max <= 256) {
-        k_select<256><<<rows, 256, smem, s>>>(q);
-    } else {
-        const cudaError_t a = smem_attr_once<k_select<1024>>(kSmemSel * 4);
-        if (a != cudaSuccess) return a;
-        k_select<1024><<<rows, 1024, smem, s>>>(q);
-    }
-    return cudaGetLastError();
+    if (n_max <= 256) return launch_pdl(k_select<256>, dim3(rows), dim3(256), smem, s, 1, q);
+    const cudaError_t a = smem_attr_once<k_select<1024>>(kSmemSel * 4);
+    if (a != cudaSuccess) return a;
+    return launch_pdl(k_select<1024>, dim3(rows), dim3(1024), smem, s, 1, q);
 }
 
 bool chunked_select_fits(int64_t ld, int k) {

@@ -24,8 +24,9 @@
  *    usual chain: hisa_block_filter(_append) -> hisa_select_topk -> hisa_sparse_attend).
  *    Without the flag (flags = 0) a call's kernels start after the previous work on the
  *    stream has completed, as with any ordinary launch, except kernels that read nothing
- *    before the previous grid has completed (the coarse stage's pipeline), which may
- *    always overlap its end.
+ *    before the previous grid has completed (the coarse stage's pipeline, and the selects
+ *    and merges that follow a call's scoring or combine kernel), which may always overlap
+ *    its end.
  *  - Ragged batches: sequence b owns pooled rows [key_off[b], key_off[b+1]) of the
  *    packed key / KV arrays, so Np_b = key_off[b+1] - key_off[b] (int64, device).
  *  - Positions: t0[b] (int32, device) is the absolute token position of query
