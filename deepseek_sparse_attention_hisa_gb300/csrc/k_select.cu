@@ -159,8 +159,11 @@ __global__ void __launch_bounds__(NT) k_select_merge(SelectParams p, int cap) {
         }
     }
     __syncthreads();
-    if (kout > 0)
-        small_topk<NT, 0, 0>(s_sc, m, (int)kout, out, [&](int64_t i) { return s_id[i]; }, sh, p.status);
+    const auto ids = [&](int64_t i) { return s_id[i]; };
+    if (kout > 0 && m <= 8 * NT)
+        small_topk<NT, 0, 0>(s_sc, m, (int)kout, out, ids, sh, p.status);
+    else if (kout > 0)                               // the usual case: the binned form, inlined
+        small_topk_binned_body<NT, 0, 0>(s_sc, m, (int)kout, out, ids, sh, p.status);
     for (int64_t e = kout + tid; e < p.k; e += NT) out[e] = -1;
 }
 

@@ -502,6 +502,9 @@ constexpr int kSmallMax = (kCand - 2 * kSmallCand) * 32;
 template <int NT, int BAR, int TID0, typename Map>
 __device__ __noinline__ void small_topk_binned(const float *sc, int n, int kout, int32_t *out, Map map,
                                                SelectShared<NT> &sh, uint32_t *status);
+template <int NT, int BAR, int TID0, typename Map>
+__device__ __forceinline__ void small_topk_binned_body(const float *sc, int n, int kout, int32_t *out, Map map,
+                                                       SelectShared<NT> &sh, uint32_t *status);
 
 template <int NT, int BAR, int TID0, typename Map>
 __device__ void small_topk(const float *sc, int n, int kout, int32_t *out, Map map,
@@ -516,10 +519,19 @@ __device__ void small_topk(const float *sc, int n, int kout, int32_t *out, Map m
 }
 
 // small_topk's general form (see above): value bins over the range, the threshold bin's
-// candidates ranked exactly, block_topk for anything it does not resolve.
+// candidates ranked exactly, block_topk for anything it does not resolve. Out of line for
+// the kernels whose hot path is fast_topk (their code stays small); a kernel whose main
+// work it is calls the inlined body, where the compiler sees that sc, out's map and sh are
+// shared memory (through a generic pointer each pass ran two to three times slower).
 template <int NT, int BAR, int TID0, typename Map>
 __device__ __noinline__ void small_topk_binned(const float *sc, int n, int kout, int32_t *out, Map map,
                                                SelectShared<NT> &sh, uint32_t *status) {
+    small_topk_binned_body<NT, BAR, TID0>(sc, n, kout, out, map, sh, status);
+}
+
+template <int NT, int BAR, int TID0, typename Map>
+__device__ __forceinline__ void small_topk_binned_body(const float *sc, int n, int kout, int32_t *out, Map map,
+                                                       SelectShared<NT> &sh, uint32_t *status) {
     constexpr int NW = NT / 32, U = 4;
     const int tid = (int)threadIdx.x - TID0, lane = tid & 31, warp = tid >> 5;
     const int seg = ((n + NW * 32 * U - 1) / (NW * 32 * U)) * (32 * U);
