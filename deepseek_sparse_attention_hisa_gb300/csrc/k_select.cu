@@ -194,7 +194,9 @@ cudaError_t launch_select(const SelectParams &p, int64_t n_max, cudaStream_t s) 
     SelectParams q = p;
     q.smem_n = n_max <= kSmemSel ? (int)n_max : 0;
     const size_t smem = (size_t)q.smem_n * 4;
-    if (n_max <= 256) return launch_pdl(k_select<256>, dim3(rows), dim3(256), smem, s, 1, q);
+    // short rows (the coarse stage of many prefill rows): four warps, four columns a thread,
+    // so that sixteen CTAs share an SM
+    if (n_max <= 512) return launch_pdl(k_select<128>, dim3(rows), dim3(128), smem, s, 1, q);
     const cudaError_t a = smem_attr_once<k_select<1024>>(kSmemSel * 4);
     if (a != cudaSuccess) return a;
     return launch_pdl(k_select<1024>, dim3(rows), dim3(1024), smem, s, 1, q);
