@@ -77,11 +77,11 @@ __device__ __forceinline__ void fence_before_sync() {
 __device__ __forceinline__ void fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// generic-proxy shared-memory writes -> visible to the async proxy (tensor core, TMA)
 // Make this thread's generic-proxy global writes visible to later async-proxy (TMA) reads.
 __device__ __forceinline__ void fence_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+// generic-proxy shared-memory writes -> visible to the async proxy (tensor core, TMA)
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -783,6 +783,53 @@ def test_few_sequences_append_filter_select(Np):
     assert np.array_equal(np_(prob.top_blk), tb)
 
 
+@pytest.mark.parametrize("B,L,Np", [(3, 4, (65536, 40000, 65536)), (2, 3, (40000, 38000))],
+                         ids=["1024_blocks", "625_blocks"])
+def test_few_long_coarse_rows_ties_and_masked_tails(B, L, Np):
+    """A few long coarse rows, L = 3 or 4 query rows per sequence (one scoring CTA per row).
+    Sequence 0's blocks from 120 on repeat with period 7, so groups of bit-equal block means
+    run across the whole row and the lowest ids must win; sequence 1 sees all of its blocks;
+    the other rows see about 312 of their blocks, so most of each row is masked. The newest
+    two blocks' means are appended by the coarse call, and a repeated call gives the same
+    kept blocks."""
+    wl = inputs.small_workload(name="few_long_rows", seed=95, B=B, L=L, H_i=64, D_i=128, index_block=64,
+                               index_keep=16, index_topk=512, q_idx_dtype="f32", key_dtype="bf16",
+                               Np=Np, t0=80000, with_attention=False)
+    data = inputs.generate(wl)
+    data["t0"][1] = 4 * Np[1]                         # every block of sequence 1 visible
+    keys, k0 = data["keys"], int(data["key_off"][0])
+    r = np.arange(120 * 64, Np[0])
+    keys[k0 + r] = keys[k0 + 120 * 64 + ((r // 64 - 120) % 7) * 64 + r % 64]
+    prob = Problem(data)
+    nb = np.asarray(Np) // 64
+    cs = torch.full((B * L, int(nb.max())), 7.0, device="cuda")
+    fs = torch.full((B * L, 1024), 7.0, device="cuda")
+    prob.block_means(first_block=np.zeros(B, np.int32))
+    prob.block_filter_append(first_block=torch.as_tensor((nb - 2).astype(np.int32), device="cuda"),
+                             cscores=cs)
+    prob.select_topk(fscores=fs)
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    tb, I, cs, fs = np_(prob.top_blk), np_(prob.I), np_(cs), np_(fs)
+    P.check_block_means(data, np_(prob.means), np_(prob.means_off), 64)
+    for b in range(B):
+        s = P.seq(data, b)
+        for j in range(L):
+            row = b * L + j
+            P.check_coarse(data, b, j, tb[row], cs[row], 64, 16)
+            P.check_fine(data, b, j, tb[row], I[row], fs[row], 64, 512)
+            if b == 0:                                # exact ties: the oracle's set itself
+                V = O.visible_len(s["t0"] + j, wl.r, s["Np"])
+                _, c_top = O.hisa_coarse(data["q_idx"][b, j], data["w"][b, j],
+                                         O.block_means(s["keys"], 64), 16, 64, V)
+                assert set(tb[row].tolist()) == set(c_top.tolist()), f"top_blk[{row}]"
+    prob.top_blk.fill_(-7)
+    prob.block_filter()
+    torch.cuda.synchronize()
+    assert prob.status() == 0
+    assert np.array_equal(np_(prob.top_blk), tb)
+
+
 @pytest.mark.parametrize("case", ["tc_rows", "tc_split", "simt"])
 def test_bf16_output_is_the_f32_output_rounded_once(case):
     """hisa_attn_desc.out_dtype = HISA_BF16: the combine's f32 result rounded to nearest even
