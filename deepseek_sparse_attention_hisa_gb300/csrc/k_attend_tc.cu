@@ -214,6 +214,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
         bool waited = false;                                  // grid_dep_wait() done
         for (int id = blockIdx.x; id < items; id += gridDim.x, ++n) {
             const Item x = item_of(p, id);
+            const __nv_bfloat16 *qrow = reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)x.row * kH * kDH;
+            // the item's q: dims [0, kQT) into the next ring slot (its Full barrier, like a
+            // tile's; the epilogue warps move them into TMEM and free the slot), dims [kQT, 512)
+            // into the q region once the previous item's S products are done with it
+            auto issue_q = [&]() -> bool {
+                const int s = g % kSlots;
+                const bool w = g < (uint32_t)kSlots || wait_bar(&bars[kBarEmpty + s], ((g / kSlots) - 1) & 1, abort);
+                if (!group_all(kBarProd, kProdThreads, w)) return false;
+                const uint32_t slot = sbase + kOffKV + s * kSlotBytes;
+                const int qu = pt & 31;                         // 16-byte unit of dims [0, kQT)
+                for (int h = pt >> 5; h < kH; h += kProdThreads / 32)
+                    cp_async16(slot + (qu >> 3) * kQChunk + sw128_offset(h, (qu & 7) * 8), qrow + h * kDH + qu * 8);
+                cp_async_arrive(&bars[kBarFull + s]);
+                if (pt == 0) mbar_arrive(&bars[kBarFull + s]);
+                ++g;
+                const bool wq = n < 1 || wait_bar(&bars[kBarQFree], (n - 1) & 1, abort);
+                if (!group_all(kBarProd, kProdThreads, wq)) return false;
+                const uint32_t qb = sbase + kOffQ;
+                for (int h = pt >> 5; h < kH; h += kProdThreads / 32)
+                    cp_async16(qb + (qu >> 3) * kQChunk + sw128_offset(h, (qu & 7) * 8),
+                               qrow + h * kDH + kQT + qu * 8);
+                cp_async_arrive(&bars[kBarQ]);
+                return true;
+            };
+            // the first item's q depends on its row alone, so it goes out before anything waits
+            // for the item's metadata loads (item_of): the kernel's start is shorter by one
+            // dependent load
+            if (n == 0 && !issue_q()) { fail(); break; }
             if (x.bad_off && x.split == 0 && pt == 0) flag(p.status, HISA_DEV_BAD_OFFSETS);
             const __nv_bfloat16 *local =
                 reinterpret_cast<const __nv_bfloat16 *>(p.local_kv) + ((int64_t)x.bq * p.W_max + x.lo) * kDH;
@@ -232,32 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attend_tc(AttnParams p) {
                 }
             };
             if (waited) fetch_pre();
-            const __nv_bfloat16 *qrow = reinterpret_cast<const __nv_bfloat16 *>(p.q) + (int64_t)x.row * kH * kDH;
-            {
-                // q dims [0, kQT) into the next ring slot (its Full barrier, like a tile's);
-                // the softmax warps move them into TMEM and free the slot
-                const int s = g % kSlots;
-                const bool w = g < (uint32_t)kSlots || wait_bar(&bars[kBarEmpty + s], ((g / kSlots) - 1) & 1, abort);
-                if (!group_all(kBarProd, kProdThreads, w)) { fail(); break; }
-                const uint32_t slot = sbase + kOffKV + s * kSlotBytes;
-                const int qu = pt & 31;                         // 16-byte unit of dims [0, kQT)
-                for (int h = pt >> 5; h < kH; h += kProdThreads / 32)
-                    cp_async16(slot + (qu >> 3) * kQChunk + sw128_offset(h, (qu & 7) * 8), qrow + h * kDH + qu * 8);
-                cp_async_arrive(&bars[kBarFull + s]);
-                if (pt == 0) mbar_arrive(&bars[kBarFull + s]);
-                ++g;
-            }
-            // q dims [kQT, 512), once the previous item's S products are done with them
-            const bool wq = n < 1 || wait_bar(&bars[kBarQFree], (n - 1) & 1, abort);
-            if (!group_all(kBarProd, kProdThreads, wq)) { fail(); break; }
-            {
-                const uint32_t qb = sbase + kOffQ;
-                const int qu = pt & 31;                         // unit of dims [kQT, 512)
-                for (int h = pt >> 5; h < kH; h += kProdThreads / 32)
-                    cp_async16(qb + (qu >> 3) * kQChunk + sw128_offset(h, (qu & 7) * 8),
-                               qrow + h * kDH + kQT + qu * 8);
-                cp_async_arrive(&bars[kBarQ]);
-            }
+            if (n > 0 && !issue_q()) { fail(); break; }
             // gathers tile i of the item into slot g % kSlots, once that slot is free
             auto issue_tile = [&](int i) -> bool {
                 const int s = g % kSlots;
